@@ -1,0 +1,306 @@
+"""Pins that tie the fp64 oracle to facts outside itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with
+something the page "GPT-OSS on day 0" (section "Kernels for GPT-OSS / Sink
+Attention") or plain mathematics fixes: hand-worked values, the reduction to
+ordinary softmax attention when the sink is -inf (checked against PyTorch's
+fp64 scaled_dot_product_attention), saturation by a huge sink, normalisation,
+closed forms, split-and-merge invariance, arbitrary-precision brute force, the
+page's own online algorithm, paging, head grouping and causal alignment.
+
+The functions look the oracle up at call time (``oracle.<name>``), so the
+mutation test can plant a mistake in the oracle and check that a pin catches it.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from decimal import Decimal, getcontext
+
+import numpy as np
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_floats(rng, shape, std=1.0):
+    """Random values that are exactly representable in bf16 (as float64)."""
+    x = (rng.standard_normal(shape) * std).astype(np.float32)
+    bits = (x.view(np.uint32) + 0x7FFF + ((x.view(np.uint32) >> 16) & 1)) >> 16
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    same_inf = (np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b)))
+    with np.errstate(invalid="ignore"):
+        diff = np.where(same_inf, 0.0, np.abs(a - b))
+    err = float(np.nanmax(diff)) if diff.size else 0.0
+    assert not np.isnan(diff).any() and err <= tol, f"{what}: max abs error {err} > {tol}"
+
+
+# ------------------------------------------------------------------ hand-worked values
+def pin_hand_worked():
+    doc = json.load(open(GOLDEN))
+    for c in doc["cases"]:
+        name = c["name"]
+        if c["op"] == "rows":
+            out, lse = oracle.attention_with_sink(np.array(c["q"]), np.array(c["k"]),
+                                                  np.array(c["v"]), c["sink"], c["sm_scale"])
+        elif c["op"] == "prefill_paged":
+            out, lse = oracle.prefill_paged(np.array(c["q"]), np.array(c["k_pages"]),
+                                            np.array(c["v_pages"]), np.array(c["page_table"]),
+                                            np.array(c["cu_seqlens_q"]), np.array(c["kv_lens"]),
+                                            np.array(c["sinks"]), c["sm_scale"], causal=True)
+        else:
+            args = (np.array(c["q"]), np.array(c["k_pages"]), np.array(c["v_pages"]),
+                    np.array(c["page_table"]), np.array(c["kv_lens"]), np.array(c["sinks"]),
+                    c["sm_scale"])
+            out, lse = oracle.decode(*args, num_splits=1)
+            po, pl = oracle.decode(*args, num_splits=2)
+            _close(po, c["split2_out"], 1e-14, name + " split o")
+            _close(pl, c["split2_lse"], 1e-14, name + " split lse")
+            _, pl3 = oracle.decode(*args, num_splits=3)
+            _close(pl3, c["split3_lse"], 1e-14, name + " 3-split lse")
+            mo, ml = oracle.merge(po, pl)
+            _close(mo, c["out"], 1e-14, name + " merged o")
+            _close(ml, c["lse"], 1e-14, name + " merged lse")
+        _close(out, c["out"], 1e-14, name + " out")
+        _close(lse, c["lse"], 1e-14, name + " lse")
+
+
+# ------------------------------------------------------------------ reduction to SDPA
+def _sdpa_reference(q, k, v, sm_scale, mask):
+    import torch
+    qt = torch.from_numpy(q).permute(1, 0, 2)[None]          # [1, H, n, D]
+    kt = torch.from_numpy(k).permute(1, 0, 2)[None]
+    vt = torch.from_numpy(v).permute(1, 0, 2)[None]
+    g = qt.shape[1] // kt.shape[1]
+    kt = kt.repeat_interleave(g, dim=1)
+    vt = vt.repeat_interleave(g, dim=1)
+    m = torch.from_numpy(mask)[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m, scale=sm_scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+def pin_sdpa_reduction():
+    """sink = -inf removes the sink column: ordinary (causal or full) GQA attention."""
+    rng = _rng(11)
+    hq, hkv, d = 4, 2, 8
+    for causal in (True, False):
+        lens = [5, 17, 1, 33]
+        cu = workloads.cu_seqlens_from(lens)
+        t = int(cu[-1])
+        q, k, v = (_bf16_floats(rng, (t, h, d)) for h in (hq, hkv, hkv))
+        sinks = np.full(hq, -np.inf)
+        out, _ = oracle.prefill(q, k, v, sinks, cu, 0.3, causal)
+        for b in range(len(lens)):
+            lo, hi = int(cu[b]), int(cu[b + 1])
+            n = hi - lo
+            mask = np.tril(np.ones((n, n), dtype=bool)) if causal else np.ones((n, n), dtype=bool)
+            ref = _sdpa_reference(q[lo:hi], k[lo:hi], v[lo:hi], 0.3, mask)
+            _close(out[lo:hi], ref, 1e-12, f"sdpa prefill causal={causal} b={b}")
+    # paged, q_len < kv_len: bottom-right causal alignment against an explicit mask
+    q_lens, kv_lens = [3, 1, 20], [7, 9, 20]
+    data = workloads.make_mixed(5, q_lens, kv_lens, hq, hkv, d, page_size=16)
+    data["sinks"] = np.full(hq, -np.inf)
+    out, _ = oracle.prefill_paged(data["q"], data["k_pages"], data["v_pages"], data["page_table"],
+                                  data["cu_seqlens_q"], data["kv_lens"], data["sinks"], 0.125, True)
+    cu = data["cu_seqlens_q"]
+    for b, (ql, kl) in enumerate(zip(q_lens, kv_lens)):
+        kb = oracle.widen_bf16(np.stack([data["k_pages"][data["page_table"][b][j // 16], :, j % 16]
+                                         for j in range(kl)]))
+        vb = oracle.widen_bf16(np.stack([data["v_pages"][data["page_table"][b][j // 16], :, j % 16]
+                                         for j in range(kl)]))
+        qb = oracle.widen_bf16(data["q"][cu[b]:cu[b + 1]])
+        mask = np.zeros((ql, kl), dtype=bool)
+        for i in range(ql):
+            mask[i, : kl - ql + i + 1] = True
+        ref = _sdpa_reference(qb, kb, vb, 0.125, mask)
+        _close(out[cu[b]:cu[b + 1]], ref, 1e-12, f"sdpa paged b={b}")
+
+
+# ------------------------------------------------------------------ limits and invariants
+def pin_large_sink_saturates():
+    rng = _rng(12)
+    q, k, v = _bf16_floats(rng, (6, 16)), _bf16_floats(rng, (40, 16)), _bf16_floats(rng, (40, 16))
+    out, lse = oracle.attention_with_sink(q, k, v, 1.0e4, 0.25)
+    assert np.all(out == 0.0), "a sink of 1e4 must take all the probability"
+    assert np.all(lse == 1.0e4), f"lse must equal the sink, got {lse}"
+
+
+def pin_normalisation():
+    rng = _rng(13)
+    for sink in (-3.0, 0.0, 2.5, -np.inf):
+        q, k, v = _bf16_floats(rng, (9, 32)), _bf16_floats(rng, (50, 32)), _bf16_floats(rng, (50, 32))
+        vis = oracle.visible_keys(9, 50, True)
+        _, _, p, ps = oracle.attention_with_sink(q, k, v, sink, 0.2, vis, return_probs=True)
+        tot = p.sum(axis=1) + ps
+        assert np.all(np.abs(tot - 1.0) <= 1e-15 * 64), f"sum p + p_sink != 1: {tot}"
+        assert np.all(p[~vis] == 0.0), "masked keys must get zero probability"
+        if sink == -np.inf:
+            assert np.all(ps == 0.0)
+
+
+def pin_single_key_closed_form():
+    """kv_len = 1: out = sigmoid(s0 - sink) v0, lse = log(e^s0 + e^sink)."""
+    rng = _rng(14)
+    for sink in (-2.0, 0.0, 0.7, 5.0):
+        q, k, v = _bf16_floats(rng, (3, 8)), _bf16_floats(rng, (1, 8)), _bf16_floats(rng, (1, 8))
+        s0 = 0.5 * (q @ k[0])
+        out, lse = oracle.attention_with_sink(q, k, v, sink, 0.5)
+        sig = 1.0 / (1.0 + np.exp(-(s0 - sink)))
+        _close(out, sig[:, None] * v[0][None], 1e-14, "single key out")
+        _close(lse, np.logaddexp(s0, sink), 1e-14, "single key lse")
+
+
+def pin_identical_keys():
+    """n equal keys with logit x: out = n e^x / (e^sink + n e^x) * mean(v)."""
+    rng = _rng(15)
+    n, d = 25, 8
+    q = _bf16_floats(rng, (1, d))
+    k = np.repeat(_bf16_floats(rng, (1, d)), n, axis=0)
+    v = _bf16_floats(rng, (n, d))
+    x = float(0.125 * (q[0] @ k[0]))
+    for sink in (-1.0, 0.0, 3.0):
+        out, lse = oracle.attention_with_sink(q, k, v, sink, 0.125)
+        w = n * math.exp(x) / (math.exp(sink) + n * math.exp(x))
+        _close(out[0], w * v.mean(axis=0), 1e-13, "identical keys out")
+        _close(lse[0], math.log(math.exp(sink) + n * math.exp(x)), 1e-13, "identical keys lse")
+
+
+def pin_split_merge_invariance():
+    """Splitting the KV range (sink in split 0 only) and merging equals the unsplit row."""
+    kv_lens = [1, 15, 16, 17, 100, 257, 600]
+    data = workloads.make_decode(21, kv_lens, 8, 2, 16, page_size=16)
+    args = (data["q"], data["k_pages"], data["v_pages"], data["page_table"], data["kv_lens"],
+            data["sinks"], 0.25)
+    ref_o, ref_l = oracle.decode(*args, num_splits=1)
+    for s in list(range(1, 9)) + [32]:
+        po, pl = oracle.decode(*args, num_splits=s)
+        if s == 1:
+            po, pl = po[:, None], pl[:, None]
+        mo, ml = oracle.merge(po, pl)
+        _close(mo, ref_o, 1e-12, f"split {s} out")
+        _close(ml, ref_l, 1e-12, f"split {s} lse")
+
+
+def pin_brute_force_decimal():
+    """Tiny cases enumerated with 50-digit decimals, without max subtraction."""
+    getcontext().prec = 50
+    rng = _rng(16)
+    for trial in range(6):
+        q_len = int(rng.integers(1, 5))
+        kv_len = int(rng.integers(q_len, 5))
+        d = int(rng.integers(1, 5))
+        q, k, v = (_bf16_floats(rng, (n, d)) for n in (q_len, kv_len, kv_len))
+        sink = float(_bf16_floats(rng, (1,))[0]) if trial != 5 else -np.inf
+        scale = 0.5
+        vis = oracle.visible_keys(q_len, kv_len, True)
+        out, lse = oracle.attention_with_sink(q, k, v, sink, scale, vis)
+        for i in range(q_len):
+            terms = []
+            for j in range(kv_len):
+                if j <= i + kv_len - q_len:
+                    s = Decimal(scale) * sum(Decimal(q[i, t]) * Decimal(k[j, t]) for t in range(d))
+                    terms.append((j, s.exp()))
+            z = sum(e for _, e in terms) + (Decimal(sink).exp() if sink != -np.inf else Decimal(0))
+            exp_out = [float(sum(e * Decimal(v[j, t]) for j, e in terms) / z) for t in range(d)]
+            _close(out[i], exp_out, 1e-12, f"brute force out trial {trial} row {i}")
+            _close(lse[i], float(z.ln()), 1e-12, f"brute force lse trial {trial} row {i}")
+
+
+def pin_online_algorithm():
+    """The page's online algorithm (m seeded with the sink, d with 1) reaches the definition."""
+    rng = _rng(17)
+    for sink in (-1.5, 0.0, 4.0, -np.inf):
+        q, k, v = _bf16_floats(rng, (64,)), _bf16_floats(rng, (300, 64)), _bf16_floats(rng, (300, 64))
+        ref_o, ref_l = oracle.attention_with_sink(q[None], k, v, sink, 0.125)
+        for block in (1, 7, 16, 128, 512):
+            o, l = oracle.online_sink_attention(q, k, v, sink, 0.125, block)
+            _close(o, ref_o[0], 1e-13, f"online out block={block} sink={sink}")
+            _close(l, ref_l[0], 1e-13, f"online lse block={block} sink={sink}")
+
+
+def pin_paging():
+    """Gathering through a permuted page table returns the logical tokens, byte for byte."""
+    rng = _rng(18)
+    kv_lens = [3, 16, 47]
+    logical = [rng.integers(0, 1 << 16, (n, 2, 4), dtype=np.uint16) for n in kv_lens]
+    table, num_pages = workloads.page_layout(3, kv_lens, 16, permute=True)
+    pages = np.zeros((num_pages, 2, 16, 4), dtype=np.uint16)
+    for b, n in enumerate(kv_lens):
+        for j in range(n):
+            pages[table[b, j // 16], :, j % 16] = logical[b][j]
+    for b, n in enumerate(kv_lens):
+        got = oracle.gather_pages(pages, table[b], n)
+        assert got.dtype == np.uint16 and np.array_equal(got, logical[b]), f"gather b={b}"
+    # the same logical KV under two permutations gives identical oracle results
+    data1 = workloads.make_decode(4, kv_lens, 4, 2, 4, permute=False)
+    t2, _ = workloads.page_layout(99, kv_lens, 16, permute=True)
+    k2 = np.zeros_like(data1["k_pages"])
+    v2 = np.zeros_like(data1["v_pages"])
+    for b, n in enumerate(kv_lens):
+        for j in range((n + 15) // 16):
+            k2[t2[b, j]] = data1["k_pages"][data1["page_table"][b, j]]
+            v2[t2[b, j]] = data1["v_pages"][data1["page_table"][b, j]]
+    a = oracle.decode(data1["q"], data1["k_pages"], data1["v_pages"], data1["page_table"],
+                      data1["kv_lens"], data1["sinks"], 0.5)
+    bb = oracle.decode(data1["q"], k2, v2, t2, data1["kv_lens"], data1["sinks"], 0.5)
+    assert np.array_equal(a[0], bb[0]) and np.array_equal(a[1], bb[1])
+
+
+def pin_gqa_mapping():
+    """Query head h reads KV head h // G: with V constant (g + 1) on KV head g,
+    out[h] = (1 - p_sink[h]) * (h // G + 1)."""
+    rng = _rng(19)
+    hq, hkv, d, n = 8, 4, 4, 10
+    q = _bf16_floats(rng, (n, hq, d))
+    k = _bf16_floats(rng, (n, hkv, d))
+    v = np.zeros((n, hkv, d))
+    for g in range(hkv):
+        v[:, g, :] = g + 1.0
+    sinks = _bf16_floats(rng, (hq,))
+    cu = np.array([0, n])
+    out, lse = oracle.prefill(q, k, v, sinks, cu, 0.5, True)
+    p_sink = np.exp(sinks[None, :] - lse)
+    for h in range(hq):
+        exp = (1.0 - p_sink[:, h])[:, None] * (h // (hq // hkv) + 1.0)
+        _close(out[:, h], np.broadcast_to(exp, (n, d)), 1e-13, f"gqa head {h}")
+
+
+def pin_causal_counts():
+    """Bottom-right causal: query i of q_len new tokens sees kv_len - q_len + i + 1 keys."""
+    rng = _rng(20)
+    for q_len, kv_len in ((1, 9), (4, 4), (5, 12)):
+        q, k, v = (_bf16_floats(rng, (n, 8)) for n in (q_len, kv_len, kv_len))
+        vis = oracle.visible_keys(q_len, kv_len, True)
+        _, _, p, _ = oracle.attention_with_sink(q, k, v, 0.0, 0.5, vis, return_probs=True)
+        for i in range(q_len):
+            assert int((p[i] > 0).sum()) == kv_len - q_len + i + 1, (q_len, kv_len, i)
+
+
+ALL_PINS = [pin_hand_worked, pin_sdpa_reduction, pin_large_sink_saturates, pin_normalisation,
+            pin_single_key_closed_form, pin_identical_keys, pin_split_merge_invariance,
+            pin_brute_force_decimal, pin_online_algorithm, pin_paging, pin_gqa_mapping,
+            pin_causal_counts]
+
+
+def failing_pins():
+    """Names of the pins that fail against the oracle as it currently is."""
+    bad = []
+    for pin in ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, IndexError, ValueError, FloatingPointError):
+            bad.append(pin.__name__)
+    return bad

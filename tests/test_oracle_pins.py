@@ -1,0 +1,106 @@
+"""The fp64 oracle against its pins, and plausible mistakes planted in it.
+
+CPU only.  The pins are in ``oracle_pins.py``; each must pass on the oracle as
+written, and each planted mistake (a mutant of the oracle, made on the CPU)
+must make at least one pin fail.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def _mut_attention(transform):
+    orig = oracle.attention_with_sink
+
+    def mutant(q, k, v, sink, sm_scale, visible=None, with_sink=True, return_probs=False):
+        return transform(orig, q, k, v, sink, sm_scale, visible, with_sink, return_probs)
+    return mutant
+
+
+def _sink_scaled(orig, q, k, v, sink, sm_scale, visible, with_sink, rp):
+    return orig(q, k, v, sink * sm_scale, sm_scale, visible, with_sink, rp)
+
+
+def _sink_dropped(orig, q, k, v, sink, sm_scale, visible, with_sink, rp):
+    return orig(q, k, v, sink, sm_scale, visible, False, rp)
+
+
+def _sink_in_every_split(orig, q, k, v, sink, sm_scale, visible, with_sink, rp):
+    return orig(q, k, v, sink, sm_scale, visible, True, rp)
+
+
+def _sink_has_value_row(orig, q, k, v, sink, sm_scale, visible, with_sink, rp):
+    out, lse, p, ps = orig(q, k, v, sink, sm_scale, visible, with_sink, True)
+    out = out + ps[:, None]
+    return (out, lse, p, ps) if rp else (out, lse)
+
+
+def _lse_log2(orig, q, k, v, sink, sm_scale, visible, with_sink, rp):
+    res = orig(q, k, v, sink, sm_scale, visible, with_sink, rp)
+    return (res[0], res[1] / math.log(2)) + tuple(res[2:])
+
+
+def _top_left_causal(q_len, kv_len, causal):
+    vis = np.ones((q_len, kv_len), dtype=bool)
+    if causal:
+        vis = np.arange(kv_len)[None, :] <= np.arange(q_len)[:, None]
+    return vis
+
+
+def _gqa_modulo(h, hq, hkv):
+    return h % hkv
+
+
+def _split_drops_last_token(kv_len, page_size, num_splits):
+    return [(a, max(a, b - 1) if b == kv_len and b > a else b)
+            for a, b in _ORIG_SPLITS(kv_len, page_size, num_splits)]
+
+
+_ORIG_SPLITS = oracle.split_token_ranges
+
+
+def _online_d_starts_at_zero(q, k, v, sink, sm_scale, block):
+    # the page's running denominator starts at 1 for the sink; this mutant forgets it
+    q = np.asarray(q, dtype=np.float64)
+    m, d, acc = float(sink), 0.0, np.zeros(np.asarray(v).shape[1])
+    for start in range(0, len(k), block):
+        s = sm_scale * (np.asarray(k[start:start + block]) @ q)
+        m_new = max(m, float(s.max()))
+        c = math.exp(m - m_new) if m != -math.inf else 0.0
+        w = np.exp(s - m_new)
+        d, acc, m = d * c + w.sum(), acc * c + w @ v[start:start + block], m_new
+    return acc / d, m + math.log(d)
+
+
+MUTANTS = {
+    "sink_scaled_by_sm_scale": ("attention_with_sink", _mut_attention(_sink_scaled)),
+    "sink_dropped": ("attention_with_sink", _mut_attention(_sink_dropped)),
+    "sink_in_every_split": ("attention_with_sink", _mut_attention(_sink_in_every_split)),
+    "sink_has_value_row": ("attention_with_sink", _mut_attention(_sink_has_value_row)),
+    "lse_in_log2": ("attention_with_sink", _mut_attention(_lse_log2)),
+    "top_left_causal": ("visible_keys", _top_left_causal),
+    "gqa_modulo": ("kv_head_of", _gqa_modulo),
+    "split_drops_last_token": ("split_token_ranges", _split_drops_last_token),
+    "online_d_starts_at_zero": ("online_sink_attention", _online_d_starts_at_zero),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(oracle, attr, fn)
+    failing = oracle_pins.failing_pins()
+    assert failing, f"no pin catches the planted mistake {name}"
+
+
+def test_pins_pass_unmutated():
+    assert oracle_pins.failing_pins() == []
