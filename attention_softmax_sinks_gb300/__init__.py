@@ -1,0 +1,235 @@
+"""GQA attention with per-head softmax sinks on GB300 (sm_103a).
+
+Thin ctypes binding of ``libsinkattn.so`` (C ABI in ``include/sink_attn.h``).
+Every function below only marshals arguments: it reads shapes off the torch
+tensors, allocates outputs when none are given, passes raw device pointers
+and the current CUDA stream, and turns a non-zero status into an exception.
+All arithmetic runs in the library's CUDA kernels; there is no fallback.
+
+The operation (page "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink
+Attention"): ``attn = softmax(q k^T * sm_scale + sink) V`` where each query
+head's sink is one extra softmax logit that carries no value row.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "SinkAttnError", "library_path", "load_library", "sink_attn_prefill", "sink_attn_prefill_paged",
+    "sink_attn_decode", "sink_attn_merge", "sink_attn_decode_splits", "sink_attn_device_status",
+    "sink_attn_set_wait_timeout_ns", "sink_attn_status_string", "sink_attn_abi_version",
+    "sink_attn_selftest_wait_timeout", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libsinkattn.so")
+_lib = None
+
+EXPORTED_SYMBOLS = (
+    "sink_attn_prefill", "sink_attn_prefill_paged", "sink_attn_decode", "sink_attn_merge",
+    "sink_attn_decode_splits", "sink_attn_device_status", "sink_attn_set_wait_timeout_ns",
+    "sink_attn_status_string", "sink_attn_abi_version", "sink_attn_selftest_wait_timeout",
+)
+
+_p, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_SIGNATURES = {
+    "sink_attn_prefill": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p, _p]),
+    "sink_attn_prefill_paged": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                     _f, _i, _p, _p, _p]),
+    "sink_attn_decode": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p, _p]),
+    "sink_attn_merge": (_i, [_p, _p, _i, _i, _i, _i, _p, _p, _p]),
+    "sink_attn_decode_splits": (_i, [_i, _i, _i, _i, _i]),
+    "sink_attn_device_status": (_i, [_i]),
+    "sink_attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
+    "sink_attn_status_string": (ctypes.c_char_p, [_i]),
+    "sink_attn_abi_version": (_i, []),
+    "sink_attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _p]),
+}
+
+
+class SinkAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({_status_text(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libsinkattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m attention_softmax_sinks_gb300._build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load_library().sink_attn_status_string(status).decode()
+    except Exception:  # library missing: still produce a message
+        return "unknown"
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise SinkAttnError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ----------------------------------------------------------------------------- entry points
+def sink_attn_prefill(q, k, v, sinks, cu_seqlens, max_seqlen: int, sm_scale: float,
+                      causal: bool = True, out=None, lse=None, return_lse: bool = True,
+                      stream=None):
+    """Prefill over contiguous ragged sequences (q_len == kv_len).
+
+    q [T, Hq, 64] bf16, k/v [T, Hkv, 64] bf16, sinks [Hq] fp32, cu_seqlens [B+1] int32.
+    Returns (out [T, Hq, 64] bf16, lse [T, Hq] fp32 or None).
+    """
+    _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16)
+    _dev(sinks, "sinks", torch.float32), _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    t, hq, d = q.shape
+    hkv = k.shape[1]
+    if k.shape != (t, hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [T, Hkv, D] with q's T and D")
+    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((t, hq), dtype=torch.float32, device=q.device)
+    st = load_library().sink_attn_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), cu_seqlens.numel() - 1, t,
+        int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
+        _stream(stream))
+    _check(st, "sink_attn_prefill")
+    return out, lse
+
+
+def sink_attn_prefill_paged(q, paged_k, paged_v, page_table, cu_seqlens_q, kv_lens, sinks,
+                            max_q_len: int, sm_scale: float, causal: bool = True, out=None,
+                            lse=None, return_lse: bool = True, stream=None):
+    """New tokens of a mixed batch against a paged cache (bottom-right causal).
+
+    q [Tq, Hq, 64] bf16, paged_k/v [P, Hkv, 16, 64] bf16, page_table [B, max_pages] int32,
+    cu_seqlens_q [B+1] int32, kv_lens [B] int32, sinks [Hq] fp32.
+    """
+    for name, tns, dt in (("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
+                          ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
+                          ("cu_seqlens_q", cu_seqlens_q, torch.int32), ("kv_lens", kv_lens, torch.int32),
+                          ("sinks", sinks, torch.float32)):
+        _dev(tns, name, dt)
+    t, hq, d = q.shape
+    num_pages, hkv, page_size, _ = paged_k.shape
+    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((t, hq), dtype=torch.float32, device=q.device)
+    st = load_library().sink_attn_prefill_paged(
+        _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(cu_seqlens_q), _ptr(kv_lens),
+        _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq, hkv, d, page_size,
+        page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
+        _stream(stream))
+    _check(st, "sink_attn_prefill_paged")
+    return out, lse
+
+
+def sink_attn_decode(q, paged_k, paged_v, page_table, kv_lens, sinks, sm_scale: float,
+                     num_splits: int = 1, out=None, lse=None, return_lse: bool = True, stream=None):
+    """One new token per sequence against a paged cache.
+
+    num_splits == 1: returns (out [B, Hq, 64] bf16, lse [B, Hq] fp32).
+    num_splits > 1: returns the partials (o [B, S, Hq, 64] fp32, lse [B, S, Hq] fp32)
+    for sink_attn_merge.
+    """
+    for name, tns, dt in (("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
+                          ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
+                          ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)):
+        _dev(tns, name, dt)
+    b, hq, d = q.shape
+    num_pages, hkv, page_size, _ = paged_k.shape
+    s = int(num_splits)
+    if out is None:
+        out = (torch.empty_like(q) if s == 1 else
+               torch.empty((b, s, hq, d), dtype=torch.float32, device=q.device))
+    if lse is None and (return_lse or s > 1):
+        shape = (b, hq) if s == 1 else (b, s, hq)
+        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+    st = load_library().sink_attn_decode(
+        _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
+        hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), s, _ptr(out), _ptr(lse),
+        _stream(stream))
+    _check(st, "sink_attn_decode")
+    return out, lse
+
+
+def sink_attn_merge(partial_o, partial_lse, out=None, lse=None, return_lse: bool = True,
+                    stream=None):
+    """Merge split partials o [B, S, H, 64] fp32 / lse [B, S, H] fp32 -> (out bf16, lse fp32)."""
+    _dev(partial_o, "partial_o", torch.float32), _dev(partial_lse, "partial_lse", torch.float32)
+    b, s, h, d = partial_o.shape
+    out = (torch.empty((b, h, d), dtype=torch.bfloat16, device=partial_o.device) if out is None
+           else _dev(out, "out", torch.bfloat16))
+    if lse is None and return_lse:
+        lse = torch.empty((b, h), dtype=torch.float32, device=partial_o.device)
+    st = load_library().sink_attn_merge(_ptr(partial_o), _ptr(partial_lse), b, s, h, d, _ptr(out),
+                                        _ptr(lse), _stream(stream))
+    _check(st, "sink_attn_merge")
+    return out, lse
+
+
+def sink_attn_decode_splits(batch: int, num_kv_heads: int, max_kv_len: int, page_size: int = 16,
+                            num_sms: int = 0) -> int:
+    if num_sms <= 0 and torch.cuda.is_available():
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return load_library().sink_attn_decode_splits(batch, num_kv_heads, max_kv_len, page_size, num_sms)
+
+
+def sink_attn_device_status(clear: bool = True) -> int:
+    """Status word of the current device (synchronises); 0 when clean."""
+    return load_library().sink_attn_device_status(int(bool(clear)))
+
+
+def sink_attn_set_wait_timeout_ns(ns: int) -> None:
+    load_library().sink_attn_set_wait_timeout_ns(int(ns))
+
+
+def sink_attn_status_string(status: int) -> str:
+    return load_library().sink_attn_status_string(int(status)).decode()
+
+
+def sink_attn_abi_version() -> int:
+    return load_library().sink_attn_abi_version()
+
+
+def sink_attn_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) -> None:
+    """Launch the bounded-wait diagnostic (records SA_ERR_TIMEOUT in the status word)."""
+    _check(load_library().sink_attn_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
+           "sink_attn_selftest_wait_timeout")

@@ -1,0 +1,304 @@
+// C-ABI entry points of libsinkattn.so (declared in include/sink_attn.h):
+// argument validation, the per-device status word, TMA descriptor encoding
+// and the launches.  No allocation, no synchronisation (except the explicit
+// status read-back).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sink_attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+// Bits set by the kernels (see ptx.cuh); one word per device.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned* g_status_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+unsigned long long g_timeout_ns = 2000000000ull;
+
+sa_status cuda_fail() { return SA_ERR_CUDA; }
+
+// Device address of this device's status word (host code must not use the
+// symbol directly).  Looked up once per device.
+sa_status status_ptr(unsigned** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_fail();
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return cuda_fail();
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return SA_OK;
+}
+
+sa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return cuda_fail();
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *fn = g_encode;
+  return SA_OK;
+}
+
+// [rows, heads, 64] bf16 tensor read in boxes of (box_rows tokens, 1 head, 64 dims).
+sa_status map_tokens_heads(CUtensorMap* m, const void* base, long long rows, int heads,
+                           int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (sa_status s = encoder(&enc)) return s;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(heads) * 64 * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SA_OK : SA_ERR_CUDA;
+}
+
+// Paged cache [num_pages, hkv, 16, 64] viewed as [num_pages*hkv*16, 64] rows,
+// one box = one (page, kv head) = 16 rows.
+sa_status map_pages(CUtensorMap* m, const void* base, int num_pages, int hkv) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (sa_status s = encoder(&enc)) return s;
+  cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(num_pages) * hkv * sa::kPageSize};
+  cuuint64_t strides[1] = {64 * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(sa::kPageSize)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SA_OK : SA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool good_scale(float s) { return std::isfinite(s) && s > 0.0f; }
+
+sa_status check_heads(int hq, int hkv, int head_dim) {
+  if (hq <= 0 || hkv <= 0) return SA_ERR_SHAPE;
+  if (head_dim != sa::kHeadDim) return SA_ERR_UNSUPPORTED;
+  if (hq % hkv != 0) return SA_ERR_SHAPE;
+  if (hq / hkv > 16) return SA_ERR_UNSUPPORTED;
+  return SA_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// One warp waits on a barrier that nothing will ever complete, with the same
+// bounded wait the attention kernels use, and reports the timeout.
+__global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    sa::mbar_init(sa::smem_u32(&bar), 1);
+    sa::fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !sa::mbar_wait(sa::smem_u32(&bar), 0, timeout_ns))
+    sa::raise_status(status, sa::kStatusTimeout);
+}
+
+}  // namespace
+
+extern "C" {
+
+int sink_attn_abi_version(void) { return 1; }
+
+const char* sink_attn_status_string(sa_status s) {
+  switch (s) {
+    case SA_OK: return "ok";
+    case SA_ERR_NULL: return "a required pointer is NULL";
+    case SA_ERR_SHAPE: return "inconsistent or out-of-range sizes or sm_scale";
+    case SA_ERR_UNSUPPORTED: return "unsupported configuration (head_dim 64, page_size 16, group <= 16)";
+    case SA_ERR_LAUNCH: return "kernel launch failed";
+    case SA_ERR_BOUNDS: return "device saw an out-of-range page id or length";
+    case SA_ERR_TIMEOUT: return "a device-side wait ran out of time";
+    case SA_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
+    case SA_ERR_CUDA: return "a CUDA runtime call failed";
+  }
+  return "unknown status";
+}
+
+void sink_attn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns; }
+
+sa_status sink_attn_selftest_wait_timeout(unsigned long long timeout_ns, cudaStream_t stream) {
+  if (timeout_ns > 1000000000ull) timeout_ns = 1000000000ull;
+  unsigned* st = nullptr;
+  if (sa_status s = status_ptr(&st)) return s;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(st, timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
+sa_status sink_attn_device_status(int clear) {
+  unsigned* p = nullptr;
+  if (sa_status s = status_ptr(&p)) return s;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_fail();
+  if (clear && word) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return cuda_fail();
+  }
+  if (word & sa::kStatusTimeout) return SA_ERR_TIMEOUT;
+  if (word & (sa::kStatusBadPage | sa::kStatusBadLen)) return SA_ERR_BOUNDS;
+  return SA_OK;
+}
+
+int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int page_size,
+                            int num_sms) {
+  if (batch <= 0 || num_kv_heads <= 0 || max_kv_len <= 0 || page_size <= 0) return 1;
+  if (num_sms <= 0) num_sms = 152;
+  const long long units = static_cast<long long>(batch) * num_kv_heads;
+  const long long pages = (max_kv_len + page_size - 1) / page_size;
+  const long long slots = 3LL * num_sms;  // resident decode CTAs per GPU
+  long long s = (4 * slots + units - 1) / units;  // about four waves of CTAs
+  const long long max_by_pages = pages / 16 > 0 ? pages / 16 : 1;  // >= 16 pages per split
+  if (s > max_by_pages) s = max_by_pages;
+  if (s < 1) s = 1;
+  if (s > 256) s = 256;
+  return static_cast<int>(s);
+}
+
+sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged_v,
+                           const int32_t* page_table, const int32_t* kv_lens, const float* sinks,
+                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                           int page_size, int max_pages, int num_pages, float sm_scale,
+                           int num_splits, void* out, float* lse, cudaStream_t stream) {
+  if (!q || !paged_k || !paged_v || !page_table || !kv_lens || !sinks || !out) return SA_ERR_NULL;
+  if (num_splits > 1 && !lse) return SA_ERR_NULL;
+  if (batch < 0 || max_pages <= 0 || num_pages <= 0) return SA_ERR_SHAPE;
+  if (num_splits < 1 || num_splits > 256) return SA_ERR_SHAPE;
+  if (sa_status s = check_heads(num_qo_heads, num_kv_heads, head_dim)) return s;
+  if (page_size != sa::kPageSize) return SA_ERR_UNSUPPORTED;
+  if (!good_scale(sm_scale)) return SA_ERR_SHAPE;
+  if (static_cast<long long>(num_pages) * num_kv_heads * page_size >= (1LL << 31)) return SA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(paged_k) || !aligned16(paged_v) || !aligned16(out))
+    return SA_ERR_ALIGNMENT;
+  if (batch > 65535) return SA_ERR_SHAPE;
+  if (batch == 0) return SA_OK;
+  sa::DecodeArgs a{};
+  a.q = q;
+  a.page_table = page_table;
+  a.kv_lens = kv_lens;
+  a.sinks = sinks;
+  a.out = out;
+  a.lse = lse;
+  a.batch = batch;
+  a.hq = num_qo_heads;
+  a.hkv = num_kv_heads;
+  a.group = num_qo_heads / num_kv_heads;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.num_splits = num_splits;
+  a.scale_log2 = sm_scale * kLog2e;
+  a.timeout_ns = g_timeout_ns;
+  if (sa_status s = status_ptr(&a.status)) return s;
+  CUtensorMap km, vm;
+  if (sa_status s = map_pages(&km, paged_k, num_pages, num_kv_heads)) return s;
+  if (sa_status s = map_pages(&vm, paged_v, num_pages, num_kv_heads)) return s;
+  return sa::launch_decode(km, vm, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
+sa_status sink_attn_merge(const float* partial_o, const float* partial_lse, int batch,
+                          int num_splits, int num_heads, int head_dim, void* out, float* lse_out,
+                          cudaStream_t stream) {
+  if (!partial_o || !partial_lse || !out) return SA_ERR_NULL;
+  if (batch < 0 || num_heads <= 0 || num_splits < 1) return SA_ERR_SHAPE;
+  if (head_dim != sa::kHeadDim) return SA_ERR_UNSUPPORTED;
+  if (!aligned16(partial_o) || !aligned16(out)) return SA_ERR_ALIGNMENT;
+  if (static_cast<long long>(batch) * num_heads >= (1LL << 31)) return SA_ERR_SHAPE;
+  if (batch == 0) return SA_OK;
+  sa::MergeArgs a{partial_o, partial_lse, out, lse_out, batch, num_splits, num_heads};
+  return sa::launch_merge(a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
+static sa_status prefill_common(const void* q, const void* k, const void* v,
+                                const int32_t* page_table, const int32_t* cu_q,
+                                const int32_t* kv_lens, const float* sinks, int batch,
+                                int total_q, int max_q, int hq, int hkv, int head_dim,
+                                int max_pages, int num_pages, float sm_scale, int causal,
+                                void* out, float* lse, cudaStream_t stream, bool paged) {
+  if (!q || !k || !v || !cu_q || !sinks || !out) return SA_ERR_NULL;
+  if (paged && (!page_table || !kv_lens)) return SA_ERR_NULL;
+  if (batch < 0 || total_q < 0 || max_q < 0) return SA_ERR_SHAPE;
+  if (sa_status s = check_heads(hq, hkv, head_dim)) return s;
+  if (!good_scale(sm_scale)) return SA_ERR_SHAPE;
+  if (paged && (max_pages <= 0 || num_pages <= 0)) return SA_ERR_SHAPE;
+  if (paged && static_cast<long long>(num_pages) * hkv * sa::kPageSize >= (1LL << 31)) return SA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SA_ERR_ALIGNMENT;
+  if (batch == 0 || total_q == 0 || max_q == 0) return SA_OK;
+  if (static_cast<long long>(total_q) >= (1LL << 31) - 256) return SA_ERR_SHAPE;
+  sa::PrefillArgs a{};
+  a.q = q;
+  a.cu_q = cu_q;
+  a.kv_lens = paged ? kv_lens : nullptr;
+  a.page_table = paged ? page_table : nullptr;
+  a.sinks = sinks;
+  a.out = out;
+  a.lse = lse;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.max_q = max_q;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.group = hq / hkv;
+  a.max_pages = paged ? max_pages : 0;
+  a.num_pages = paged ? num_pages : 0;
+  a.causal = causal ? 1 : 0;
+  a.paged = paged ? 1 : 0;
+  a.scale_log2 = sm_scale * kLog2e;
+  a.timeout_ns = g_timeout_ns;
+  if (sa_status s = status_ptr(&a.status)) return s;
+  CUtensorMap qm, km, vm;
+  if (sa_status s = map_tokens_heads(&qm, q, total_q, hq, 128)) return s;
+  if (paged) {
+    if (sa_status s = map_pages(&km, k, num_pages, hkv)) return s;
+    if (sa_status s = map_pages(&vm, v, num_pages, hkv)) return s;
+  } else {
+    if (sa_status s = map_tokens_heads(&km, k, total_q, hkv, 128)) return s;
+    if (sa_status s = map_tokens_heads(&vm, v, total_q, hkv, 128)) return s;
+  }
+  return sa::launch_prefill(qm, km, vm, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
+sa_status sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                            const int32_t* cu_seqlens, int batch, int total_tokens,
+                            int max_seqlen, int num_qo_heads, int num_kv_heads, int head_dim,
+                            float sm_scale, int causal, void* out, float* lse,
+                            cudaStream_t stream) {
+  return prefill_common(q, k, v, nullptr, cu_seqlens, nullptr, sinks, batch, total_tokens,
+                        max_seqlen, num_qo_heads, num_kv_heads, head_dim, 0, 0, sm_scale, causal,
+                        out, lse, stream, false);
+}
+
+sa_status sink_attn_prefill_paged(const void* q, const void* paged_k, const void* paged_v,
+                                  const int32_t* page_table, const int32_t* cu_seqlens_q,
+                                  const int32_t* kv_lens, const float* sinks, int batch,
+                                  int total_q_tokens, int max_q_len, int num_qo_heads,
+                                  int num_kv_heads, int head_dim, int page_size, int max_pages,
+                                  int num_pages, float sm_scale, int causal, void* out,
+                                  float* lse, cudaStream_t stream) {
+  if (page_size != sa::kPageSize && page_size > 0) return SA_ERR_UNSUPPORTED;
+  if (page_size <= 0) return SA_ERR_SHAPE;
+  return prefill_common(q, paged_k, paged_v, page_table, cu_seqlens_q, kv_lens, sinks, batch,
+                        total_q_tokens, max_q_len, num_qo_heads, num_kv_heads, head_dim,
+                        max_pages, num_pages, sm_scale, causal, out, lse, stream, true);
+}
+
+}  // extern "C"

@@ -1,0 +1,324 @@
+// Paged split-KV decode with softmax sinks (one new query token per sequence).
+//
+// Page "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention":
+// attention is parallel over heads and along the KV length; the online
+// softmax keeps a running max m and denominator d, seeded with the head's
+// sink (m = sink, d = 1) in the first KV block only.
+//
+// GB300 design (memory bound, ~8 flop per KV byte at a group of 8):
+//  * one CTA per (split, kv head, sequence); its 4 warps walk the split's
+//    pages interleaved, each with a private 4-deep ring of TMA page loads
+//    (one 2 KiB K box + one 2 KiB V box per page, 128-byte swizzle, L2
+//    evict-first), so no CTA-wide barrier sits in the streaming loop;
+//  * the whole GQA group of a KV head is one 8-wide MMA "N" tile: scores are
+//    computed transposed, S^T[16 tok x 8 heads] = K_page . Q^T, and the PV
+//    product as O^T[64 x 8] += V^T . P^T, so mma.sync m16n8k16 runs with no
+//    padding; P^T is formed from the score fragments with movmatrix;
+//  * per-lane partial denominators, warp-shuffle row max, one smem merge of
+//    the 4 warp states at the end; split 0's warp 0 starts from the sink.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 4;
+constexpr int kPageBytes = kPageSize * kHeadDim * 2;  // 2 KiB per (page, kv head)
+constexpr int kSlotBytes = 2 * kPageBytes;            // K + V
+constexpr int kRingBytes = kWarps * kStages * kSlotBytes;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <int NT>
+struct MergeArea {  // aliases the ring once streaming is over
+  float m[kWarps][NT * 8];
+  float d[kWarps][NT * 8];
+  float o[kWarps][NT * 8][kHeadDim];
+};
+
+constexpr size_t decode_smem_bytes() {
+  return 1024 /*alignment slack*/ + kRingBytes + kWarps * kStages * sizeof(uint64_t);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kWarps * 32)
+    sink_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  static_assert(sizeof(MergeArea<NT>) <= kRingBytes, "merge area must fit in the ring");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingBytes);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.group;
+
+  int kv_len = a.kv_lens[b];
+  const int cap = a.max_pages * kPageSize;
+  if (kv_len < 0 || kv_len > cap) {
+    if (threadIdx.x == 0) raise_status(a.status, kStatusBadLen);
+    kv_len = kv_len < 0 ? 0 : cap;
+  }
+  const int n_pages = (kv_len + kPageSize - 1) / kPageSize;
+  const int per_split = (n_pages + a.num_splits - 1) / a.num_splits;
+  const int p_begin = min(split * per_split, n_pages);
+  const int p_end = min(p_begin + per_split, n_pages);
+  // this warp's pages: p_begin + warp + j * kWarps, j = 0 .. my_count-1
+  const int my_first = p_begin + warp;
+  const int my_count = my_first < p_end ? (p_end - my_first + kWarps - 1) / kWarps : 0;
+
+  const uint32_t ring_w = smem_u32(ring + warp * kStages * kSlotBytes);
+  const uint32_t full_w = smem_u32(full + warp * kStages);
+  const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(full_w + 8 * s, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  __syncwarp();
+
+  const uint64_t policy = l2_policy_evict_first();
+  auto issue = [&](int j) {  // lane 0 only
+    const int pg = my_first + j * kWarps;
+    const int phys = ptab[pg];
+    const uint32_t bar = full_w + 8 * (j % kStages);
+    if (phys < 0 || phys >= a.num_pages) {
+      raise_status(a.status, kStatusBadPage);
+      mbar_arrive(bar);  // completes the phase with nothing copied; page is skipped
+      return;
+    }
+    const uint32_t dst = ring_w + (j % kStages) * kSlotBytes;
+    const int row = (phys * a.hkv + kvh) * kPageSize;
+    mbar_arrive_expect_tx(bar, kSlotBytes);
+    tma_load_2d(dst, &kmap, 0, row, bar, policy);
+    tma_load_2d(dst + kPageBytes, &vmap, 0, row, bar, policy);
+  };
+  int issued = min(kStages, my_count);  // meaningful on lane 0
+  if (lane == 0)
+    for (int j = 0; j < issued; ++j) issue(j);
+
+  // Q^T fragments (B operand of S^T = K Q^T): lane holds head (lane/4) of each
+  // 8-wide tile, dims kk*16 + 2*(lane%4) + {0,1} and +8.
+  uint32_t qf[NT][4][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hh = nt * 8 + (lane >> 2);
+    const bool ok = hh < G;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        static_cast<const uint16_t*>(a.q) +
+        (static_cast<size_t>(b) * a.hq + kvh * G + (ok ? hh : 0)) * kHeadDim);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      qf[nt][kk][0] = ok ? qrow[kk * 8 + (lane & 3)] : 0u;
+      qf[nt][kk][1] = ok ? qrow[kk * 8 + 4 + (lane & 3)] : 0u;
+    }
+  }
+
+  // Running state for heads nt*8 + 2*(lane%4) + {0,1}; m in log2 units.
+  float m[NT][2], dsum[NT][2], o[NT][4][4];
+  const bool seed = (split == 0 && warp == 0);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int hh = nt * 8 + 2 * (lane & 3) + e;
+      float sink = kNegInf;
+      if (seed && hh < G) sink = a.sinks[kvh * G + hh] * kLog2e;
+      m[nt][e] = sink;
+      // d starts at exp(sink - sink) = 1, counted once (lane/4 == 0); 0 for -inf
+      dsum[nt][e] = (sink != kNegInf && (lane >> 2) == 0) ? 1.0f : 0.0f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) o[nt][mt][r] = 0.0f;
+  }
+
+  bool timed_out = false;
+  int j = 0;
+  for (; j < my_count; ++j) {
+    const int slot = j % kStages;
+    if (!mbar_wait(full_w + 8 * slot, (j / kStages) & 1, a.timeout_ns)) {
+      timed_out = true;
+      break;
+    }
+    const int pg = my_first + j * kWarps;
+    const int phys = ptab[pg];
+    if (phys >= 0 && phys < a.num_pages) {
+      const uint32_t kb = ring_w + slot * kSlotBytes;
+      const uint32_t vb = kb + kPageBytes;
+      // ---- S^T = K Q^T (16 tokens x 8 heads per tile)
+      float s[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) s[nt][r] = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chunk = kk * 2 + (lane >> 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kb + row * 128 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+      }
+      // ---- scale, mask the ragged tail, online softmax update
+      const int tok0 = pg * kPageSize + (lane >> 2);
+      const bool v0 = tok0 < kv_len, v1 = tok0 + 8 < kv_len;
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float x0 = v0 ? s[nt][0] * a.scale_log2 : kNegInf;
+        float x1 = v0 ? s[nt][1] * a.scale_log2 : kNegInf;
+        float x2 = v1 ? s[nt][2] * a.scale_log2 : kNegInf;
+        float x3 = v1 ? s[nt][3] * a.scale_log2 : kNegInf;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+        const float mu0 = mn0 == kNegInf ? 0.0f : mn0;
+        const float mu1 = mn1 == kNegInf ? 0.0f : mn1;
+        const float c0 = m[nt][0] == mn0 ? 1.0f : ex2(m[nt][0] - mu0);
+        const float c1 = m[nt][1] == mn1 ? 1.0f : ex2(m[nt][1] - mu1);
+        m[nt][0] = mn0;
+        m[nt][1] = mn1;
+        const float p0 = ex2(x0 - mu0), p1 = ex2(x1 - mu1);
+        const float p2 = ex2(x2 - mu0), p3 = ex2(x3 - mu1);
+        dsum[nt][0] = dsum[nt][0] * c0 + (p0 + p2);
+        dsum[nt][1] = dsum[nt][1] * c1 + (p1 + p3);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          o[nt][mt][0] *= c0;
+          o[nt][mt][1] *= c1;
+          o[nt][mt][2] *= c0;
+          o[nt][mt][3] *= c1;
+        }
+        // P^T as the B operand of O^T += V^T P^T: transpose the two 8x8 blocks
+        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+      }
+      // ---- O^T += V^T P^T (64 dims x 8 heads per tile)
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int tok = (lane & 7) + (lane >> 4) * 8;
+        const int chunk = mt * 2 + ((lane >> 3) & 1);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vb + tok * 128 + ((chunk ^ (tok & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && j + kStages < my_count) {
+      issue(j + kStages);
+      ++issued;
+    }
+  }
+
+  if (timed_out) {
+    if (lane == 0) {
+      raise_status(a.status, kStatusTimeout);
+      // let copies still in flight land before the CTA's shared memory goes away
+      // (bounded again; default limit even if the caller asked for a tiny one)
+      for (int jj = j; jj < issued; ++jj)
+        mbar_wait(full_w + 8 * (jj % kStages), (jj / kStages) & 1, 2000000000ull);
+    }
+    __syncwarp();
+  }
+
+  // ---- combine the lanes' partial denominators
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+        dsum[nt][e] += __shfl_xor_sync(0xffffffffu, dsum[nt][e], off);
+
+  __syncthreads();  // every warp is done with its ring; reuse it for the merge
+  MergeArea<NT>* mg = reinterpret_cast<MergeArea<NT>*>(ring);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int hh = nt * 8 + 2 * (lane & 3) + e;
+      if ((lane >> 2) == 0) {
+        mg->m[warp][hh] = m[nt][e];
+        mg->d[warp][hh] = dsum[nt][e];
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        mg->o[warp][hh][mt * 16 + (lane >> 2)] = o[nt][mt][e];
+        mg->o[warp][hh][mt * 16 + (lane >> 2) + 8] = o[nt][mt][2 + e];
+      }
+    }
+  }
+  __syncthreads();
+
+  for (int i = threadIdx.x; i < G * 16; i += kWarps * 32) {
+    const int hh = i >> 4, d0 = (i & 15) * 4;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mg->m[w][hh]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float den = 0.0f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = mg->m[w][hh];
+        const float c = mw == M ? 1.0f : ex2(mw - M);
+        den += mg->d[w][hh] * c;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] += mg->o[w][hh][d0 + r] * c;
+      }
+    }
+    const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+    const float lse = den > 0.0f ? (M + lg2(den)) * kLn2 : kNegInf;
+    const int head = kvh * G + hh;
+    if (a.num_splits == 1) {
+      uint16_t* out = static_cast<uint16_t*>(a.out) +
+                      (static_cast<size_t>(b) * a.hq + head) * kHeadDim + d0;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(out) = pk;
+      if (a.lse && d0 == 0) a.lse[static_cast<size_t>(b) * a.hq + head] = lse;
+    } else {
+      const size_t row = (static_cast<size_t>(b) * a.num_splits + split) * a.hq + head;
+      float* out = static_cast<float*>(a.out) + row * kHeadDim + d0;
+      *reinterpret_cast<float4*>(out) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv,
+                                                    acc[3] * inv);
+      if (d0 == 0) a.lse[row] = lse;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
+                          cudaStream_t stream) {
+  const dim3 grid(a.num_splits, a.hkv, a.batch);
+  const size_t smem = decode_smem_bytes();
+  if (a.group <= 8) {
+    auto kern = sink_decode_kernel<1>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kWarps * 32, smem, stream>>>(kmap, vmap, a);
+  } else {
+    auto kern = sink_decode_kernel<2>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kWarps * 32, smem, stream>>>(kmap, vmap, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sa

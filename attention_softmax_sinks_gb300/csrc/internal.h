@@ -1,0 +1,55 @@
+// Internal interface between the C-ABI layer (abi.cu) and the kernel
+// translation units.  Arguments arrive here already validated.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sa {
+
+constexpr int kHeadDim = 64;
+constexpr int kPageSize = 16;
+
+struct DecodeArgs {
+  const void* q;
+  const int32_t* page_table;
+  const int32_t* kv_lens;
+  const float* sinks;
+  void* out;
+  float* lse;
+  int batch, hq, hkv, group, max_pages, num_pages, num_splits;
+  float scale_log2;  // sm_scale * log2(e)
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+struct MergeArgs {
+  const float* partial_o;
+  const float* partial_lse;
+  void* out;
+  float* lse;
+  int batch, num_splits, heads;
+};
+
+struct PrefillArgs {
+  const void* q;           // [T, Hq, 64]
+  const int32_t* cu_q;     // [B + 1]
+  const int32_t* kv_lens;  // [B] (paged) or nullptr (contiguous: kv_len == q_len)
+  const int32_t* page_table;
+  const float* sinks;
+  void* out;
+  float* lse;
+  int batch, total_q, max_q, hq, hkv, group, max_pages, num_pages, causal, paged;
+  float scale_log2;
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+// Tensor maps (TMA descriptors) built on the host by abi.cu.
+cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
+                          cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace sa

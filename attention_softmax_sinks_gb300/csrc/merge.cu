@@ -1,0 +1,75 @@
+// Merge of split-KV partials: lse = ln sum_s e^(lse_s), out = sum_s e^(lse_s - lse) o_s.
+//
+// The split rule comes from the page "GPT-OSS on day 0", section "Kernels for
+// GPT-OSS / Sink Attention" (the sink-seeded max belongs to the first block
+// only); this is the log-sum-exp combine that undoes the split.  One warp per
+// (sequence, head): lanes read the split lse values, a shuffle max, then each
+// lane accumulates two of the 64 output dims over the splits with coalesced
+// float2 loads (256 contiguous bytes per split per warp).
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kPosInf = __builtin_huge_valf();
+constexpr int kMergeWarps = 4;
+
+__device__ __forceinline__ float split_weight(float lse_s, float M) {
+  // e^(lse_s - M); the max term gets exactly 1, -inf terms exactly 0
+  if (lse_s == M) return 1.0f;
+  if (lse_s == kNegInf || M == kPosInf) return 0.0f;
+  return ex2((lse_s - M) * kLog2e);
+}
+
+__global__ void __launch_bounds__(kMergeWarps * 32) sink_merge_kernel(const MergeArgs a) {
+  const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.batch * a.heads) return;
+  const int b = row / a.heads, h = row % a.heads;
+  const int S = a.num_splits;
+  const float* lse_p = a.partial_lse + static_cast<size_t>(b) * S * a.heads + h;
+
+  float M = kNegInf;
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, lse_p[static_cast<size_t>(s) * a.heads]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float z = 0.0f;
+  float2 acc = make_float2(0.0f, 0.0f);
+  if (M != kNegInf) {
+    const float* o_p = a.partial_o + (static_cast<size_t>(b) * S * a.heads + h) * kHeadDim + 2 * lane;
+    for (int s = 0; s < S; ++s) {
+      const float w = split_weight(lse_p[static_cast<size_t>(s) * a.heads], M);
+      if (w != 0.0f) {
+        const float2 v = *reinterpret_cast<const float2*>(o_p + static_cast<size_t>(s) * a.heads * kHeadDim);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        z += w;
+      }
+    }
+  }
+  const float inv = z > 0.0f ? 1.0f / z : 0.0f;
+  uint16_t* out = static_cast<uint16_t*>(a.out) + static_cast<size_t>(row) * kHeadDim + 2 * lane;
+  *reinterpret_cast<uint32_t*>(out) = pack_bf16x2(acc.x * inv, acc.y * inv);
+  if (a.lse && lane == 0) {
+    float l = kNegInf;
+    if (M == kPosInf) l = kPosInf;
+    else if (z > 0.0f) l = M + lg2(z) * kLn2;
+    a.lse[row] = l;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+  const int rows = a.batch * a.heads;
+  const int blocks = (rows + kMergeWarps - 1) / kMergeWarps;
+  sink_merge_kernel<<<blocks, kMergeWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

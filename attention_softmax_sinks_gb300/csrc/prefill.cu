@@ -1,0 +1,432 @@
+// Causal / ragged prefill with softmax sinks on tcgen05 tensor cores.
+//
+// Page "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention":
+// attn = softmax(q k^T * sm_scale + sink) V with the head's sink seeding the
+// online softmax (running max m = sink, running denominator d = 1).  Here a
+// CTA owns one 128-token query block of the whole sequence, so the sink seeds
+// its single KV walk.
+//
+// GB300 design (one CTA per SM, 12 warps, warp-specialised):
+//  * warp 0, lane 0 -- TMA producer: Q for two query heads of one KV group
+//    (two 128x64 tiles), then K and V tiles of 128 keys into a 3-stage ring
+//    (128-byte swizzle; contiguous tensors by one 3-D box, paged caches by
+//    eight 16-row page boxes through the page table).
+//  * warp 1 -- allocates 512 TMEM columns; lane 0 issues tcgen05.mma:
+//    S_t = Q_t K^T (M=128, N=128, K=64) into TMEM, and O_t += P_t V with P_t
+//    read from TMEM (M=128, N=64, K=128).  Completion is signalled through
+//    tcgen05.commit onto mbarriers.
+//  * warps 4-7 and 8-11 -- one softmax warpgroup per query tile; thread r
+//    owns row r (TMEM lane r): reads its 128 scores, masks on diagonal tiles
+//    only, updates the running max lazily (O and d are rescaled only when the
+//    max grows by more than 2^8, which leaves the final O/d unchanged), writes
+//    P as bf16 into TMEM and finally stores out = O/d and lse = m + ln d.
+//  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
+//                P0 [384,448) P1 [448,512).
+//  The two query tiles let the tensor core work on one tile while the other
+//  warpgroup runs its softmax.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kBlockQ = 128;
+constexpr int kBlockK = 128;
+constexpr int kStages = 3;
+constexpr int kThreads = 384;
+constexpr int kTileBytes = kBlockQ * kHeadDim * 2;  // 16 KiB
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384, kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct __align__(1024) PrefillSmem {
+  uint8_t q[2][kTileBytes];
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  uint64_t q_full;
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int issued_tiles;
+};
+
+// Shared-memory matrix descriptor, 128-byte swizzle, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(1024 >> 4) << 16;  // leading byte offset (unused for N <= 64 / K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+  d |= 1ull << 46;                               // descriptor version for tcgen05
+  d |= 2ull << 61;                               // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A/B, fp32 D, M x N, optional MN-major B.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                         volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+struct WorkItem {
+  int b, h0, ntiles, q0, q_start, q_len, kv_len, n_kv;
+  bool valid;
+};
+
+__device__ __forceinline__ WorkItem decode_work(const PrefillArgs& a) {
+  WorkItem w;
+  const int tiles = (a.group % 2 == 0) ? 2 : 1;
+  const int n_hg = a.hq / tiles;
+  const int n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
+  const int idx = blockIdx.x;
+  const int per_qb = n_hg * a.batch;
+  const int qb = n_qb - 1 - idx / per_qb;  // longest (last) query blocks first
+  const int rem = idx % per_qb;
+  w.b = rem / n_hg;
+  w.h0 = (rem % n_hg) * tiles;
+  w.ntiles = tiles;
+  w.q0 = qb * kBlockQ;
+  w.valid = false;
+  const int qs = a.cu_q[w.b], qe = a.cu_q[w.b + 1];
+  w.q_start = qs;
+  w.q_len = qe - qs;
+  w.kv_len = a.paged ? a.kv_lens[w.b] : w.q_len;
+  const bool bad = qs < 0 || w.q_len < 0 || w.q_len > a.max_q || qe > a.total_q ||
+                   w.kv_len < w.q_len || (a.paged && w.kv_len > a.max_pages * kPageSize);
+  if (bad) {
+    if (threadIdx.x == 0 && w.q0 == 0 && w.h0 == 0) raise_status(a.status, kStatusBadLen);
+    return w;
+  }
+  if (w.q0 >= w.q_len) return w;
+  // keys visible to the last row of this block (bottom-right causal alignment)
+  const int last_row = min(w.q0 + kBlockQ, w.q_len) - 1;
+  const int kv_end = a.causal ? min(w.kv_len, last_row + w.kv_len - w.q_len + 1) : w.kv_len;
+  w.n_kv = (kv_end + kBlockK - 1) / kBlockK;
+  w.valid = true;
+  return w;
+}
+
+template <bool kPaged>
+__global__ void __launch_bounds__(kThreads, 1)
+    sink_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const WorkItem w = decode_work(a);
+  if (!w.valid) return;  // uniform across the CTA, before any barrier or TMEM use
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = w.h0 / a.group;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&sm.s_full[t]), 1);
+      mbar_init(smem_u32(&sm.p_full[t]), 128);
+      mbar_init(smem_u32(&sm.o_full[t]), 1);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    sm.issued_tiles = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      const uint64_t keep = l2_policy_evict_last();  // K/V are re-read by the group's other heads
+      const uint64_t once = l2_policy_evict_first();
+      const uint32_t qbar = smem_u32(&sm.q_full);
+      mbar_arrive_expect_tx(qbar, w.ntiles * kTileBytes);
+      for (int t = 0; t < w.ntiles; ++t)
+        tma_load_3d(smem_u32(sm.q[t]), &qmap, 0, w.h0 + t, w.q_start + w.q0, qbar, once);
+      const int32_t* ptab = kPaged ? a.page_table + static_cast<size_t>(w.b) * a.max_pages : nullptr;
+      const int seq_pages = (w.kv_len + kPageSize - 1) / kPageSize;
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < w.n_kv && ok; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages &&
+            !wait_bar(smem_u32(&sm.kv_empty[st]), ((j / kStages) - 1) & 1, a.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t kbar = smem_u32(&sm.k_full[st]), vbar = smem_u32(&sm.v_full[st]);
+        mbar_arrive_expect_tx(kbar, kTileBytes);
+        mbar_arrive_expect_tx(vbar, kTileBytes);
+        if constexpr (kPaged) {
+          for (int i = 0; i < kBlockK / kPageSize; ++i) {
+            int lp = j * (kBlockK / kPageSize) + i;
+            if (lp >= seq_pages) lp = seq_pages - 1;  // ragged tail: any valid page, masked later
+            int phys = ptab[lp];
+            if (phys < 0 || phys >= a.num_pages) {
+              raise_status(a.status, kStatusBadPage);
+              phys = 0;
+            }
+            const int row = (phys * a.hkv + kvh) * kPageSize;
+            tma_load_2d(smem_u32(sm.k[st]) + i * kPageSize * 128, &kmap, 0, row, kbar, keep);
+            tma_load_2d(smem_u32(sm.v[st]) + i * kPageSize * 128, &vmap, 0, row, vbar, keep);
+          }
+        } else {
+          tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, kbar, keep);
+          tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, vbar, keep);
+        }
+        ++issued;
+      }
+      if (!ok) raise_status(a.status, kStatusTimeout);
+      sm.issued_tiles = issued;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = wait_bar(smem_u32(&sm.q_full), 0, a.timeout_ns, abort_flag);
+      const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+      auto issue_s = [&](int j, int t) {
+        const uint32_t k_addr = smem_u32(sm.k[j % kStages]);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          tc_mma_ss(tmem + kColS + t * 128, sw128_desc(q_addr[t] + kk * 32),
+                    sw128_desc(k_addr + kk * 32), kIdescS, kk > 0);
+        tc_commit(smem_u32(&sm.s_full[t]));
+      };
+      auto issue_pv = [&](int j, int t) {
+        const uint32_t v_addr = smem_u32(sm.v[j % kStages]);
+#pragma unroll
+        for (int kk = 0; kk < kBlockK / 16; ++kk)
+          tc_mma_ts(tmem + kColO + t * 64, tmem + kColP + t * 64 + kk * 8,
+                    sw128_desc(v_addr + kk * 16 * 128), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      if (ok) ok = wait_bar(smem_u32(&sm.k_full[0]), 0, a.timeout_ns, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < w.ntiles; ++t) issue_s(0, t);
+      }
+      for (int j = 0; j < w.n_kv && ok; ++j) {
+        const int st = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        ok = wait_bar(smem_u32(&sm.v_full[st]), ph, a.timeout_ns, abort_flag);
+        for (int t = 0; t < w.ntiles && ok; ++t) {
+          ok = wait_bar(smem_u32(&sm.p_full[t]), j & 1, a.timeout_ns, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(j, t);
+          if (j + 1 < w.n_kv) {
+            if (t == 0)
+              ok = wait_bar(smem_u32(&sm.k_full[(j + 1) % kStages]), ((j + 1) / kStages) & 1,
+                            a.timeout_ns, abort_flag);
+            if (ok) issue_s(j + 1, t);
+          }
+        }
+        if (ok) tc_commit(smem_u32(&sm.kv_empty[st]));
+      }
+      if (ok) {
+        for (int t = 0; t < w.ntiles; ++t) tc_commit(smem_u32(&sm.o_full[t]));
+      } else {
+        raise_status(a.status, kStatusTimeout);
+      }
+      // whatever happened, wait for every issued MMA before TMEM is released
+      tc_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, 2000000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = (warp - 4) >> 2;      // query tile of this warpgroup
+    const int qw = warp & 3;            // TMEM lane quarter
+    const int r = qw * 32 + lane;       // row within the block
+    if (t < w.ntiles) {
+      const int h = w.h0 + t;
+      const int i = w.q0 + r;           // query index within the sequence
+      const int limit = a.causal ? min(i + w.kv_len - w.q_len, w.kv_len - 1) : w.kv_len - 1;
+      const float sink = a.sinks[h] * kLog2e;
+      float m = sink;                                 // running max (log2 units)
+      float d = (sink == kNegInf) ? 0.0f : 1.0f;      // running denominator
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+      const uint32_t s_col = lane_base + kColS + t * 128;
+      const uint32_t o_col = lane_base + kColO + t * 64;
+      const uint32_t p_col = lane_base + kColP + t * 64;
+      bool ok = true;
+      for (int j = 0; j < w.n_kv; ++j) {
+        if (!wait_bar(smem_u32(&sm.s_full[t]), j & 1, a.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(s_col + c * 32, u);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[e]);
+        }
+        tc_wait_ld();
+        const int key0 = j * kBlockK;
+        if (key0 + kBlockK - 1 > limit) {  // diagonal / tail tile: mask
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (key0 + c > limit) s[c] = kNegInf;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        mx *= a.scale_log2;
+        const bool grow = mx > m + kRescaleThreshold;
+        float factor = 1.0f;
+        if (grow) {
+          factor = (m == kNegInf) ? 0.0f : ex2(m - mx);
+          m = mx;
+          d *= factor;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {  // O holds earlier tiles: rescale it
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t u[32];
+            tmem_ld32(o_col + c * 32, u);
+            tc_wait_ld();
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              lo[e] = __float_as_uint(__uint_as_float(u[e]) * factor);
+              hi[e] = __float_as_uint(__uint_as_float(u[16 + e]) * factor);
+            }
+            tmem_st16(o_col + c * 32, lo);
+            tmem_st16(o_col + c * 32 + 16, hi);
+          }
+        }
+        const float mu = (m == kNegInf) ? 0.0f : m;
+        float rs = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(s[c * 32 + 2 * e], a.scale_log2, -mu));
+            const float p1 = ex2(fmaf(s[c * 32 + 2 * e + 1], a.scale_log2, -mu));
+            rs += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(p_col + c * 16, pk);
+        }
+        d += rs;
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full[t]));
+      }
+      if (ok && w.n_kv > 0) ok = wait_bar(smem_u32(&sm.o_full[t]), 0, a.timeout_ns, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        const bool row_ok = i < w.q_len;
+        const float inv = d > 0.0f ? 1.0f / d : 0.0f;
+        uint16_t* out = static_cast<uint16_t*>(a.out) +
+                        (static_cast<size_t>(w.q_start + i) * a.hq + h) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t u[32];
+          if (w.n_kv > 0) {
+            tmem_ld32(o_col + c * 32, u);
+            tc_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = 0u;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 pk;
+              pk.x = pack_bf16x2(__uint_as_float(u[8 * e + 0]) * inv, __uint_as_float(u[8 * e + 1]) * inv);
+              pk.y = pack_bf16x2(__uint_as_float(u[8 * e + 2]) * inv, __uint_as_float(u[8 * e + 3]) * inv);
+              pk.z = pack_bf16x2(__uint_as_float(u[8 * e + 4]) * inv, __uint_as_float(u[8 * e + 5]) * inv);
+              pk.w = pack_bf16x2(__uint_as_float(u[8 * e + 6]) * inv, __uint_as_float(u[8 * e + 7]) * inv);
+              reinterpret_cast<uint4*>(out + c * 32)[e] = pk;
+            }
+          }
+        }
+        if (row_ok && a.lse)
+          a.lse[static_cast<size_t>(w.q_start + i) * a.hq + h] =
+              d > 0.0f ? (m + lg2(d)) * kLn2 : kNegInf;
+      } else {
+        raise_status(a.status, kStatusTimeout);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // some role gave up: copies it never consumed may still be in flight; let
+    // the last tile of every stage (and Q) land before shared memory is released
+    const int issued = sm.issued_tiles;
+    for (int j = max(0, issued - kStages); j < issued; ++j) {
+      const int st = j % kStages;
+      mbar_wait(smem_u32(&sm.k_full[st]), (j / kStages) & 1, 2000000000ull);
+      mbar_wait(smem_u32(&sm.v_full[st]), (j / kStages) & 1, 2000000000ull);
+    }
+    mbar_wait(smem_u32(&sm.q_full), 0, 2000000000ull);
+  }
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t stream) {
+  const int tiles = (a.group % 2 == 0) ? 2 : 1;
+  const int n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
+  const long long blocks = static_cast<long long>(n_qb) * (a.hq / tiles) * a.batch;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const size_t smem = sizeof(PrefillSmem) + 1024;
+  auto kern = a.paged ? sink_prefill_kernel<true> : sink_prefill_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(qmap, kmap, vmap, a);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -1,0 +1,184 @@
+/*
+ * sink_attn.h -- C ABI of libsinkattn.so: GQA attention with per-head softmax
+ * sinks on NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one stated on the page "GPT-OSS on day 0" (Perplexity,
+ * 2025), section "Kernels for GPT-OSS / Sink Attention":
+ *
+ *     attn = softmax(q k^T * sm_scale  (+)  sink_h) V
+ *
+ * where each query head h owns one pretrained sink logit sink_h that joins
+ * the softmax denominator as one extra column and contributes no row of V.
+ * For one query row over its visible keys J (s_j = sm_scale * q.k_j):
+ *
+ *     M = max(max_j s_j, sink_h),  Z = sum_j e^(s_j - M) + e^(sink_h - M)
+ *     out = sum_j e^(s_j - M) v_j / Z,   lse = M + ln Z   (natural log)
+ *
+ * The same section's online algorithm seeds the running max with the sink
+ * (and the running denominator with 1) and, when the KV range is split into
+ * blocks, does so for the first block only; sink_attn_decode follows that rule
+ * across its splits and sink_attn_merge recombines the split results.
+ *
+ * Conventions shared by every entry point
+ *  - All tensors are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or synchronises.  Every call is asynchronous on `stream`.
+ *  - q/k/v/out are bf16 (passed as void*), row-major, dense, 16-byte aligned.
+ *    sinks are fp32 [num_qo_heads]; lse outputs are fp32.
+ *  - Grouped-query attention: query head h reads KV head h / (Hq / Hkv).
+ *  - head_dim must be 64 and page_size 16; Hq % Hkv == 0 and Hq / Hkv <= 16.
+ *  - sm_scale must be finite and > 0; it multiplies q.k only, never the sink.
+ *  - Invalid arguments are rejected before any launch with a status code.
+ *    Device-side problems (a page id outside [0, num_pages), a length larger
+ *    than the declared bound, a bounded wait that ran out) never fault: the
+ *    kernel skips the access, ORs a bit into a per-device status word and
+ *    carries on; sink_attn_device_status() reports and clears it.
+ *  - Empty work (batch == 0 or no tokens) returns SA_OK without launching.
+ */
+#ifndef SINK_ATTN_H
+#define SINK_ATTN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sa_status {
+  SA_OK = 0,
+  SA_ERR_NULL = 1,        /* a required pointer is NULL                        */
+  SA_ERR_SHAPE = 2,       /* inconsistent or out-of-range sizes / sm_scale      */
+  SA_ERR_UNSUPPORTED = 3, /* head_dim != 64, page_size != 16, group size > 16   */
+  SA_ERR_LAUNCH = 4,      /* the kernel launch itself failed                   */
+  SA_ERR_BOUNDS = 5,      /* device saw a bad page id or length (status word)  */
+  SA_ERR_TIMEOUT = 6,     /* device wait ran out of time (status word)         */
+  SA_ERR_ALIGNMENT = 7,   /* a tensor pointer is not 16-byte aligned           */
+  SA_ERR_CUDA = 8         /* a CUDA runtime call made by the library failed    */
+} sa_status;
+
+/*
+ * Causal or full attention over a ragged batch of contiguous sequences whose
+ * queries are their keys (q_len == kv_len for every sequence): prefill.
+ * Section "Kernels for GPT-OSS / Sink Attention" (formula, and the note that
+ * the page's FlashInfer-based template serves prefill).
+ *
+ *  q          bf16 [total_tokens, num_qo_heads, head_dim]
+ *  k, v       bf16 [total_tokens, num_kv_heads, head_dim]
+ *  sinks      fp32 [num_qo_heads]  (may hold -inf: no sink; +inf: all weight)
+ *  cu_seqlens int32 [batch + 1], device; sequence b is rows
+ *             [cu_seqlens[b], cu_seqlens[b+1]); must be non-decreasing,
+ *             cu_seqlens[0] == 0, cu_seqlens[batch] == total_tokens and every
+ *             length <= max_seqlen (violations set SA_ERR_BOUNDS, rows skipped)
+ *  causal     nonzero: key j visible to query i iff j <= i
+ *  out        bf16 [total_tokens, num_qo_heads, head_dim]
+ *  lse        fp32 [total_tokens, num_qo_heads] or NULL
+ */
+sa_status sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks,
+                            const int32_t* cu_seqlens, int batch, int total_tokens,
+                            int max_seqlen, int num_qo_heads, int num_kv_heads, int head_dim,
+                            float sm_scale, int causal, void* out, float* lse,
+                            cudaStream_t stream);
+
+/*
+ * Attention of a mixed batch of new tokens over a paged KV cache: sequence b
+ * has q_len_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new query tokens which are
+ * the last q_len_b of its kv_lens[b] cached tokens (q_len_b <= kv_lens[b]).
+ * Decode rows (q_len 1) and prefill chunks may be mixed in one call.
+ * Causal masking is bottom-right aligned: query i sees key j iff
+ * j <= i + kv_len - q_len.
+ *
+ *  q            bf16 [total_q_tokens, num_qo_heads, head_dim]
+ *  paged_k/v    bf16 [num_pages, num_kv_heads, page_size, head_dim]
+ *  page_table   int32 [batch, max_pages]; entry (b, j) is the physical page of
+ *               logical tokens [j*page_size, (j+1)*page_size) of sequence b
+ *  cu_seqlens_q int32 [batch + 1];  kv_lens int32 [batch]
+ *  max_q_len    upper bound on every q_len_b
+ *  out, lse     as for sink_attn_prefill, indexed by query token
+ */
+sa_status sink_attn_prefill_paged(const void* q, const void* paged_k, const void* paged_v,
+                                  const int32_t* page_table, const int32_t* cu_seqlens_q,
+                                  const int32_t* kv_lens, const float* sinks, int batch,
+                                  int total_q_tokens, int max_q_len, int num_qo_heads,
+                                  int num_kv_heads, int head_dim, int page_size, int max_pages,
+                                  int num_pages, float sm_scale, int causal, void* out,
+                                  float* lse, cudaStream_t stream);
+
+/*
+ * Decode: one new query token per sequence against its paged KV cache, with
+ * the KV range optionally split across CTAs.  Section "Kernels for GPT-OSS /
+ * Sink Attention": parallel over heads and along the KV length; the sink seeds
+ * the running max of the first block only.  Split s of a sequence with
+ * n = ceil(kv_len / page_size) pages covers pages [s*c, min((s+1)*c, n)),
+ * c = ceil(n / num_splits); only split 0 carries the sink.
+ *
+ *  q          bf16 [batch, num_qo_heads, head_dim]
+ *  paged_k/v, page_table, kv_lens: as for sink_attn_prefill_paged
+ *  num_splits 1..256.
+ *    == 1: out bf16 [batch, num_qo_heads, head_dim], lse fp32
+ *          [batch, num_qo_heads] or NULL -- the final result.
+ *    >  1: out fp32 [batch, num_splits, num_qo_heads, head_dim] holds each
+ *          split's normalised partial output and lse fp32
+ *          [batch, num_splits, num_qo_heads] (required) its log-sum-exp
+ *          (-inf for an empty split without sink); combine with
+ *          sink_attn_merge.
+ */
+sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged_v,
+                           const int32_t* page_table, const int32_t* kv_lens, const float* sinks,
+                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                           int page_size, int max_pages, int num_pages, float sm_scale,
+                           int num_splits, void* out, float* lse, cudaStream_t stream);
+
+/*
+ * Merge split partials into the final result:
+ *   lse = ln sum_s e^(lse_s),  out = sum_s e^(lse_s - lse) o_s  (bf16).
+ * Implied by the split rule of section "Kernels for GPT-OSS / Sink Attention";
+ * the combine itself is the standard log-sum-exp merge.
+ *
+ *  partial_o   fp32 [batch, num_splits, num_heads, head_dim]
+ *  partial_lse fp32 [batch, num_splits, num_heads]
+ *  out         bf16 [batch, num_heads, head_dim];  lse_out fp32 [batch, num_heads] or NULL
+ * A row whose partials are all -inf yields out = 0, lse = -inf.
+ */
+sa_status sink_attn_merge(const float* partial_o, const float* partial_lse, int batch,
+                          int num_splits, int num_heads, int head_dim, void* out, float* lse_out,
+                          cudaStream_t stream);
+
+/*
+ * Host-only helper: a split count for sink_attn_decode that fills `num_sms`
+ * SMs with work while keeping every split at least a few pages long.
+ * Returns a value in [1, 256].  No CUDA call.
+ */
+int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int page_size,
+                            int num_sms);
+
+/*
+ * Read (and, if `clear` is nonzero, reset) the current device's status word.
+ * SYNCHRONISES the device.  Returns SA_OK, SA_ERR_BOUNDS or SA_ERR_TIMEOUT
+ * (timeout wins if both bits are set), or SA_ERR_CUDA.
+ */
+sa_status sink_attn_device_status(int clear);
+
+/* Upper bound, in nanoseconds, on every device-side wait of later launches
+ * (default 2e9).  A wait that runs out stops its CTA cleanly and sets
+ * SA_ERR_TIMEOUT in the status word.  Host-only, not thread-safe. */
+void sink_attn_set_wait_timeout_ns(unsigned long long ns);
+
+/* Diagnostic: launch one warp that waits on a device barrier nothing will
+ * ever release, using the same bounded wait as the attention kernels.  After
+ * timeout_ns (capped at 1e9) the wait gives up and SA_ERR_TIMEOUT is recorded
+ * in the status word; read it with sink_attn_device_status().  Lets a caller
+ * confirm, without faulting the GPU, that device waits end and are reported.
+ * Not part of the page's method. */
+sa_status sink_attn_selftest_wait_timeout(unsigned long long timeout_ns, cudaStream_t stream);
+
+/* Static string for a status code (never NULL). */
+const char* sink_attn_status_string(sa_status status);
+
+/* Version of this ABI (incremented on incompatible change). */
+int sink_attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINK_ATTN_H */

@@ -1,0 +1,140 @@
+"""The C ABI on the CPU: the library builds and loads, exports every function
+that include/sink_attn.h declares, and rejects bad arguments with a status
+code before touching the GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sink_attn.h")
+
+SA_OK, SA_ERR_NULL, SA_ERR_SHAPE, SA_ERR_UNSUPPORTED = 0, 1, 2, 3
+SA_ERR_ALIGNMENT = 7
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_softmax_sinks_gb300 import _build
+    import attention_softmax_sinks_gb300 as sa
+    _build.build()
+    return sa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sink_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("sink_attn_prefill", "sink_attn_prefill_paged", "sink_attn_decode", "sink_attn_merge"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import attention_softmax_sinks_gb300 as sa
+    names = declared_functions()
+    assert set(names) == set(sa.EXPORTED_SYMBOLS)
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    nm = subprocess.run(["nm", "-D", "--defined-only", sa.library_path()], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = set(re.findall(r"\sT\s(\w+)", nm.stdout))
+        for n in names:
+            assert n in exported, f"{n} missing from the dynamic symbol table"
+
+
+def test_library_targets_sm103a_only():
+    from attention_softmax_sinks_gb300 import _build
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings_and_version(lib):
+    assert lib.sink_attn_abi_version() == 1
+    for s in range(9):
+        assert lib.sink_attn_status_string(s)
+    assert lib.sink_attn_status_string(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: rejected first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, pt=FAKE, kv=FAKE, sinks=FAKE, batch=2, hq=64, hkv=8, d=64,
+             ps=16, max_pages=4, num_pages=8, scale=0.125, splits=1, out=FAKE, lse=FAKE)
+    a.update(kw)
+    return lib.sink_attn_decode(a["q"], a["k"], a["v"], a["pt"], a["kv"], a["sinks"], a["batch"],
+                                a["hq"], a["hkv"], a["d"], a["ps"], a["max_pages"], a["num_pages"],
+                                a["scale"], a["splits"], a["out"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), SA_ERR_NULL), (dict(pt=None), SA_ERR_NULL), (dict(sinks=None), SA_ERR_NULL),
+    (dict(splits=4, lse=None), SA_ERR_NULL),
+    (dict(d=128), SA_ERR_UNSUPPORTED), (dict(ps=32), SA_ERR_UNSUPPORTED),
+    (dict(hq=64, hkv=3), SA_ERR_SHAPE), (dict(hq=64, hkv=2), SA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), SA_ERR_SHAPE), (dict(scale=float("nan")), SA_ERR_SHAPE),
+    (dict(scale=float("inf")), SA_ERR_SHAPE), (dict(splits=0), SA_ERR_SHAPE),
+    (dict(splits=257), SA_ERR_SHAPE), (dict(batch=-1), SA_ERR_SHAPE),
+    (dict(num_pages=0), SA_ERR_SHAPE), (dict(q=MISALIGNED), SA_ERR_ALIGNMENT),
+    (dict(k=MISALIGNED), SA_ERR_ALIGNMENT), (dict(batch=0), SA_OK),
+])
+def test_decode_rejects_before_launch(lib, kw, status):
+    assert _decode(lib, **kw) == status
+
+
+def _prefill(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, sinks=FAKE, cu=FAKE, batch=1, t=128, maxq=128, hq=4, hkv=1,
+             d=64, scale=0.125, causal=1, out=FAKE, lse=None)
+    a.update(kw)
+    return lib.sink_attn_prefill(a["q"], a["k"], a["v"], a["sinks"], a["cu"], a["batch"], a["t"],
+                                 a["maxq"], a["hq"], a["hkv"], a["d"], a["scale"], a["causal"],
+                                 a["out"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), SA_ERR_NULL), (dict(cu=None), SA_ERR_NULL), (dict(out=None), SA_ERR_NULL),
+    (dict(d=96), SA_ERR_UNSUPPORTED), (dict(hq=6, hkv=4), SA_ERR_SHAPE),
+    (dict(scale=-1.0), SA_ERR_SHAPE), (dict(t=-5), SA_ERR_SHAPE),
+    (dict(out=MISALIGNED), SA_ERR_ALIGNMENT), (dict(batch=0), SA_OK), (dict(t=0), SA_OK),
+])
+def test_prefill_rejects_before_launch(lib, kw, status):
+    assert _prefill(lib, **kw) == status
+
+
+def test_prefill_paged_rejects(lib):
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 8, 64, 8, 64, 16, 4, 8, 0.125, 1, FAKE, None, None]
+    ok = list(args)
+    bad_page = list(args); bad_page[13] = 8
+    null_pt = list(args); null_pt[3] = None
+    no_pages = list(args); no_pages[15] = 0
+    assert lib.sink_attn_prefill_paged(*bad_page) == SA_ERR_UNSUPPORTED
+    assert lib.sink_attn_prefill_paged(*null_pt) == SA_ERR_NULL
+    assert lib.sink_attn_prefill_paged(*no_pages) == SA_ERR_SHAPE
+    zero = list(ok); zero[7] = 0
+    assert lib.sink_attn_prefill_paged(*zero) == SA_OK
+
+
+def test_merge_rejects(lib):
+    assert lib.sink_attn_merge(None, FAKE, 2, 4, 64, 64, FAKE, None, None) == SA_ERR_NULL
+    assert lib.sink_attn_merge(FAKE, FAKE, 2, 0, 64, 64, FAKE, None, None) == SA_ERR_SHAPE
+    assert lib.sink_attn_merge(FAKE, FAKE, 2, 4, 64, 32, FAKE, None, None) == SA_ERR_UNSUPPORTED
+    assert lib.sink_attn_merge(FAKE, FAKE, 0, 4, 64, 64, FAKE, None, None) == SA_OK
+
+
+def test_decode_split_heuristic(lib):
+    f = lib.sink_attn_decode_splits
+    # every result is within [1, 256] and keeps >= 16 pages per split
+    for b, hkv, kv in [(1, 8, 131072), (8, 8, 131072), (64, 8, 4096), (256, 8, 512), (1, 1, 1)]:
+        s = f(b, hkv, kv, 16, 152)
+        assert 1 <= s <= 256
+        pages = (kv + 15) // 16
+        assert s == 1 or pages // s >= 16
+    assert f(1, 8, 16, 16, 152) == 1           # a single page cannot be split
+    assert f(8, 8, 131072, 16, 152) >= 16      # long context spreads over the GPU
+    assert f(0, 8, 4096, 16, 152) == 1

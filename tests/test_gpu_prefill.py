@@ -1,0 +1,85 @@
+"""GPU parity: contiguous causal / full prefill against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_common import assert_close, bf16, dev, host, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(sa, data, max_len, scale, causal):
+    return sa.sink_attn_prefill(bf16(data["q"]), bf16(data["k"]), bf16(data["v"]), dev(data["sinks"]),
+                                dev(data["cu_seqlens"]), max_len, scale, causal=causal)
+
+
+def test_tiny_prefill_config_full():
+    """1 x 128 tokens, causal, 4 query heads on 1 KV head, head_dim 64, sm_scale 1/8."""
+    sa = require_gpu()
+    cfg = workloads.WORKLOADS["tiny_prefill"]
+    data = workloads.make_prefill(cfg["seed"], [cfg["seqlen"]], cfg["hq"], cfg["hkv"], cfg["d"],
+                                  cfg["sink_std"])
+    o, l = _run(sa, data, cfg["seqlen"], cfg["sm_scale"], True)
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"],
+                            cfg["sm_scale"], True)
+    assert_close(host(o), host(l), ro, rl, "tiny prefill")
+    assert sa.sink_attn_device_status(True) == 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (64, 8), (3, 3), (16, 1)])
+def test_ragged_prefill(causal, hq, hkv):
+    """Lengths that span several 128-tiles plus ragged tails, single tokens included."""
+    sa = require_gpu()
+    lens = [1, 127, 128, 129, 300, 513]
+    data = workloads.make_prefill(5, lens, hq, hkv, 64)
+    o, l = _run(sa, data, max(lens), 0.125, causal)
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"],
+                            0.125, causal)
+    assert_close(host(o), host(l), ro, rl, f"ragged prefill causal={causal} {hq}/{hkv}")
+    assert sa.sink_attn_device_status(True) == 0
+
+
+@pytest.mark.parametrize("sink_fill", [-np.inf, 20.0, 1.0e4])
+def test_prefill_sink_limits(sink_fill):
+    sa = require_gpu()
+    data = workloads.make_prefill(6, [200, 64], 8, 1, 64, sink_fill=sink_fill)
+    o, l = _run(sa, data, 200, 0.125, True)
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"],
+                            0.125, True)
+    assert_close(host(o), host(l), ro, rl, f"sink={sink_fill}")
+    if sink_fill == 1.0e4:
+        assert np.all(host(o) == 0.0)
+
+
+def test_prefill_large_scores_rescale():
+    """Scores that grow along the sequence force the running max to move many times."""
+    sa = require_gpu()
+    data = workloads.make_prefill(7, [1024], 8, 1, 64)
+    scale = 1.0  # 8x the usual scale: logits of O(10), max jumps across tiles
+    o, l = _run(sa, data, 1024, scale, True)
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"], scale, True)
+    assert_close(host(o), host(l), ro, rl, "large logits")
+
+
+def test_causal_prefill_config_sampled():
+    """4 x 8192 tokens, 64/8 heads, sinks with variance 2: sampled rows against the oracle."""
+    sa = require_gpu()
+    cfg = workloads.WORKLOADS["causal_prefill"]
+    lens = [cfg["seqlen"]] * cfg["batch"]
+    data = workloads.make_prefill(cfg["seed"], lens, cfg["hq"], cfg["hkv"], cfg["d"], cfg["sink_std"])
+    o, l = _run(sa, data, cfg["seqlen"], cfg["sm_scale"], True)
+    rng = np.random.default_rng(42)
+    t = int(data["cu_seqlens"][-1])
+    toks = list(rng.integers(0, t, 40)) + [0, 1, 127, 128, 8191, 8192, t - 1]
+    heads = list(rng.integers(0, cfg["hq"], len(toks)))
+    rows = [(int(a), int(b)) for a, b in zip(toks, heads)]
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"],
+                            cfg["sm_scale"], True, rows=rows)
+    go = host(o)[[r[0] for r in rows], [r[1] for r in rows]]
+    gl = host(l)[[r[0] for r in rows], [r[1] for r in rows]]
+    assert_close(go, gl, ro, rl, "causal prefill sampled")
+    assert np.isfinite(host(l)).all()
+    assert sa.sink_attn_device_status(True) == 0
