@@ -1,0 +1,457 @@
+"""Benchmark of the sink-attention hot path on GB300.
+
+One step = one pass of the decode path over the paged-decode workload
+(64 sequences x 4096 cached tokens, 64 query / 8 KV heads, head_dim 64, page
+size 16, seeded random page permutation): sink_attn_decode (split KV) then
+sink_attn_merge.  Headline metric: algorithmic decode bytes per second
+(KV cache + q + out + lse + page table), reported with the decode kernel's
+fraction of the measured HBM copy bandwidth.  The same JSON line carries the
+causal-prefill measurement (4 x 8192 tokens, 64/8 heads) in TFLOP/s against
+the measured dense bf16 peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on bounded samples of the same
+workload (host cores only).  For N > 1 (torchrun) every rank runs its own
+replica on its own GPU; nothing is exchanged but the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+# The CPU baseline runs the oracle single-threaded so that its core count is exact.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "sink-attn prefill TFLOP/s & decode KV GB/s on 1 GB300, % of roofline"
+DECODE = workloads.WORKLOADS["paged_decode"]
+PREFILL = workloads.WORKLOADS["causal_prefill"]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sust=p["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
+
+
+def decode_bytes(batch, kv_len, hq, hkv, d, max_pages):
+    """Algorithmic bytes of one decode step: KV read once, q, out, lse, page table, lens, sinks."""
+    kv = batch * kv_len * hkv * d * 2 * 2
+    return kv + batch * hq * d * 2 * 2 + batch * hq * 4 + batch * max_pages * 4 + batch * 4 + hq * 4
+
+
+def prefill_flops(batch, seqlen, hq, d):
+    pairs = seqlen * (seqlen + 1) // 2
+    return 4.0 * hq * d * pairs * batch
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), reasons=parts[4:9]))
+            except ValueError:
+                continue
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"], samples=0)
+        loaded = [r for r in rows if r["sm"] > 0.5 * r["smax"]] or rows
+        seen = set()
+        for r in loaded:
+            for n, v in zip(names[1:], r["reasons"][1:]):
+                if v.lower() == "active":
+                    seen.add(n)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in loaded),
+                    sm_max_mhz=max(r["smax"] for r in rows), reasons=sorted(seen),
+                    samples=len(loaded))
+
+
+# ----------------------------------------------------------------------------- our arm
+def to_dev(x, torch, device):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(x).to(device)
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import attention_softmax_sinks_gb300 as sa
+    from attention_softmax_sinks_gb300 import _build
+
+    _build.build()
+    sa.load_library()
+    torch.cuda.set_device(device)
+    pk = peaks()
+    cfg = DECODE
+    kv_lens = [cfg["kv_len"]] * cfg["batch"]
+    host = workloads.make_decode(cfg["seed"], kv_lens, cfg["hq"], cfg["hkv"], cfg["d"],
+                                 cfg["page_size"], cfg["sink_std"])
+    names = ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")
+    dev = {n: to_dev(host[n], torch, device) for n in names}
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    splits = sa.sink_attn_decode_splits(cfg["batch"], cfg["hkv"], cfg["kv_len"], cfg["page_size"], sms)
+    b, hq, d = cfg["batch"], cfg["hq"], cfg["d"]
+    part_o = torch.empty((b, splits, hq, d), dtype=torch.float32, device=device)
+    part_l = torch.empty((b, splits, hq), dtype=torch.float32, device=device)
+    out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((b, hq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    max_pages = host["page_table"].shape[1]
+    alg_bytes = decode_bytes(b, cfg["kv_len"], hq, cfg["hkv"], d, max_pages)
+
+    def step(ev=None):
+        if splits > 1:
+            if ev is not None:
+                ev[0].record(stream)
+            sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
+                                dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=splits,
+                                out=part_o, lse=part_l, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            sa.sink_attn_merge(part_o, part_l, out=out, lse=lse, stream=stream)
+        else:
+            if ev is not None:
+                ev[0].record(stream)
+            sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
+                                dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=1,
+                                out=out, lse=lse, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    kern_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = alg_bytes * world / (ms_per_step * 1e-3) / 1e9
+    dec_ms = sum(kern_ms) / len(kern_ms)
+    achieved = alg_bytes / (dec_ms * 1e-3) / 1e9
+    launches_per_step = 2 if splits > 1 else 1
+    status = sa.sink_attn_device_status(True)
+
+    # ---- end to end through the public API: pinned host inputs in, result out
+    pinned = {n: (torch.from_numpy(np.ascontiguousarray(host[n]).view(np.int16)).view(torch.bfloat16)
+                  if host[n].dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(host[n]))
+                  ).pin_memory() for n in names}
+    h_out = torch.empty((b, hq, d), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((b, hq), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    e2e_steps = max(3, min(20, args.steps))
+
+    def e2e_step():
+        for n in names:
+            dev[n].copy_(pinned[n], non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- causal prefill measured on its own (tensor-core bound kernel)
+    prefill = None
+    if not args.no_prefill:
+        prefill = bench_prefill(args, sa, torch, device, pk)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks, random page permutation)",
+        "config": {"workload": "paged_decode: 64 seqs x 4096 cached tokens, 1 new token each, "
+                               "64 query / 8 KV heads, head_dim 64, page 16, permuted pages",
+                   "batch": b, "kv_len": cfg["kv_len"], "num_qo_heads": hq, "num_kv_heads": cfg["hkv"],
+                   "head_dim": d, "page_size": cfg["page_size"], "num_splits": splits,
+                   "step": "sink_attn_decode + sink_attn_merge" if splits > 1 else "sink_attn_decode",
+                   "l2": "inputs larger than L2 (512 MiB KV cache per step, 129 MB L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "algorithmic_bytes_per_step": alg_bytes},
+        "roofline": {"bound": "hbm", "kernel": "sink_decode_kernel", "achieved": round(achieved, 1),
+                     "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
+                     "peak_source": pk["source"] + " (hbm_gbs, copy bandwidth)",
+                     "traffic": None, "kernel_ms": round(dec_ms, 5)},
+        "e2e": {"value": round(alg_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "pinned host -> device copies of every input, decode + merge, result -> host"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "device_status": status,
+    }
+    if prefill is not None:
+        line["prefill"] = prefill
+    return line
+
+
+def bench_prefill(args, sa, torch, device, pk):
+    cfg = PREFILL
+    lens = [cfg["seqlen"]] * cfg["batch"]
+    host = workloads.make_prefill(cfg["seed"], lens, cfg["hq"], cfg["hkv"], cfg["d"], cfg["sink_std"])
+    q, k, v = (to_dev(host[n], torch, device) for n in ("q", "k", "v"))
+    sinks = to_dev(host["sinks"], torch, device)
+    cu = to_dev(host["cu_seqlens"], torch, device)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=device)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    flops = prefill_flops(cfg["batch"], cfg["seqlen"], cfg["hq"], cfg["d"])
+
+    def run():
+        sa.sink_attn_prefill(q, k, v, sinks, cu, cfg["seqlen"], cfg["sm_scale"], causal=True,
+                             out=out, lse=lse, stream=stream)
+
+    for _ in range(max(3, args.warmup // 10)):
+        run()
+    steps = max(5, min(50, args.steps))
+    times = []
+    for _ in range(steps):
+        flush.zero_()  # evict the previous launch's K/V from L2
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize(device)
+    ms = [a.elapsed_time(b) for a, b in times]
+    avg = sum(ms) / len(ms)
+    tflops = flops / (avg * 1e-3) / 1e12
+    return {"workload": "causal_prefill: 4 x 8192 tokens, causal, 64 query / 8 KV heads, head_dim 64, "
+                        "sinks N(0, 2), out + fp32 lse",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(avg, 4),
+            "flops": flops, "l2": "flushed (256 MiB write) before every launch",
+            "roofline": {"bound": "tensor", "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2),
+                         "peak": pk["bf16"], "unit": "TFLOP/s", "frac": round(tflops / pk["bf16"], 4),
+                         "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)",
+                         "traffic": None},
+            "gpu_launches": steps}
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+def oracle_decode_sample(units, host):
+    """Oracle time for the first `units` (sequence, KV head) groups; returns (seconds, bytes)."""
+    import oracle
+    cfg = DECODE
+    g = cfg["hq"] // cfg["hkv"]
+    t0 = time.perf_counter()
+    done = 0
+    nbytes = 0
+    for u in range(units):
+        b, kvh = divmod(u % (cfg["batch"] * cfg["hkv"]), cfg["hkv"])
+        kv = int(host["kv_lens"][b])
+        kb = oracle.widen_bf16(oracle.gather_pages(host["k_pages"], host["page_table"][b], kv)[:, kvh])
+        vb = oracle.widen_bf16(oracle.gather_pages(host["v_pages"], host["page_table"][b], kv)[:, kvh])
+        qf = oracle.widen_bf16(host["q"][b, kvh * g:(kvh + 1) * g])
+        for hh in range(g):
+            oracle.attention_with_sink(qf[hh][None], kb, vb, float(host["sinks"][kvh * g + hh]),
+                                       cfg["sm_scale"])
+        done += 1
+        nbytes += kv * cfg["d"] * 2 * 2 + g * cfg["d"] * 2 * 2 + g * 4
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_baseline(budget_s=15.0):
+    cfg = DECODE
+    host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * cfg["batch"], cfg["hq"], cfg["hkv"],
+                                 cfg["d"], cfg["page_size"], cfg["sink_std"])
+    oracle_decode_sample(1, host)                      # warm the code paths
+    t4, _ = oracle_decode_sample(4, host)
+    units = max(1, min(cfg["batch"] * cfg["hkv"], int(budget_s / max(t4 / 4, 1e-4))))
+    secs, nbytes = oracle_decode_sample(units, host)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{units} of {cfg['batch'] * cfg['hkv']} (sequence, KV head) groups of the "
+                      f"paged-decode workload, {secs:.1f} s, fp64 numpy, 1 thread"}
+
+
+def run_reference(args):
+    cfg = DECODE
+    host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * cfg["batch"], cfg["hq"], cfg["hkv"],
+                                 cfg["d"], cfg["page_size"], cfg["sink_std"])
+    oracle_decode_sample(1, host)                      # warm the code paths
+    t4, _ = oracle_decode_sample(4, host)
+    per_step_budget = max(0.002, 150.0 / max(1, args.steps + args.warmup))
+    units = max(1, min(cfg["batch"] * cfg["hkv"], int(per_step_budget / max(t4 / 4, 1e-4))))
+    for _ in range(args.warmup):
+        oracle_decode_sample(units, host)
+    tot_s = 0.0
+    tot_b = 0
+    for _ in range(args.steps):
+        s, nb = oracle_decode_sample(units, host)
+        tot_s += s
+        tot_b += nb
+    value = tot_b / tot_s / 1e9
+    sample = f"{units} (sequence, KV head) group(s) of the paged-decode workload per step, fp64 numpy, 1 thread"
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "paged_decode: 64 seqs x 4096 cached tokens, 1 new token each, "
+                               "64 query / 8 KV heads, head_dim 64, page 16, permuted pages"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- ncu cases
+def run_profile_case(case):
+    """Small launches of one kernel for ncu captures: 2 warm-up launches, then 3.
+
+    decode:  32 sequences x 4096 tokens (256 MiB of KV, larger than L2), 64/8 heads, 4 splits.
+    prefill: 1 x 8192 tokens causal, 64/8 heads.
+    """
+    import torch
+    import attention_softmax_sinks_gb300 as sa
+    from attention_softmax_sinks_gb300 import _build
+    _build.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    if case == "decode":
+        cfg = DECODE
+        host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * 32, cfg["hq"], cfg["hkv"], cfg["d"],
+                                     cfg["page_size"], cfg["sink_std"])
+        dev = {n: to_dev(host[n], torch, device)
+               for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
+        for _ in range(5):
+            po, pl = sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
+                                         dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=4)
+            sa.sink_attn_merge(po, pl)
+    else:
+        cfg = PREFILL
+        host = workloads.make_prefill(cfg["seed"], [cfg["seqlen"]], cfg["hq"], cfg["hkv"], cfg["d"],
+                                      cfg["sink_std"])
+        q, k, v, sinks, cu = (to_dev(host[n], torch, device) for n in ("q", "k", "v", "sinks", "cu_seqlens"))
+        for _ in range(5):
+            sa.sink_attn_prefill(q, k, v, sinks, cu, cfg["seqlen"], cfg["sm_scale"], causal=True)
+    torch.cuda.synchronize(device)
+    print(json.dumps({"profile_case": case, "device_status": sa.sink_attn_device_status(True)}))
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+                    help="run a small case of one kernel for an ncu capture, then exit")
+    args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    line = run_ours(args, rank, world, device)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
