@@ -21,7 +21,7 @@ __all__ = [
     "SinkAttnError", "library_path", "load_library", "sink_attn_prefill", "sink_attn_prefill_paged",
     "sink_attn_decode", "sink_attn_merge", "sink_attn_decode_splits", "sink_attn_device_status",
     "sink_attn_set_wait_timeout_ns", "sink_attn_status_string", "sink_attn_abi_version",
-    "sink_attn_selftest_wait_timeout", "EXPORTED_SYMBOLS",
+    "sink_attn_selftest_wait_timeout", "sink_attn_decode_noalloc", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "sink_attn_prefill", "sink_attn_prefill_paged", "sink_attn_decode", "sink_attn_merge",
     "sink_attn_decode_splits", "sink_attn_device_status", "sink_attn_set_wait_timeout_ns",
     "sink_attn_status_string", "sink_attn_abi_version", "sink_attn_selftest_wait_timeout",
+    "sink_attn_decode_noalloc",
 )
 
 _p, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -47,6 +48,8 @@ _SIGNATURES = {
     "sink_attn_status_string": (ctypes.c_char_p, [_i]),
     "sink_attn_abi_version": (_i, []),
     "sink_attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _p]),
+    "sink_attn_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p,
+                                      _p]),
 }
 
 
@@ -187,6 +190,34 @@ def sink_attn_decode(q, paged_k, paged_v, page_table, kv_lens, sinks, sm_scale: 
         hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), s, _ptr(out), _ptr(lse),
         _stream(stream))
     _check(st, "sink_attn_decode")
+    return out, lse
+
+
+def sink_attn_decode_noalloc(q, paged_k, paged_v, page_table, kv_lens, sinks, sm_scale: float,
+                             num_splits: int, out=None, lse=None, return_lse: bool = True,
+                             stream=None):
+    """Split decode + merge in one library call that allocates no device memory.
+
+    For callers that cannot allocate when they enqueue work: the split partials
+    live in the library's fixed 8 MiB device array (batch * num_splits * Hq * 65
+    floats at most).  Pass preallocated ``out`` [B, Hq, 64] bf16 and ``lse``
+    [B, Hq] fp32 to keep this wrapper allocation-free as well.  Calls that
+    overlap on the GPU race on the shared array.
+    """
+    for name, tns, dt in (("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
+                          ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
+                          ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)):
+        _dev(tns, name, dt)
+    b, hq, d = q.shape
+    num_pages, hkv, page_size, _ = paged_k.shape
+    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((b, hq), dtype=torch.float32, device=q.device)
+    st = load_library().sink_attn_decode_noalloc(
+        _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
+        hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(num_splits), _ptr(out),
+        _ptr(lse), _stream(stream))
+    _check(st, "sink_attn_decode_noalloc")
     return out, lse
 
 

@@ -132,6 +132,7 @@ const char* sink_attn_status_string(sa_status s) {
     case SA_ERR_TIMEOUT: return "a device-side wait ran out of time";
     case SA_ERR_ALIGNMENT: return "a tensor pointer is not 16-byte aligned";
     case SA_ERR_CUDA: return "a CUDA runtime call failed";
+    case SA_ERR_CAPACITY: return "request exceeds the fixed device scratch of sink_attn_decode_noalloc";
   }
   return "unknown status";
 }

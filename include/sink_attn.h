@@ -53,7 +53,9 @@ typedef enum sa_status {
   SA_ERR_BOUNDS = 5,      /* device saw a bad page id or length (status word)  */
   SA_ERR_TIMEOUT = 6,     /* device wait ran out of time (status word)         */
   SA_ERR_ALIGNMENT = 7,   /* a tensor pointer is not 16-byte aligned           */
-  SA_ERR_CUDA = 8         /* a CUDA runtime call made by the library failed    */
+  SA_ERR_CUDA = 8,        /* a CUDA runtime call made by the library failed    */
+  SA_ERR_CAPACITY = 9     /* request larger than sink_attn_decode_noalloc's
+                             fixed device scratch                              */
 } sa_status;
 
 /*
@@ -142,6 +144,37 @@ sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged
 sa_status sink_attn_merge(const float* partial_o, const float* partial_lse, int batch,
                           int num_splits, int num_heads, int head_dim, void* out, float* lse_out,
                           cudaStream_t stream);
+
+/*
+ * Split-KV decode followed by the merge, in one call that allocates nothing.
+ * The page has no counterpart for this entry point; it exists for callers that
+ * cannot allocate device memory when they enqueue work (a plugin that is only
+ * handed its input and output buffers, a serving loop that bans allocation on
+ * its hot path because cudaMalloc may synchronise or fail).  Those callers
+ * cannot supply the fp32 partials that sink_attn_decode and sink_attn_merge
+ * exchange, so this call keeps them in a fixed device array inside the library
+ * (8 MiB, 2,097,152 floats, held on every GPU where the library is loaded
+ * until the process exits).
+ *
+ *  Arguments are those of sink_attn_decode, but `out` is always the final
+ *  bf16 [batch, num_qo_heads, head_dim] and `lse` the final fp32
+ *  [batch, num_qo_heads] (or NULL), whatever num_splits is.
+ *  Limit: batch * num_splits * num_qo_heads * (head_dim + 1) <= 2,097,152,
+ *  otherwise SA_ERR_CAPACITY and nothing is launched.  num_splits == 1 needs
+ *  no scratch and behaves exactly like sink_attn_decode.
+ *  No cudaMalloc, cudaFree or other allocation happens in this call.  The first
+ *  call on each device looks up the array's device address (a runtime query,
+ *  not an allocation); make that first call before any stream capture.
+ *  Every call shares the array, which keeps the previous call's contents; a
+ *  call writes every element it later reads, so nothing needs clearing, but
+ *  two calls that overlap on the GPU race on it: order them on one stream.
+ */
+sa_status sink_attn_decode_noalloc(const void* q, const void* paged_k, const void* paged_v,
+                                   const int32_t* page_table, const int32_t* kv_lens,
+                                   const float* sinks, int batch, int num_qo_heads,
+                                   int num_kv_heads, int head_dim, int page_size, int max_pages,
+                                   int num_pages, float sm_scale, int num_splits, void* out,
+                                   float* lse, cudaStream_t stream);
 
 /*
  * Host-only helper: a split count for sink_attn_decode that fills `num_sms`
