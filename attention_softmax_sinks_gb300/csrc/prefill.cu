@@ -46,12 +46,12 @@ struct __align__(1024) PrefillSmem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_full[2];
+  uint64_t kv_full[kStages];  // K_j and V_j landed                          (TMA tx)
+  uint64_t kv_empty[kStages]; // the MMAs reading stage j%kStages finished    (tcgen05.commit)
+  uint64_t s_full;            // S_0(j), S_1(j) are in TMEM                   (tcgen05.commit)
+  uint64_t s_free;            // both softmax warpgroups have read S(j)       (128 per tile)
+  uint64_t p_full;            // P(j) written and O rescaled in both tiles    (128 per tile)
+  uint64_t pv_done;           // O_t += P_t(j) V_j completed for both tiles   (tcgen05.commit)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -150,15 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.kv_full[s]), 1);
       mbar_init(smem_u32(&sm.kv_empty[s]), 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&sm.s_full[t]), 1);
-      mbar_init(smem_u32(&sm.p_full[t]), 128);
-      mbar_init(smem_u32(&sm.o_full[t]), 1);
-    }
+    mbar_init(smem_u32(&sm.s_full), 1);
+    mbar_init(smem_u32(&sm.s_free), 128 * w.ntiles);
+    mbar_init(smem_u32(&sm.p_full), 128 * w.ntiles);
+    mbar_init(smem_u32(&sm.pv_done), 1);
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort_flag = 0;
     sm.issued_tiles = 0;
@@ -172,7 +170,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-
+  // Producer / MMA warpgroup needs few registers; the softmax warpgroups hold a
+  // whole 128-wide score row each.  128*120 + 256*192 = 384*168 (launch total).
+  // Each setmaxnreg sits inside its own role branch so the compiler can give
+  // every region its own budget.
+  if (warp < 4) {
+    regs_dec<120>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -196,9 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t kbar = smem_u32(&sm.k_full[st]), vbar = smem_u32(&sm.v_full[st]);
-        mbar_arrive_expect_tx(kbar, kTileBytes);
-        mbar_arrive_expect_tx(vbar, kTileBytes);
+        const uint32_t kbar = smem_u32(&sm.kv_full[st]), vbar = kbar;
+        mbar_arrive_expect_tx(kbar, 2 * kTileBytes);
         if constexpr (kPaged) {
           for (int i = 0; i < kBlockK / kPageSize; ++i) {
             int lp = j * (kBlockK / kPageSize) + i;
@@ -232,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
           tc_mma_ss(tmem + kColS + t * 128, sw128_desc(q_addr[t] + kk * 32),
                     sw128_desc(k_addr + kk * 32), kIdescS, kk > 0);
-        tc_commit(smem_u32(&sm.s_full[t]));
       };
       auto issue_pv = [&](int j, int t) {
         const uint32_t v_addr = smem_u32(sm.v[j % kStages]);
@@ -241,39 +242,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_ts(tmem + kColO + t * 64, tmem + kColP + t * 64 + kk * 8,
                     sw128_desc(v_addr + kk * 16 * 128), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
-      if (ok) ok = wait_bar(smem_u32(&sm.k_full[0]), 0, a.timeout_ns, abort_flag);
+      if (ok) ok = wait_bar(smem_u32(&sm.kv_full[0]), 0, a.timeout_ns, abort_flag);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < w.ntiles; ++t) issue_s(0, t);
+        tc_commit(smem_u32(&sm.s_full));
       }
+      // Per KV tile j: S(j+1) for both query tiles as soon as both softmax
+      // warpgroups have read S(j) (so the next scores are ready when they need
+      // them), then O_t += P_t(j) V_j for both tiles.  One wait and one commit
+      // per step keeps the single issuing thread off the critical path.
       for (int j = 0; j < w.n_kv && ok; ++j) {
         const int st = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        ok = wait_bar(smem_u32(&sm.v_full[st]), ph, a.timeout_ns, abort_flag);
-        for (int t = 0; t < w.ntiles && ok; ++t) {
-          ok = wait_bar(smem_u32(&sm.p_full[t]), j & 1, a.timeout_ns, abort_flag);
+        if (j + 1 < w.n_kv) {
+          ok = wait_bar(smem_u32(&sm.kv_full[(j + 1) % kStages]), ((j + 1) / kStages) & 1,
+                        a.timeout_ns, abort_flag);
+          if (ok) ok = wait_bar(smem_u32(&sm.s_free), j & 1, a.timeout_ns, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(j, t);
-          if (j + 1 < w.n_kv) {
-            if (t == 0)
-              ok = wait_bar(smem_u32(&sm.k_full[(j + 1) % kStages]), ((j + 1) / kStages) & 1,
-                            a.timeout_ns, abort_flag);
-            if (ok) issue_s(j + 1, t);
-          }
+          for (int t = 0; t < w.ntiles; ++t) issue_s(j + 1, t);
+          tc_commit(smem_u32(&sm.s_full));
         }
-        if (ok) tc_commit(smem_u32(&sm.kv_empty[st]));
+        ok = wait_bar(smem_u32(&sm.p_full), j & 1, a.timeout_ns, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < w.ntiles; ++t) issue_pv(j, t);
+        tc_commit(smem_u32(&sm.pv_done));
+        tc_commit(smem_u32(&sm.kv_empty[st]));
       }
-      if (ok) {
-        for (int t = 0; t < w.ntiles; ++t) tc_commit(smem_u32(&sm.o_full[t]));
-      } else {
-        raise_status(a.status, kStatusTimeout);
-      }
+      if (!ok) raise_status(a.status, kStatusTimeout);
       // whatever happened, wait for every issued MMA before TMEM is released
       tc_commit(smem_u32(&sm.drain));
       mbar_wait(smem_u32(&sm.drain), 0, 2000000000ull);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    regs_inc<192>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - 4) >> 2;      // query tile of this warpgroup
     const int qw = warp & 3;            // TMEM lane quarter
@@ -289,32 +293,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s_col = lane_base + kColS + t * 128;
       const uint32_t o_col = lane_base + kColO + t * 64;
       const uint32_t p_col = lane_base + kColP + t * 64;
+      const uint64_t scale2 = f2(a.scale_log2, a.scale_log2);
       bool ok = true;
       for (int j = 0; j < w.n_kv; ++j) {
-        if (!wait_bar(smem_u32(&sm.s_full[t]), j & 1, a.timeout_ns, abort_flag)) {
+        if (!wait_bar(smem_u32(&sm.s_full), j & 1, a.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld32_at<0>(s_col + 0, sr);
+        tmem_ld32_at<32>(s_col + 32, sr);
+        tmem_ld32_at<64>(s_col + 64, sr);
+        tmem_ld32_at<96>(s_col + 96, sr);
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.s_free));  // the MMA may now overwrite S_t
         float s[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tmem_ld32(s_col + c * 32, u);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(u[e]);
-        }
-        tc_wait_ld();
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
         const int key0 = j * kBlockK;
         if (key0 + kBlockK - 1 > limit) {  // diagonal / tail tile: mask
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (key0 + c > limit) s[c] = kNegInf;
         }
-        float mx = s[0];
+        // row max: four independent 3-input max chains
+        float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        mx *= a.scale_log2;
+        for (int c = 4; c < 124; c += 8) {
+          m0 = fmax3(m0, s[c], s[c + 1]);
+          m1 = fmax3(m1, s[c + 2], s[c + 3]);
+          m2 = fmax3(m2, s[c + 4], s[c + 5]);
+          m3 = fmax3(m3, s[c + 6], s[c + 7]);
+        }
+        m0 = fmax3(m0, s[124], s[125]);
+        m1 = fmax3(m1, s[126], s[127]);
+        const float mx = fmax3(m0, m1, fmaxf(m2, m3)) * a.scale_log2;
         const bool grow = mx > m + kRescaleThreshold;
         float factor = 1.0f;
         if (grow) {
@@ -322,7 +337,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
           d *= factor;
         }
+        const float mu = (m == kNegInf) ? 0.0f : m;
+        const uint64_t negm2 = f2(-mu, -mu);
+        // p = 2^(s * scale - m), packed two per instruction; four partial row sums
+        uint32_t pk[64];
+        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float x0, x1;
+          f2_split(f2_fma(f2(s[2 * c], s[2 * c + 1]), scale2, negm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          const uint64_t pp = f2(p0, p1);
+          if ((c & 3) == 0) acc0 = f2_add(acc0, pp);
+          if ((c & 3) == 1) acc1 = f2_add(acc1, pp);
+          if ((c & 3) == 2) acc2 = f2_add(acc2, pp);
+          if ((c & 3) == 3) acc3 = f2_add(acc3, pp);
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        float r0, r1, r2, r3;
+        f2_split(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), r0, r1);
+        (void)r2;
+        (void)r3;
+        d += r0 + r1;
+        // P_t and O_t are still in use by the previous PV until it completes
+        if (j > 0 && !wait_bar(smem_u32(&sm.pv_done), (j - 1) & 1, a.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         if (j > 0 && __any_sync(0xffffffffu, grow)) {  // O holds earlier tiles: rescale it
+          const uint64_t f22 = f2(factor, factor);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t u[32];
@@ -330,34 +374,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_wait_ld();
             uint32_t lo[16], hi[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              lo[e] = __float_as_uint(__uint_as_float(u[e]) * factor);
-              hi[e] = __float_as_uint(__uint_as_float(u[16 + e]) * factor);
+            for (int e = 0; e < 16; e += 2) {
+              float a0, a1;
+              f2_split(f2_mul(f2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), f22), a0, a1);
+              lo[e] = __float_as_uint(a0);
+              lo[e + 1] = __float_as_uint(a1);
+              f2_split(f2_mul(f2(__uint_as_float(u[16 + e]), __uint_as_float(u[17 + e])), f22), a0, a1);
+              hi[e] = __float_as_uint(a0);
+              hi[e + 1] = __float_as_uint(a1);
             }
             tmem_st16(o_col + c * 32, lo);
             tmem_st16(o_col + c * 32 + 16, hi);
           }
         }
-        const float mu = (m == kNegInf) ? 0.0f : m;
-        float rs = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(s[c * 32 + 2 * e], a.scale_log2, -mu));
-            const float p1 = ex2(fmaf(s[c * 32 + 2 * e + 1], a.scale_log2, -mu));
-            rs += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(p_col + c * 16, pk);
-        }
-        d += rs;
+        tmem_st16_at<0>(p_col + 0, pk);
+        tmem_st16_at<16>(p_col + 16, pk);
+        tmem_st16_at<32>(p_col + 32, pk);
+        tmem_st16_at<48>(p_col + 48, pk);
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.p_full[t]));
+        mbar_arrive(smem_u32(&sm.p_full));
       }
-      if (ok && w.n_kv > 0) ok = wait_bar(smem_u32(&sm.o_full[t]), 0, a.timeout_ns, abort_flag);
+      if (ok && w.n_kv > 0)
+        ok = wait_bar(smem_u32(&sm.pv_done), (w.n_kv - 1) & 1, a.timeout_ns, abort_flag);
       if (ok) {
         tc_fence_after();
         const bool row_ok = i < w.q_len;
@@ -404,8 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int issued = sm.issued_tiles;
     for (int j = max(0, issued - kStages); j < issued; ++j) {
       const int st = j % kStages;
-      mbar_wait(smem_u32(&sm.k_full[st]), (j / kStages) & 1, 2000000000ull);
-      mbar_wait(smem_u32(&sm.v_full[st]), (j / kStages) & 1, 2000000000ull);
+      mbar_wait(smem_u32(&sm.kv_full[st]), (j / kStages) & 1, 2000000000ull);
     }
     mbar_wait(smem_u32(&sm.q_full), 0, 2000000000ull);
   }
