@@ -32,7 +32,7 @@ namespace {
 
 constexpr int kBlockQ = 128;
 constexpr int kBlockK = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr int kTileBytes = kBlockQ * kHeadDim * 2;  // 16 KiB
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384, kTmemCols = 512;
@@ -46,16 +46,17 @@ struct __align__(1024) PrefillSmem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint64_t q_full;
-  uint64_t kv_full[kStages];  // K_j and V_j landed                          (TMA tx)
-  uint64_t kv_empty[kStages]; // the MMAs reading stage j%kStages finished    (tcgen05.commit)
-  uint64_t s_full;            // S_0(j), S_1(j) are in TMEM                   (tcgen05.commit)
-  uint64_t s_free;            // both softmax warpgroups have read S(j)       (128 per tile)
-  uint64_t p_full;            // P(j) written and O rescaled in both tiles    (128 per tile)
-  uint64_t pv_done;           // O_t += P_t(j) V_j completed for both tiles   (tcgen05.commit)
-  uint64_t drain;
+  uint64_t kv_full[kStages];   // K_j and V_j landed                            (TMA tx)
+  uint64_t kv_empty[kStages];  // every query tile's MMAs on stage j finished   (1 commit per tile)
+  uint64_t s_full[2];          // S_t(j) is in TMEM                              (tcgen05.commit)
+  uint64_t s_free[2];          // softmax warpgroup t has read S_t(j)            (128 arrivals)
+  uint64_t p_full[2];          // P_t(j) written and O_t rescaled                (128 arrivals)
+  uint64_t pv_done[2];         // O_t += P_t(j) V_j completed                    (tcgen05.commit)
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
   int issued_tiles;
+  int issued_k;
 };
 
 // Shared-memory matrix descriptor, 128-byte swizzle, 8-row atoms 1024 B apart.
@@ -151,15 +152,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.q_full), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.kv_full[s]), 1);
-      mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+      mbar_init(smem_u32(&sm.kv_empty[s]), w.ntiles);
     }
-    mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.s_free), 128 * w.ntiles);
-    mbar_init(smem_u32(&sm.p_full), 128 * w.ntiles);
-    mbar_init(smem_u32(&sm.pv_done), 1);
-    mbar_init(smem_u32(&sm.drain), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&sm.s_full[t]), 1);
+      mbar_init(smem_u32(&sm.s_free[t]), 128);
+      mbar_init(smem_u32(&sm.p_full[t]), 128);
+      mbar_init(smem_u32(&sm.pv_done[t]), 1);
+      mbar_init(smem_u32(&sm.drain[t]), 1);
+    }
     sm.abort_flag = 0;
     sm.issued_tiles = 0;
+    sm.issued_k = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -199,8 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t kbar = smem_u32(&sm.kv_full[st]), vbar = kbar;
-        mbar_arrive_expect_tx(kbar, 2 * kTileBytes);
+        const uint32_t bar = smem_u32(&sm.kv_full[st]);
+        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
         if constexpr (kPaged) {
           for (int i = 0; i < kBlockK / kPageSize; ++i) {
             int lp = j * (kBlockK / kPageSize) + i;
@@ -211,69 +215,69 @@ __global__ void __launch_bounds__(kThreads, 1)
               phys = 0;
             }
             const int row = (phys * a.hkv + kvh) * kPageSize;
-            tma_load_2d(smem_u32(sm.k[st]) + i * kPageSize * 128, &kmap, 0, row, kbar, keep);
-            tma_load_2d(smem_u32(sm.v[st]) + i * kPageSize * 128, &vmap, 0, row, vbar, keep);
+            tma_load_2d(smem_u32(sm.k[st]) + i * kPageSize * 128, &kmap, 0, row, bar, keep);
+            tma_load_2d(smem_u32(sm.v[st]) + i * kPageSize * 128, &vmap, 0, row, bar, keep);
           }
         } else {
-          tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, kbar, keep);
-          tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, vbar, keep);
+          tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
+          tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
         }
         ++issued;
       }
       if (!ok) raise_status(a.status, kStatusTimeout);
       sm.issued_tiles = issued;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues query tile 0's MMAs, warp 2 tile 1's: the two tiles run
+    // as independent pipelines that only share K/V stages, so neither blocks
+    // the other's issue order.
+    const int t = warp - 1;
+    if (lane == 0 && t < w.ntiles) {
       bool ok = wait_bar(smem_u32(&sm.q_full), 0, a.timeout_ns, abort_flag);
-      const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
-      auto issue_s = [&](int j, int t) {
-        const uint32_t k_addr = smem_u32(sm.k[j % kStages]);
+      const uint32_t q_addr = smem_u32(sm.q[t]);
+      const uint32_t d_s = tmem + kColS + t * 128, d_o = tmem + kColO + t * 64, a_p = tmem + kColP + t * 64;
+      auto s_step = [&](int jj) {  // S_t(jj) = Q_t K_jj^T
+        ok = wait_bar(smem_u32(&sm.kv_full[jj % kStages]), (jj / kStages) & 1, a.timeout_ns, abort_flag);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm.k[jj % kStages]);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          tc_mma_ss(tmem + kColS + t * 128, sw128_desc(q_addr[t] + kk * 32),
-                    sw128_desc(k_addr + kk * 32), kIdescS, kk > 0);
+          tc_mma_ss(d_s, sw128_desc(q_addr + kk * 32), sw128_desc(k_addr + kk * 32), kIdescS, kk > 0);
+        tc_commit(smem_u32(&sm.s_full[t]));
       };
-      auto issue_pv = [&](int j, int t) {
-        const uint32_t v_addr = smem_u32(sm.v[j % kStages]);
+      auto pv_step = [&](int jj) {  // O_t += P_t(jj) V_jj
+        ok = wait_bar(smem_u32(&sm.p_full[t]), jj & 1, a.timeout_ns, abort_flag);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sm.v[jj % kStages]);
 #pragma unroll
         for (int kk = 0; kk < kBlockK / 16; ++kk)
-          tc_mma_ts(tmem + kColO + t * 64, tmem + kColP + t * 64 + kk * 8,
-                    sw128_desc(v_addr + kk * 16 * 128), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(d_o, a_p + kk * 8, sw128_desc(v_addr + kk * 16 * 128), kIdescPV,
+                    (jj > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&sm.pv_done[t]));
+        tc_commit(smem_u32(&sm.kv_empty[jj % kStages]));
       };
-      if (ok) ok = wait_bar(smem_u32(&sm.kv_full[0]), 0, a.timeout_ns, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < w.ntiles; ++t) issue_s(0, t);
-        tc_commit(smem_u32(&sm.s_full));
-      }
-      // Per KV tile j: S(j+1) for both query tiles as soon as both softmax
-      // warpgroups have read S(j) (so the next scores are ready when they need
-      // them), then O_t += P_t(j) V_j for both tiles.  One wait and one commit
-      // per step keeps the single issuing thread off the critical path.
+      // Tile 1 starts one softmax phase behind tile 0, so that one warpgroup
+      // computes (exp2 on the MUFU pipe) while the other loads and stores.
+      if (ok && t == 1) ok = wait_bar(smem_u32(&sm.p_full[0]), 0, a.timeout_ns, abort_flag);
+      if (ok) s_step(0);
+      // Step j: PV_t(j-1) (P_t(j-1) is ready before softmax(j) starts), then
+      // S_t(j+1) once softmax t has read S_t(j); both finish while softmax(j)
+      // still runs.
       for (int j = 0; j < w.n_kv && ok; ++j) {
-        const int st = j % kStages;
-        if (j + 1 < w.n_kv) {
-          ok = wait_bar(smem_u32(&sm.kv_full[(j + 1) % kStages]), ((j + 1) / kStages) & 1,
-                        a.timeout_ns, abort_flag);
-          if (ok) ok = wait_bar(smem_u32(&sm.s_free), j & 1, a.timeout_ns, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          for (int t = 0; t < w.ntiles; ++t) issue_s(j + 1, t);
-          tc_commit(smem_u32(&sm.s_full));
+        if (j >= 1) pv_step(j - 1);
+        if (ok && j + 1 < w.n_kv) {
+          ok = wait_bar(smem_u32(&sm.s_free[t]), j & 1, a.timeout_ns, abort_flag);
+          if (ok) s_step(j + 1);
         }
-        ok = wait_bar(smem_u32(&sm.p_full), j & 1, a.timeout_ns, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; t < w.ntiles; ++t) issue_pv(j, t);
-        tc_commit(smem_u32(&sm.pv_done));
-        tc_commit(smem_u32(&sm.kv_empty[st]));
       }
+      if (ok) pv_step(w.n_kv - 1);
       if (!ok) raise_status(a.status, kStatusTimeout);
-      // whatever happened, wait for every issued MMA before TMEM is released
-      tc_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, 2000000000ull);
+      // whatever happened, wait for every MMA this thread issued before TMEM is released
+      tc_commit(smem_u32(&sm.drain[t]));
+      mbar_wait(smem_u32(&sm.drain[t]), 0, 2000000000ull);
     }
   }
   } else {
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t scale2 = f2(a.scale_log2, a.scale_log2);
       bool ok = true;
       for (int j = 0; j < w.n_kv; ++j) {
-        if (!wait_bar(smem_u32(&sm.s_full), j & 1, a.timeout_ns, abort_flag)) {
+        if (!wait_bar(smem_u32(&sm.s_full[t]), j & 1, a.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32_at<96>(s_col + 96, sr);
         tc_wait_ld();
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.s_free));  // the MMA may now overwrite S_t
+        mbar_arrive(smem_u32(&sm.s_free[t]));  // the MMA may now overwrite S_t
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)r3;
         d += r0 + r1;
         // P_t and O_t are still in use by the previous PV until it completes
-        if (j > 0 && !wait_bar(smem_u32(&sm.pv_done), (j - 1) & 1, a.timeout_ns, abort_flag)) {
+        if (j > 0 && !wait_bar(smem_u32(&sm.pv_done[t]), (j - 1) & 1, a.timeout_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -393,10 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16_at<48>(p_col + 48, pk);
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.p_full));
+        mbar_arrive(smem_u32(&sm.p_full[t]));
       }
       if (ok && w.n_kv > 0)
-        ok = wait_bar(smem_u32(&sm.pv_done), (w.n_kv - 1) & 1, a.timeout_ns, abort_flag);
+        ok = wait_bar(smem_u32(&sm.pv_done[t]), (w.n_kv - 1) & 1, a.timeout_ns, abort_flag);
       if (ok) {
         tc_fence_after();
         const bool row_ok = i < w.q_len;
@@ -441,10 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // some role gave up: copies it never consumed may still be in flight; let
     // the last tile of every stage (and Q) land before shared memory is released
     const int issued = sm.issued_tiles;
-    for (int j = max(0, issued - kStages); j < issued; ++j) {
-      const int st = j % kStages;
-      mbar_wait(smem_u32(&sm.kv_full[st]), (j / kStages) & 1, 2000000000ull);
-    }
+    for (int j = max(0, issued - kStages); j < issued; ++j)
+      mbar_wait(smem_u32(&sm.kv_full[j % kStages]), (j / kStages) & 1, 2000000000ull);
     mbar_wait(smem_u32(&sm.q_full), 0, 2000000000ull);
   }
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
