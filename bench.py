@@ -52,6 +52,42 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
 
 
+def recorded_traffic(kernel, sources):
+    """DRAM bytes per full-size launch from profiles/traffic.txt, or None when the
+    kernel sources changed after the capture (or nothing was recorded)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in sources:
+        h.update(open(os.path.join(ROOT, "attention_softmax_sinks_gb300", "csrc", f), "rb").read())
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(item.split("=", 1) for item in line.split())
+        if kv.get("kernel") == kernel and kv.get("source_sha") == h.hexdigest()[:16]:
+            return int(kv["bytes_per_launch"])
+    return None
+
+
+def max_over_ranks(x, world):
+    """Largest value of x over all ranks (the job time is the slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step, world, ms_per_step):
+    """Whole-job GB/s: every rank processes its own replica in the (max) step time."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def decode_bytes(batch, kv_len, hq, hkv, d, max_pages):
     """Algorithmic bytes of one decode step: KV read once, q, out, lse, page table, lens, sinks."""
     kv = batch * kv_len * hkv * d * 2 * 2
@@ -190,14 +226,10 @@ def run_ours(args, rank, world, device):
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     kern_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = alg_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(alg_bytes, world, ms_per_step)
     dec_ms = sum(kern_ms) / len(kern_ms)
     achieved = alg_bytes / (dec_ms * 1e-3) / 1e9
     launches_per_step = 2 if splits > 1 else 1
@@ -228,11 +260,7 @@ def run_ours(args, rank, world, device):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
     # ---- causal prefill measured on its own (tensor-core bound kernel)
     prefill = None
@@ -255,8 +283,10 @@ def run_ours(args, rank, world, device):
         "roofline": {"bound": "hbm", "kernel": "sink_decode_kernel", "achieved": round(achieved, 1),
                      "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
                      "peak_source": pk["source"] + " (hbm_gbs, copy bandwidth)",
-                     "traffic": None, "kernel_ms": round(dec_ms, 5)},
-        "e2e": {"value": round(alg_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                     "traffic": recorded_traffic("sink_decode_kernel", ("decode.cu", "ptx.cuh", "internal.h")),
+                     "traffic_source": "profiles/traffic.txt (ncu capture of 32 of the 64 sequences, x2)",
+                     "kernel_ms": round(dec_ms, 5)},
+        "e2e": {"value": round(job_throughput(alg_bytes, world, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host -> device copies of every input, decode + merge, result -> host"},
         "gpu_launches": launches_per_step * args.steps,
@@ -307,7 +337,9 @@ def bench_prefill(args, sa, torch, device, pk):
             "roofline": {"bound": "tensor", "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2),
                          "peak": pk["bf16"], "unit": "TFLOP/s", "frac": round(tflops / pk["bf16"], 4),
                          "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)",
-                         "traffic": None},
+                         "traffic": recorded_traffic("sink_prefill_kernel", ("prefill.cu", "ptx.cuh", "internal.h")),
+                         "traffic_unit": "bytes per launch",
+                         "traffic_source": "profiles/traffic.txt (ncu capture of 1 of the 4 sequences, x4)"},
             "gpu_launches": steps}
 
 
