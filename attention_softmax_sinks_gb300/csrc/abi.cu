@@ -102,6 +102,30 @@ sa_status check_heads(int hq, int hkv, int head_dim) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+int g_sm_count[kMaxDevices] = {};
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+// Cluster size for an unsplit decode: CTAs of one (sequence, KV head) share its
+// KV range and merge on chip.  Grow (powers of two, <= 4: larger clusters
+// schedule poorly) while the grid is below about four waves of resident CTAs
+// and every CTA keeps >= 16 pages.
+int cluster_split(int units, int max_pages) {
+  const long long slots = 3LL * sm_count();
+  int c = 1;
+  while (c < 4 && static_cast<long long>(units) * c < 4 * slots && max_pages / (2 * c) >= 16) c *= 2;
+  return c;
+}
+
 // One warp waits on a barrier that nothing will ever complete, with the same
 // bounded wait the attention kernels use, and reports the timeout.
 __global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeout_ns) {
@@ -207,6 +231,7 @@ sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged
   a.max_pages = max_pages;
   a.num_pages = num_pages;
   a.num_splits = num_splits;
+  a.cluster = num_splits == 1 ? cluster_split(batch * num_kv_heads, max_pages) : 1;
   a.scale_log2 = sm_scale * kLog2e;
   a.timeout_ns = g_timeout_ns;
   if (sa_status s = status_ptr(&a.status)) return s;

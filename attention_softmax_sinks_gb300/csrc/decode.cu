@@ -38,6 +38,15 @@ struct MergeArea {  // aliases the ring once streaming is over
   float o[kWarps][NT * 8][kHeadDim];
 };
 
+// One CTA's combined state, read by cluster rank 0 through distributed shared memory.
+template <int NT>
+struct CtaState {
+  float m[NT * 8];
+  float d[NT * 8];
+  float o[NT * 8][kHeadDim];  // un-normalised: sum of p * v relative to m
+};
+constexpr int kCtaStateOffset = 32768;  // inside the ring, after the merge area
+
 constexpr size_t decode_smem_bytes() {
   return 1024 /*alignment slack*/ + kRingBytes + kWarps * kStages * sizeof(uint64_t);
 }
@@ -46,7 +55,8 @@ template <int NT>
 __global__ void __launch_bounds__(kWarps * 32)
     sink_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  static_assert(sizeof(MergeArea<NT>) <= kRingBytes, "merge area must fit in the ring");
+  static_assert(sizeof(MergeArea<NT>) <= kCtaStateOffset, "merge area must fit before the CTA state");
+  static_assert(kCtaStateOffset + sizeof(CtaState<NT>) <= kRingBytes, "CTA state must fit in the ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -63,7 +73,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     kv_len = kv_len < 0 ? 0 : cap;
   }
   const int n_pages = (kv_len + kPageSize - 1) / kPageSize;
-  const int per_split = (n_pages + a.num_splits - 1) / a.num_splits;
+  const bool clustered = a.cluster > 1;  // splits of one (sequence, KV head) form a cluster
+  const int n_split = clustered ? a.cluster : a.num_splits;
+  const int per_split = (n_pages + n_split - 1) / n_split;
   const int p_begin = min(split * per_split, n_pages);
   const int p_end = min(p_begin + per_split, n_pages);
   // this warp's pages: p_begin + warp + j * kWarps, j = 0 .. my_count-1
@@ -234,6 +246,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     __syncwarp();
   }
 
+  // the merge kernel that follows may start launching; it waits for this grid's results
+  pdl_launch_dependents();
+
   // ---- combine the lanes' partial denominators
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -263,6 +278,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   __syncthreads();
 
+  CtaState<NT>* cs = reinterpret_cast<CtaState<NT>*>(ring + kCtaStateOffset);
   for (int i = threadIdx.x; i < G * 16; i += kWarps * 32) {
     const int hh = i >> 4, d0 = (i & 15) * 4;
     float M = kNegInf;
@@ -279,6 +295,14 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[r] += mg->o[w][hh][d0 + r] * c;
       }
+    }
+    if (clustered) {  // hand the CTA's state to cluster rank 0
+      if (d0 == 0) {
+        cs->m[hh] = M;
+        cs->d[hh] = den;
+      }
+      *reinterpret_cast<float4*>(&cs->o[hh][d0]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      continue;
     }
     const float inv = den > 0.0f ? 1.0f / den : 0.0f;
     const float lse = den > 0.0f ? (M + lg2(den)) * kLn2 : kNegInf;
@@ -299,25 +323,77 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (d0 == 0) a.lse[row] = lse;
     }
   }
+  if (!clustered) return;
+
+  // ---- on-chip merge of the cluster's splits (same log-sum-exp combine as the merge kernel)
+  cluster_sync();  // every CTA's state is written
+  if (cluster_ctarank() == 0) {
+    const uint32_t cs_addr = smem_u32(cs);
+    for (int i = threadIdx.x; i < G * 16; i += kWarps * 32) {
+      const int hh = i >> 4, d0 = (i & 15) * 4;
+      const uint32_t off_m = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->m[hh]) - reinterpret_cast<uintptr_t>(cs));
+      const uint32_t off_d = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->d[hh]) - reinterpret_cast<uintptr_t>(cs));
+      const uint32_t off_o = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->o[hh][d0]) - reinterpret_cast<uintptr_t>(cs));
+      float M = kNegInf;
+      for (int r = 0; r < a.cluster; ++r) M = fmaxf(M, dsmem_ld(dsmem_addr(cs_addr + off_m, r)));
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float den = 0.0f;
+      if (M != kNegInf) {
+        for (int r = 0; r < a.cluster; ++r) {
+          const uint32_t base = dsmem_addr(cs_addr, r);
+          const float mr = dsmem_ld(base + off_m);
+          const float c = mr == M ? 1.0f : ex2(mr - M);
+          den += dsmem_ld(base + off_d) * c;
+          const float4 o4 = dsmem_ld4(base + off_o);
+          acc[0] += o4.x * c;
+          acc[1] += o4.y * c;
+          acc[2] += o4.z * c;
+          acc[3] += o4.w * c;
+        }
+      }
+      const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+      const int head = kvh * G + hh;
+      uint16_t* out = static_cast<uint16_t*>(a.out) +
+                      (static_cast<size_t>(b) * a.hq + head) * kHeadDim + d0;
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(out) = pk;
+      if (a.lse && d0 == 0)
+        a.lse[static_cast<size_t>(b) * a.hq + head] = den > 0.0f ? (M + lg2(den)) * kLn2 : kNegInf;
+    }
+  }
+  cluster_sync();  // rank 0 has read every CTA's shared memory; all may exit
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
                           cudaStream_t stream) {
-  const dim3 grid(a.num_splits, a.hkv, a.batch);
+  const bool clustered = a.cluster > 1;
+  const dim3 grid(clustered ? a.cluster : a.num_splits, a.hkv, a.batch);
   const size_t smem = decode_smem_bytes();
-  if (a.group <= 8) {
-    auto kern = sink_decode_kernel<1>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+  auto kern = a.group <= 8 ? sink_decode_kernel<1> : sink_decode_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (!clustered) {
     kern<<<grid, kWarps * 32, smem, stream>>>(kmap, vmap, a);
-  } else {
-    auto kern = sink_decode_kernel<2>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kWarps * 32, smem, stream>>>(kmap, vmap, a);
+    return cudaGetLastError();
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -18,6 +18,7 @@ struct DecodeArgs {
   void* out;
   float* lse;
   int batch, hq, hkv, group, max_pages, num_pages, num_splits;
+  int cluster;       // > 1 (num_splits == 1 only): KV range split across a CTA cluster, merged on chip
   float scale_log2;  // sm_scale * log2(e)
   unsigned* status;
   unsigned long long timeout_ns;

@@ -26,6 +26,9 @@ __device__ __forceinline__ float split_weight(float lse_s, float M) {
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32) sink_merge_kernel(const MergeArgs a) {
+  // launched with programmatic stream serialisation: the partials come from the
+  // preceding decode grid, so wait for it before reading them
+  pdl_wait_primary();
   const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= a.batch * a.heads) return;
@@ -68,7 +71,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32) sink_merge_kernel(const Merg
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   const int rows = a.batch * a.heads;
   const int blocks = (rows + kMergeWarps - 1) / kMergeWarps;
-  sink_merge_kernel<<<blocks, kMergeWarps * 32, 0, stream>>>(a);
+  // Programmatic dependent launch: the grid may be scheduled while the decode
+  // kernel before it drains, hiding the launch latency of this short kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sink_merge_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

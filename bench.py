@@ -215,18 +215,25 @@ def run_ours(args, rank, world, device):
     barrier()
     clocks = ClockSampler(device.index if device.index is not None else 0)
     clocks.start()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # pass 1 (headline): K steps, events only at the ends of the timed region, so the
+    # merge can overlap the decode tail (programmatic dependent launch)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step()
     t_end.record(stream)
     barrier()
-    clk = clocks.stop()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    # pass 2 (roofline): the same K steps with CUDA events around every decode launch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        step(evs[i])
+    barrier()
+    clk = clocks.stop()
     kern_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     ms_per_step = total_ms / args.steps
     value = job_throughput(alg_bytes, world, ms_per_step)
@@ -276,7 +283,9 @@ def run_ours(args, rank, world, device):
                                "64 query / 8 KV heads, head_dim 64, page 16, permuted pages",
                    "batch": b, "kv_len": cfg["kv_len"], "num_qo_heads": hq, "num_kv_heads": cfg["hkv"],
                    "head_dim": d, "page_size": cfg["page_size"], "num_splits": splits,
-                   "step": "sink_attn_decode + sink_attn_merge" if splits > 1 else "sink_attn_decode",
+                   "step": ("sink_attn_decode (split KV, fp32 partials) + sink_attn_merge" if splits > 1 else
+                            "sink_attn_decode: KV of each (sequence, KV head) split across a CTA cluster, "
+                            "sink in split 0, log-sum-exp merge on chip through distributed shared memory"),
                    "l2": "inputs larger than L2 (512 MiB KV cache per step, 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "algorithmic_bytes_per_step": alg_bytes},
@@ -285,11 +294,15 @@ def run_ours(args, rank, world, device):
                      "peak_source": pk["source"] + " (hbm_gbs, copy bandwidth)",
                      "traffic": recorded_traffic("sink_decode_kernel", ("decode.cu", "ptx.cuh", "internal.h")),
                      "traffic_source": "profiles/traffic.txt (ncu capture of 32 of the 64 sequences, x2)",
-                     "kernel_ms": round(dec_ms, 5)},
+                     "kernel_ms": round(dec_ms, 5),
+                     "kernel_timing": "CUDA events around each decode launch in a second pass of the "
+                                      "same K steps (events between the two kernels would stop the "
+                                      "merge overlapping the decode tail in the headline pass)"},
         "e2e": {"value": round(job_throughput(alg_bytes, world, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "pinned host -> device copies of every input, decode + merge, result -> host"},
         "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_note": "headline pass only; the roofline pass launches the same number again",
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "device_status": status,
     }

@@ -138,3 +138,4 @@ def test_decode_split_heuristic(lib):
     assert f(1, 8, 16, 16, 152) == 1           # a single page cannot be split
     assert f(8, 8, 131072, 16, 152) >= 16      # long context spreads over the GPU
     assert f(0, 8, 4096, 16, 152) == 1
+    assert f(64, 8, 4096, 16, 152) == 4        # 512 (sequence, KV head) units: four waves

@@ -30,6 +30,25 @@ def test_decode_small(hq, hkv, sink_fill):
     assert sa.sink_attn_device_status(True) == 0
 
 
+@pytest.mark.parametrize("batch,kv", [(1, 3000), (2, 777), (16, 2048), (64, 4096), (256, 600)])
+def test_unsplit_decode_with_on_chip_cluster_split(batch, kv):
+    """num_splits == 1: each sequence's KV range may be split across a CTA cluster
+    (sizes 1..4 depending on the shape) and merged on chip; parity with the oracle
+    and with the explicit split + merge path."""
+    sa = require_gpu()
+    lens = [kv - (7 * b) % 50 for b in range(batch)]
+    d = workloads.make_decode(17, lens, 64, 8, 64)
+    o, l, args = _run(sa, d, 0.125, 1)
+    ro, rl = oracle.decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["kv_lens"],
+                           d["sinks"], 0.125, batches=range(min(batch, 16)))
+    n = min(batch, 16)
+    assert_close(host(o)[:n], host(l)[:n], ro[:n], rl[:n], f"cluster decode batch={batch}")
+    po, pl = sa.sink_attn_decode(*args, 0.125, num_splits=5)
+    mo, ml = sa.sink_attn_merge(po, pl)
+    assert_close(host(o), host(l), host(mo), host(ml), f"cluster vs split+merge batch={batch}")
+    assert sa.sink_attn_device_status(True) == 0
+
+
 @pytest.mark.parametrize("splits", [2, 3, 7, 32, 200])
 def test_decode_split_partials_and_merge(splits):
     sa = require_gpu()
