@@ -270,9 +270,10 @@ def run_ours(args, rank, world, device):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
     # ---- causal prefill measured on its own (tensor-core bound kernel)
-    prefill = None
+    prefill = mixed = None
     if not args.no_prefill:
         prefill = bench_prefill(args, sa, torch, device, pk)
+        mixed = bench_mixed(args, sa, torch, device, pk)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -308,7 +309,58 @@ def run_ours(args, rank, world, device):
     }
     if prefill is not None:
         line["prefill"] = prefill
+    if mixed is not None:
+        line["mixed"] = mixed
     return line
+
+
+def bench_mixed(args, sa, torch, device, pk):
+    """Ragged mixed batch: 32 sequences, KV log-uniform in [1, 32768], half decode rows
+    (q_len 1) and half prefill chunks (q_len 128..2048), one sink_attn_prefill_paged call."""
+    cfg = workloads.WORKLOADS["ragged_mixed"]
+    q_lens, kv_lens = workloads.ragged_mixed_lengths(cfg["seed"] + 2, cfg["num_seqs"], cfg["max_kv"])
+    host = workloads.make_mixed(cfg["seed"], q_lens, kv_lens, cfg["hq"], cfg["hkv"], cfg["d"],
+                                cfg["page_size"], cfg["sink_std"])
+    names = ("q", "k_pages", "v_pages", "page_table", "cu_seqlens_q", "kv_lens", "sinks")
+    dv = {n: to_dev(host[n], torch, device) for n in names}
+    out = torch.empty_like(dv["q"])
+    lse = torch.empty((dv["q"].shape[0], cfg["hq"]), dtype=torch.float32, device=device)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    q = q_lens.astype(np.int64)
+    kv = kv_lens.astype(np.int64)
+    pairs = int((q * (kv - q) + q * (q + 1) // 2).sum())
+    flops = 4.0 * cfg["hq"] * cfg["d"] * pairs
+    nbytes = int((kv * cfg["hkv"] * cfg["d"] * 2 * 2).sum() + q.sum() * cfg["hq"] * cfg["d"] * 2 * 2)
+
+    def run():
+        sa.sink_attn_prefill_paged(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"],
+                                   dv["cu_seqlens_q"], dv["kv_lens"], dv["sinks"], int(q.max()),
+                                   cfg["sm_scale"], causal=True, out=out, lse=lse, stream=stream)
+
+    for _ in range(3):
+        run()
+    times = []
+    for _ in range(max(5, min(30, args.steps))):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize(device)
+    ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+    t_tc = flops / (pk["bf16"] * 1e12)
+    t_hbm = nbytes / (pk["hbm"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    return {"workload": "ragged_mixed: 32 seqs, KV log-uniform in [1, 32768], half decode rows, "
+                        "half 128-2048-token chunks, causal, 64/8 heads, page 16",
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "ms": round(ms, 4), "flops": flops, "bytes": nbytes, "decode_rows": int((q == 1).sum()),
+            "roofline": {"bound": bound, "frac": round(max(t_tc, t_hbm) / (ms * 1e-3), 4),
+                         "tensor_frac": round(t_tc / (ms * 1e-3), 4), "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
+                         "note": "frac = max(FLOPs / peak bf16, bytes / peak HBM) / time"},
+            "gpu_launches": len(times)}
 
 
 def bench_prefill(args, sa, torch, device, pk):
