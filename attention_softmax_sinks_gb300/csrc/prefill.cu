@@ -2,28 +2,38 @@
 //
 // Page "GPT-OSS on day 0", section "Kernels for GPT-OSS / Sink Attention":
 // attn = softmax(q k^T * sm_scale + sink) V with the head's sink seeding the
-// online softmax (running max m = sink, running denominator d = 1).  Here a
-// CTA owns one 128-token query block of the whole sequence, so the sink seeds
-// its single KV walk.
+// online softmax (running max m = sink, running denominator d = 1).  Each
+// work item is one 128-token query block of a whole sequence, so the sink
+// seeds its single KV walk.
 //
-// GB300 design (one CTA per SM, 12 warps, warp-specialised):
-//  * warp 0, lane 0 -- TMA producer: Q for two query heads of one KV group
-//    (two 128x64 tiles), then K and V tiles of 128 keys into a 3-stage ring
-//    (128-byte swizzle; contiguous tensors by one 3-D box, paged caches by
-//    eight 16-row page boxes through the page table).
-//  * warp 1 -- allocates 512 TMEM columns; lane 0 issues tcgen05.mma:
-//    S_t = Q_t K^T (M=128, N=128, K=64) into TMEM, and O_t += P_t V with P_t
-//    read from TMEM (M=128, N=64, K=128).  Completion is signalled through
-//    tcgen05.commit onto mbarriers.
+// GB300 design: 12 warps, warp-specialised, one CTA per SM at a time.
+//  * Schedule.  Work items are (sequence, 128-token query block, pair of
+//    query heads of one KV group).  Every CTA sorts the (sequence, query
+//    block) pairs by their number of KV tiles in shared memory (heaviest
+//    first; all CTAs compute the same order) and deals the items out in
+//    alternating (snake) order, so long rows of a ragged batch start first, the
+//    CTAs end up with nearly equal work and no scratch memory is needed.  The
+//    grid is persistent (one CTA per SM) except when every sequence has the
+//    same length and contiguous KV: then one CTA per item, heaviest first, and
+//    the hardware's block scheduler balances.
+//  * warp 0, lane 0 -- TMA producer: Q for two query heads (two 128x64 tiles,
+//    double-buffered across items), then K and V tiles of 128 keys into a
+//    4-stage ring shared by consecutive items (128-byte swizzle; contiguous
+//    tensors by one 3-D box, paged caches by eight 16-row page boxes through
+//    the page table).
+//  * warps 1 and 2, lane 0 -- one tcgen05 issuer per query tile t:
+//    S_t = Q_t K^T (M=128, N=128, K=64) into TMEM and O_t += P_t V with P_t
+//    read from TMEM (M=128, N=64, K=128); completion through tcgen05.commit.
+//    Per KV tile the issuer puts PV(j-1) ahead of S(j+1).
 //  * warps 4-7 and 8-11 -- one softmax warpgroup per query tile; thread r
 //    owns row r (TMEM lane r): reads its 128 scores, masks on diagonal tiles
 //    only, updates the running max lazily (O and d are rescaled only when the
-//    max grows by more than 2^8, which leaves the final O/d unchanged), writes
-//    P as bf16 into TMEM and finally stores out = O/d and lse = m + ln d.
+//    max grows by more than 2^8, which leaves O/d unchanged), writes P as bf16
+//    into TMEM and finally stores out = O/d and lse = m + ln d.
 //  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 //                P0 [384,448) P1 [448,512).
-//  The two query tiles let the tensor core work on one tile while the other
-//  warpgroup runs its softmax.
+#include <cstddef>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -35,6 +45,7 @@ constexpr int kBlockK = 128;
 constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr int kTileBytes = kBlockQ * kHeadDim * 2;  // 16 KiB
+constexpr int kMaxPairs = 1024;                     // (sequence, query block) pairs sorted on chip
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384, kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -42,22 +53,35 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct __align__(1024) PrefillSmem {
-  uint8_t q[2][kTileBytes];
+  uint8_t q0[2][kTileBytes];    // Q of even items [query tile]
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
-  uint64_t q_full;
-  uint64_t kv_full[kStages];   // K_j and V_j landed                            (TMA tx)
-  uint64_t kv_empty[kStages];  // every query tile's MMAs on stage j finished   (1 commit per tile)
-  uint64_t s_full[2];          // S_t(j) is in TMEM                              (tcgen05.commit)
-  uint64_t s_free[2];          // softmax warpgroup t has read S_t(j)            (128 arrivals)
-  uint64_t p_full[2];          // P_t(j) written and O_t rescaled                (128 arrivals)
-  uint64_t pv_done[2];         // O_t += P_t(j) V_j completed                    (tcgen05.commit)
+  uint64_t q_full[2];           // Q of the item landed                         (TMA tx)
+  uint64_t q_empty[2];          // every S of the item has read its Q           (1 commit per tile)
+  uint64_t kv_full[kStages];    // K_j and V_j landed                           (TMA tx)
+  uint64_t kv_empty[kStages];   // every query tile's MMAs on the stage finished (1 commit per tile)
+  uint64_t s_full[2];           // S_t(j) is in TMEM                             (tcgen05.commit)
+  uint64_t s_free[2];           // softmax warpgroup t has read S_t(j)           (128 arrivals)
+  uint64_t p_full[2];           // P_t(j) written and O_t rescaled               (128 arrivals)
+  uint64_t pv_done[2];          // O_t += P_t(j) V_j completed                   (tcgen05.commit)
+  uint64_t o_free[2];           // softmax warpgroup t has read O_t of its item  (128 arrivals)
   uint64_t drain[2];
+  int n_pairs;                  // pairs with work (a prefix of sortkey)
+  int sorted;                   // 0 when the items are in reverse query-block order
   uint32_t tmem_base;
   int abort_flag;
-  int issued_tiles;
-  int issued_k;
+  int issued_kv;                // producer bookkeeping for the drain
+  int issued_q;
+  // Only the persistent schedule uses what follows; a one-item-per-CTA launch
+  // allocates shared memory up to here (a smaller carve-out leaves more L1).
+  alignas(1024) uint8_t q1[2][kTileBytes];  // Q of odd items [query tile]
+  unsigned long long sortkey[kMaxPairs];    // (KV tiles << 32) | (~pair): heaviest first
 };
+constexpr size_t kSmemOnePerCta = offsetof(PrefillSmem, q1);
+
+__device__ __forceinline__ uint8_t* q_tile(PrefillSmem& sm, int parity, int t) {
+  return parity ? sm.q1[t] : sm.q0[t];
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle, 8-row atoms 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -96,44 +120,81 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t
 }
 
 struct WorkItem {
-  int b, h0, ntiles, q0, q_start, q_len, kv_len, n_kv;
-  bool valid;
+  int b, h0, q0, q_start, q_len, kv_len, n_kv;
 };
 
-__device__ __forceinline__ WorkItem decode_work(const PrefillArgs& a) {
-  WorkItem w;
-  const int tiles = (a.group % 2 == 0) ? 2 : 1;
-  const int n_hg = a.hq / tiles;
-  const int n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
-  const int idx = blockIdx.x;
-  const int per_qb = n_hg * a.batch;
-  const int qb = n_qb - 1 - idx / per_qb;  // longest (last) query blocks first
-  const int rem = idx % per_qb;
-  w.b = rem / n_hg;
-  w.h0 = (rem % n_hg) * tiles;
-  w.ntiles = tiles;
-  w.q0 = qb * kBlockQ;
-  w.valid = false;
-  const int qs = a.cu_q[w.b], qe = a.cu_q[w.b + 1];
-  w.q_start = qs;
-  w.q_len = qe - qs;
-  w.kv_len = a.paged ? a.kv_lens[w.b] : w.q_len;
-  const bool bad = qs < 0 || w.q_len < 0 || w.q_len > a.max_q || qe > a.total_q ||
-                   w.kv_len < w.q_len || (a.paged && w.kv_len > a.max_pages * kPageSize);
-  if (bad) {
-    if (threadIdx.x == 0 && w.q0 == 0 && w.h0 == 0) raise_status(a.status, kStatusBadLen);
-    return w;
+struct Schedule {
+  int n_qb, n_hg, tiles;
+};
+
+__device__ __forceinline__ Schedule make_schedule(const PrefillArgs& a) {
+  Schedule s;
+  s.tiles = (a.group % 2 == 0) ? 2 : 1;
+  s.n_hg = a.hq / s.tiles;
+  s.n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
+  return s;
+}
+
+// Lengths of sequence b; false when they break the declared bounds.
+__device__ __forceinline__ bool seq_lengths(const PrefillArgs& a, int b, int& qs, int& q_len,
+                                            int& kv_len) {
+  qs = a.cu_q[b];
+  const int qe = a.cu_q[b + 1];
+  q_len = qe - qs;
+  kv_len = a.paged ? a.kv_lens[b] : q_len;
+  const bool bad = qs < 0 || q_len < 0 || q_len > a.max_q || qe > a.total_q || kv_len < q_len ||
+                   (a.paged && kv_len > a.max_pages * kPageSize);
+  return !bad;
+}
+
+// KV tiles a query block visits (0 when the block is empty): the keys visible to
+// its last row under bottom-right causal alignment, or all keys.
+__device__ __forceinline__ int block_tiles(const PrefillArgs& a, int q0, int q_len, int kv_len) {
+  if (q0 >= q_len) return 0;
+  const int last_row = min(q0 + kBlockQ, q_len) - 1;
+  const int kv_end = a.causal ? min(kv_len, last_row + kv_len - q_len + 1) : kv_len;
+  return (kv_end + kBlockK - 1) / kBlockK;
+}
+
+// Work item k of the schedule (k < n_pairs * n_hg).  n_kv == 0 marks an item
+// with nothing to do (only possible in the unsorted fallback order).
+__device__ __forceinline__ WorkItem item_at(const PrefillArgs& a, const PrefillSmem& sm,
+                                            const Schedule& sc, int k) {
+  const int rank = k / sc.n_hg, hg = k % sc.n_hg;
+  int b, qb;
+  if (sm.sorted) {
+    const int pair = static_cast<int>(~static_cast<uint32_t>(sm.sortkey[rank] & 0xffffffffu));
+    b = pair / sc.n_qb;
+    qb = pair % sc.n_qb;
+  } else {  // reverse query-block order
+    qb = sc.n_qb - 1 - rank / a.batch;
+    b = rank % a.batch;
   }
-  if (w.q0 >= w.q_len) return w;
-  // keys visible to the last row of this block (bottom-right causal alignment)
-  const int last_row = min(w.q0 + kBlockQ, w.q_len) - 1;
-  const int kv_end = a.causal ? min(w.kv_len, last_row + w.kv_len - w.q_len + 1) : w.kv_len;
-  w.n_kv = (kv_end + kBlockK - 1) / kBlockK;
-  w.valid = true;
+  WorkItem w;
+  w.b = b;
+  w.h0 = hg * sc.tiles;
+  w.q0 = qb * kBlockQ;
+  int qs, q_len, kv_len;
+  const bool good = seq_lengths(a, b, qs, q_len, kv_len);
+  w.q_start = qs;
+  w.q_len = q_len;
+  w.kv_len = kv_len;
+  w.n_kv = good ? block_tiles(a, w.q0, q_len, kv_len) : 0;
   return w;
 }
 
-template <bool kPaged>
+// The r-th item of CTA c in "snake" order: rounds of gridDim.x items are
+// dealt alternately left-to-right and right-to-left, which balances the sorted
+// (heaviest first) list across CTAs.  Returns -1 past the end.
+__device__ __forceinline__ int snake_item(int r, int n_items) {
+  const int g = gridDim.x, c = blockIdx.x;
+  const int base = r * g;
+  if (base >= n_items) return -1;
+  const int k = base + ((r & 1) ? g - 1 - c : c);
+  return k < n_items ? k : -2;  // -2: this CTA sits out the last, partial round
+}
+
+template <bool kPaged, bool kPersistent>
 __global__ void __launch_bounds__(kThreads, 1)
     sink_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                         const __grid_constant__ CUtensorMap kmap,
@@ -141,29 +202,107 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const WorkItem w = decode_work(a);
-  if (!w.valid) return;  // uniform across the CTA, before any barrier or TMEM use
-
+  const Schedule sc = make_schedule(a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kvh = w.h0 / a.group;
-  volatile int* abort_flag = &sm.abort_flag;
 
+  // ---------------------------------------------------------------- schedule
+  const int pairs = a.batch * sc.n_qb;
+  int n_items;
+  if constexpr (kPersistent) {
+    // Sort the (sequence, query block) pairs by KV tiles, heaviest first.
+    // Every CTA computes the same order; a pair with no work sorts last (key 0).
+    if (pairs <= kMaxPairs) {
+      int cap = 1;
+      while (cap < pairs) cap <<= 1;
+      for (int p = threadIdx.x; p < cap; p += kThreads) {
+        unsigned long long key = 0;
+        if (p < pairs) {
+          const int b = p / sc.n_qb, qb = p % sc.n_qb;
+          int qs, q_len, kv_len;
+          int tiles = 0;
+          if (seq_lengths(a, b, qs, q_len, kv_len)) tiles = block_tiles(a, qb * kBlockQ, q_len, kv_len);
+          else if (qb == 0 && blockIdx.x == 0) raise_status(a.status, kStatusBadLen);
+          key = tiles > 0 ? (static_cast<unsigned long long>(tiles) << 32) | (~static_cast<uint32_t>(p))
+                          : 0ull;
+        }
+        sm.sortkey[p] = key;
+      }
+      __syncthreads();
+      for (int size = 2; size <= cap; size <<= 1) {  // bitonic sort, descending
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int i = threadIdx.x; i < cap; i += kThreads) {
+            const int jx = i ^ stride;
+            if (jx > i) {
+              const bool desc = (i & size) == 0;
+              const unsigned long long x = sm.sortkey[i], y = sm.sortkey[jx];
+              if (desc ? (x < y) : (x > y)) {
+                sm.sortkey[i] = y;
+                sm.sortkey[jx] = x;
+              }
+            }
+          }
+          __syncthreads();
+        }
+      }
+      if (threadIdx.x == 0) {
+        int n = 0;
+        while (n < pairs && sm.sortkey[n] != 0ull) ++n;
+        sm.n_pairs = n;
+        sm.sorted = 1;
+      }
+    } else if (threadIdx.x == 0) {
+      // too many pairs to sort on chip: reverse query-block order (empty items skipped)
+      sm.n_pairs = pairs;
+      sm.sorted = 0;
+      if (blockIdx.x == 0)
+        for (int b = 0; b < a.batch; ++b) {
+          int qs, q_len, kv_len;
+          if (!seq_lengths(a, b, qs, q_len, kv_len)) raise_status(a.status, kStatusBadLen);
+        }
+    }
+    __syncthreads();
+    n_items = sm.n_pairs * sc.n_hg;
+    if (static_cast<int>(blockIdx.x) >= n_items) return;  // uniform; before any barrier or TMEM use
+  } else {
+    // one item per CTA, reverse query-block order (heaviest first for causal blocks)
+    if (threadIdx.x == 0) sm.sorted = 0;
+    __syncthreads();
+    n_items = pairs * sc.n_hg;
+  }
+  // the one item of a non-persistent CTA
+  const WorkItem w0 = kPersistent ? WorkItem{} : item_at(a, sm, sc, blockIdx.x);
+  if (!kPersistent) {
+    if (w0.n_kv == 0) {
+      if (threadIdx.x == 0 && w0.q0 == 0 && w0.h0 == 0) {
+        int qs, q_len, kv_len;
+        if (!seq_lengths(a, w0.b, qs, q_len, kv_len)) raise_status(a.status, kStatusBadLen);
+      }
+      return;  // uniform across the CTA
+    }
+  }
+
+  volatile int* abort_flag = &sm.abort_flag;
+  const int ntiles = sc.tiles;
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sm.q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.q_full[i]), 1);
+      mbar_init(smem_u32(&sm.q_empty[i]), ntiles);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.kv_full[s]), 1);
-      mbar_init(smem_u32(&sm.kv_empty[s]), w.ntiles);
+      mbar_init(smem_u32(&sm.kv_empty[s]), ntiles);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&sm.s_full[t]), 1);
       mbar_init(smem_u32(&sm.s_free[t]), 128);
       mbar_init(smem_u32(&sm.p_full[t]), 128);
       mbar_init(smem_u32(&sm.pv_done[t]), 1);
+      mbar_init(smem_u32(&sm.o_free[t]), 128);
       mbar_init(smem_u32(&sm.drain[t]), 1);
     }
     sm.abort_flag = 0;
-    sm.issued_tiles = 0;
-    sm.issued_k = 0;
+    sm.issued_kv = 0;
+    sm.issued_q = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -174,234 +313,267 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+
+  // Runs `body(item, item_index_of_this_cta, first_global_kv_tile)` for every
+  // item of this CTA: the single item of a non-persistent CTA, or the snake
+  // sequence of the persistent schedule.  Stops when body returns false.
+  auto for_items = [&](auto&& body) {
+    if constexpr (!kPersistent) {
+      body(w0, 0, 0);
+    } else {
+      int it = 0, g = 0;
+      for (int rr = 0;; ++rr) {
+        const int k = snake_item(rr, n_items);
+        if (k == -1) break;
+        if (k < 0) continue;
+        const WorkItem w = item_at(a, sm, sc, k);
+        if (w.n_kv == 0) continue;
+        if (!body(w, it, g)) break;
+        ++it;
+        g += w.n_kv;
+      }
+    }
+  };
+
   // Producer / MMA warpgroup needs few registers; the softmax warpgroups hold a
   // whole 128-wide score row each.  128*120 + 256*192 = 384*168 (launch total).
   // Each setmaxnreg sits inside its own role branch so the compiler can give
   // every region its own budget.
   if (warp < 4) {
     regs_dec<120>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      const uint64_t keep = l2_policy_evict_last();  // K/V are re-read by the group's other heads
-      const uint64_t once = l2_policy_evict_first();
-      const uint32_t qbar = smem_u32(&sm.q_full);
-      mbar_arrive_expect_tx(qbar, w.ntiles * kTileBytes);
-      for (int t = 0; t < w.ntiles; ++t)
-        tma_load_3d(smem_u32(sm.q[t]), &qmap, 0, w.h0 + t, w.q_start + w.q0, qbar, once);
-      const int32_t* ptab = kPaged ? a.page_table + static_cast<size_t>(w.b) * a.max_pages : nullptr;
-      const int seq_pages = (w.kv_len + kPageSize - 1) / kPageSize;
-      int issued = 0;
-      bool ok = true;
-      for (int j = 0; j < w.n_kv && ok; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages &&
-            !wait_bar(smem_u32(&sm.kv_empty[st]), ((j / kStages) - 1) & 1, a.timeout_ns, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t bar = smem_u32(&sm.kv_full[st]);
-        mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-        if constexpr (kPaged) {
-          for (int i = 0; i < kBlockK / kPageSize; ++i) {
-            int lp = j * (kBlockK / kPageSize) + i;
-            if (lp >= seq_pages) lp = seq_pages - 1;  // ragged tail: any valid page, masked later
-            int phys = ptab[lp];
-            if (phys < 0 || phys >= a.num_pages) {
-              raise_status(a.status, kStatusBadPage);
-              phys = 0;
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        const uint64_t keep = l2_policy_evict_last();  // K/V are re-read by the group's other heads
+        const uint64_t once = l2_policy_evict_first();
+        bool ok = true;
+        for_items([&](const WorkItem& w, int it, int g) {
+          const int kvh = w.h0 / a.group;
+          const int qb = it & 1;
+          if (it >= 2 &&
+              !wait_bar(smem_u32(&sm.q_empty[qb]), ((it >> 1) - 1) & 1, a.timeout_ns, abort_flag))
+            return ok = false;
+          const uint32_t qbar = smem_u32(&sm.q_full[qb]);
+          mbar_arrive_expect_tx(qbar, ntiles * kTileBytes);
+          for (int t = 0; t < ntiles; ++t)
+            tma_load_3d(smem_u32(q_tile(sm, qb, t)), &qmap, 0, w.h0 + t, w.q_start + w.q0, qbar, once);
+          sm.issued_q = it + 1;
+          const int32_t* ptab = kPaged ? a.page_table + static_cast<size_t>(w.b) * a.max_pages : nullptr;
+          const int seq_pages = (w.kv_len + kPageSize - 1) / kPageSize;
+          for (int j = 0; j < w.n_kv; ++j) {
+            const int gg = g + j, st = gg % kStages;
+            if (gg >= kStages &&
+                !wait_bar(smem_u32(&sm.kv_empty[st]), ((gg / kStages) - 1) & 1, a.timeout_ns, abort_flag))
+              return ok = false;
+            const uint32_t bar = smem_u32(&sm.kv_full[st]);
+            mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+            if constexpr (kPaged) {
+              for (int i = 0; i < kBlockK / kPageSize; ++i) {
+                int lp = j * (kBlockK / kPageSize) + i;
+                if (lp >= seq_pages) lp = seq_pages - 1;  // ragged tail: any valid page, masked later
+                int phys = ptab[lp];
+                if (phys < 0 || phys >= a.num_pages) {
+                  raise_status(a.status, kStatusBadPage);
+                  phys = 0;
+                }
+                const int row = (phys * a.hkv + kvh) * kPageSize;
+                tma_load_2d(smem_u32(sm.k[st]) + i * kPageSize * 128, &kmap, 0, row, bar, keep);
+                tma_load_2d(smem_u32(sm.v[st]) + i * kPageSize * 128, &vmap, 0, row, bar, keep);
+              }
+            } else {
+              tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
+              tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
             }
-            const int row = (phys * a.hkv + kvh) * kPageSize;
-            tma_load_2d(smem_u32(sm.k[st]) + i * kPageSize * 128, &kmap, 0, row, bar, keep);
-            tma_load_2d(smem_u32(sm.v[st]) + i * kPageSize * 128, &vmap, 0, row, bar, keep);
+            sm.issued_kv = gg + 1;
           }
-        } else {
-          tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
-          tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
-        }
-        ++issued;
+          return true;
+        });
+        if (!ok) raise_status(a.status, kStatusTimeout);
       }
-      if (!ok) raise_status(a.status, kStatusTimeout);
-      sm.issued_tiles = issued;
-    }
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ MMA issuers
-    // Warp 1 issues query tile 0's MMAs, warp 2 tile 1's: the two tiles run
-    // as independent pipelines that only share K/V stages, so neither blocks
-    // the other's issue order.
-    const int t = warp - 1;
-    if (lane == 0 && t < w.ntiles) {
-      bool ok = wait_bar(smem_u32(&sm.q_full), 0, a.timeout_ns, abort_flag);
-      const uint32_t q_addr = smem_u32(sm.q[t]);
-      const uint32_t d_s = tmem + kColS + t * 128, d_o = tmem + kColO + t * 64, a_p = tmem + kColP + t * 64;
-      auto s_step = [&](int jj) {  // S_t(jj) = Q_t K_jj^T
-        ok = wait_bar(smem_u32(&sm.kv_full[jj % kStages]), (jj / kStages) & 1, a.timeout_ns, abort_flag);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sm.k[jj % kStages]);
+    } else if (warp == 1 || warp == 2) {
+      // ---------------------------------------------------------- MMA issuers
+      // Warp 1 issues query tile 0's MMAs, warp 2 tile 1's: the two tiles run
+      // as independent pipelines that only share Q buffers and K/V stages.
+      const int t = warp - 1;
+      if (lane == 0 && t < ntiles) {
+        bool ok = true;
+        const uint32_t d_s = tmem + kColS + t * 128, d_o = tmem + kColO + t * 64;
+        const uint32_t a_p = tmem + kColP + t * 64;
+        for_items([&](const WorkItem& w, int it, int g) {
+          const int qb = it & 1;
+          ok = wait_bar(smem_u32(&sm.q_full[qb]), (it >> 1) & 1, a.timeout_ns, abort_flag);
+          if (!ok) return false;
+          const uint32_t q_addr = smem_u32(q_tile(sm, qb, t));
+          auto s_step = [&](int jj) {  // S_t(jj) = Q_t K_jj^T
+            const int gg = g + jj;
+            ok = wait_bar(smem_u32(&sm.kv_full[gg % kStages]), (gg / kStages) & 1, a.timeout_ns,
+                          abort_flag);
+            if (!ok) return;
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(sm.k[gg % kStages]);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          tc_mma_ss(d_s, sw128_desc(q_addr + kk * 32), sw128_desc(k_addr + kk * 32), kIdescS, kk > 0);
-        tc_commit(smem_u32(&sm.s_full[t]));
-      };
-      auto pv_step = [&](int jj) {  // O_t += P_t(jj) V_jj
-        ok = wait_bar(smem_u32(&sm.p_full[t]), jj & 1, a.timeout_ns, abort_flag);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sm.v[jj % kStages]);
+            for (int kk = 0; kk < kHeadDim / 16; ++kk)
+              tc_mma_ss(d_s, sw128_desc(q_addr + kk * 32), sw128_desc(k_addr + kk * 32), kIdescS, kk > 0);
+            tc_commit(smem_u32(&sm.s_full[t]));
+          };
+          auto pv_step = [&](int jj) {  // O_t += P_t(jj) V_jj
+            const int gg = g + jj;
+            if (jj == 0 && it > 0)  // O_t still holds the previous item until its epilogue read it
+              ok = wait_bar(smem_u32(&sm.o_free[t]), (it - 1) & 1, a.timeout_ns, abort_flag);
+            if (ok) ok = wait_bar(smem_u32(&sm.p_full[t]), gg & 1, a.timeout_ns, abort_flag);
+            if (!ok) return;
+            tc_fence_after();
+            const uint32_t v_addr = smem_u32(sm.v[gg % kStages]);
 #pragma unroll
-        for (int kk = 0; kk < kBlockK / 16; ++kk)
-          tc_mma_ts(d_o, a_p + kk * 8, sw128_desc(v_addr + kk * 16 * 128), kIdescPV,
-                    (jj > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(smem_u32(&sm.pv_done[t]));
-        tc_commit(smem_u32(&sm.kv_empty[jj % kStages]));
-      };
-      // Tile 1 starts one softmax phase behind tile 0, so that one warpgroup
-      // computes (exp2 on the MUFU pipe) while the other loads and stores.
-      if (ok && t == 1) ok = wait_bar(smem_u32(&sm.p_full[0]), 0, a.timeout_ns, abort_flag);
-      if (ok) s_step(0);
-      // Step j: PV_t(j-1) (P_t(j-1) is ready before softmax(j) starts), then
-      // S_t(j+1) once softmax t has read S_t(j); both finish while softmax(j)
-      // still runs.
-      for (int j = 0; j < w.n_kv && ok; ++j) {
-        if (j >= 1) pv_step(j - 1);
-        if (ok && j + 1 < w.n_kv) {
-          ok = wait_bar(smem_u32(&sm.s_free[t]), j & 1, a.timeout_ns, abort_flag);
-          if (ok) s_step(j + 1);
-        }
+            for (int kk = 0; kk < kBlockK / 16; ++kk)
+              tc_mma_ts(d_o, a_p + kk * 8, sw128_desc(v_addr + kk * 16 * 128), kIdescPV,
+                        (jj > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(smem_u32(&sm.pv_done[t]));
+            tc_commit(smem_u32(&sm.kv_empty[gg % kStages]));
+          };
+          // The very first tile of tile 1 starts one softmax phase behind tile 0,
+          // so one warpgroup runs exp2 while the other loads and stores.
+          if (it == 0 && t == 1) ok = wait_bar(smem_u32(&sm.p_full[0]), 0, a.timeout_ns, abort_flag);
+          if (ok) s_step(0);
+          // Step j: PV_t(j-1) (P_t(j-1) is ready before softmax(j) starts), then
+          // S_t(j+1) once softmax t has read S_t(j).
+          for (int j = 0; j < w.n_kv && ok; ++j) {
+            if (j >= 1) pv_step(j - 1);
+            if (ok && j + 1 < w.n_kv) {
+              ok = wait_bar(smem_u32(&sm.s_free[t]), (g + j) & 1, a.timeout_ns, abort_flag);
+              if (ok) s_step(j + 1);
+            }
+          }
+          if (ok) pv_step(w.n_kv - 1);
+          if (ok && kPersistent) tc_commit(smem_u32(&sm.q_empty[qb]));  // every S of the item issued
+          return ok;
+        });
+        if (!ok) raise_status(a.status, kStatusTimeout);
+        // whatever happened, wait for every MMA this thread issued before TMEM is released
+        tc_commit(smem_u32(&sm.drain[t]));
+        mbar_wait(smem_u32(&sm.drain[t]), 0, 2000000000ull);
       }
-      if (ok) pv_step(w.n_kv - 1);
-      if (!ok) raise_status(a.status, kStatusTimeout);
-      // whatever happened, wait for every MMA this thread issued before TMEM is released
-      tc_commit(smem_u32(&sm.drain[t]));
-      mbar_wait(smem_u32(&sm.drain[t]), 0, 2000000000ull);
     }
-  }
   } else {
     regs_inc<192>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - 4) >> 2;      // query tile of this warpgroup
     const int qw = warp & 3;            // TMEM lane quarter
     const int r = qw * 32 + lane;       // row within the block
-    if (t < w.ntiles) {
-      const int h = w.h0 + t;
-      const int i = w.q0 + r;           // query index within the sequence
-      const int limit = a.causal ? min(i + w.kv_len - w.q_len, w.kv_len - 1) : w.kv_len - 1;
-      const float sink = a.sinks[h] * kLog2e;
-      float m = sink;                                 // running max (log2 units)
-      float d = (sink == kNegInf) ? 0.0f : 1.0f;      // running denominator
+    if (t < ntiles) {
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
       const uint32_t s_col = lane_base + kColS + t * 128;
       const uint32_t o_col = lane_base + kColO + t * 64;
       const uint32_t p_col = lane_base + kColP + t * 64;
       const uint64_t scale2 = f2(a.scale_log2, a.scale_log2);
       bool ok = true;
-      for (int j = 0; j < w.n_kv; ++j) {
-        if (!wait_bar(smem_u32(&sm.s_full[t]), j & 1, a.timeout_ns, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld32_at<0>(s_col + 0, sr);
-        tmem_ld32_at<32>(s_col + 32, sr);
-        tmem_ld32_at<64>(s_col + 64, sr);
-        tmem_ld32_at<96>(s_col + 96, sr);
-        tc_wait_ld();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm.s_free[t]));  // the MMA may now overwrite S_t
-        float s[128];
+      for_items([&](const WorkItem& w, int it, int g) {
+        const int h = w.h0 + t;
+        const int i = w.q0 + r;           // query index within the sequence
+        const int limit = a.causal ? min(i + w.kv_len - w.q_len, w.kv_len - 1) : w.kv_len - 1;
+        const float sink = a.sinks[h] * kLog2e;
+        float m = sink;                                 // running max (log2 units)
+        float d = (sink == kNegInf) ? 0.0f : 1.0f;      // running denominator
+        for (int j = 0; j < w.n_kv; ++j) {
+          const int gg = g + j;
+          if (!wait_bar(smem_u32(&sm.s_full[t]), gg & 1, a.timeout_ns, abort_flag)) return ok = false;
+          tc_fence_after();
+          uint32_t sr[128];
+          tmem_ld32_at<0>(s_col + 0, sr);
+          tmem_ld32_at<32>(s_col + 32, sr);
+          tmem_ld32_at<64>(s_col + 64, sr);
+          tmem_ld32_at<96>(s_col + 96, sr);
+          tc_wait_ld();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.s_free[t]));  // the MMA may now overwrite S_t
+          float s[128];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        const int key0 = j * kBlockK;
-        if (key0 + kBlockK - 1 > limit) {  // diagonal / tail tile: mask
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+          const int key0 = j * kBlockK;
+          if (key0 + kBlockK - 1 > limit) {  // diagonal / tail tile: mask
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (key0 + c > limit) s[c] = kNegInf;
-        }
-        // row max: four independent 3-input max chains
-        float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
-#pragma unroll
-        for (int c = 4; c < 124; c += 8) {
-          m0 = fmax3(m0, s[c], s[c + 1]);
-          m1 = fmax3(m1, s[c + 2], s[c + 3]);
-          m2 = fmax3(m2, s[c + 4], s[c + 5]);
-          m3 = fmax3(m3, s[c + 6], s[c + 7]);
-        }
-        m0 = fmax3(m0, s[124], s[125]);
-        m1 = fmax3(m1, s[126], s[127]);
-        const float mx = fmax3(m0, m1, fmaxf(m2, m3)) * a.scale_log2;
-        const bool grow = mx > m + kRescaleThreshold;
-        float factor = 1.0f;
-        if (grow) {
-          factor = (m == kNegInf) ? 0.0f : ex2(m - mx);
-          m = mx;
-          d *= factor;
-        }
-        const float mu = (m == kNegInf) ? 0.0f : m;
-        const uint64_t negm2 = f2(-mu, -mu);
-        // p = 2^(s * scale - m), packed two per instruction; four partial row sums
-        uint32_t pk[64];
-        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float x0, x1;
-          f2_split(f2_fma(f2(s[2 * c], s[2 * c + 1]), scale2, negm2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          const uint64_t pp = f2(p0, p1);
-          if ((c & 3) == 0) acc0 = f2_add(acc0, pp);
-          if ((c & 3) == 1) acc1 = f2_add(acc1, pp);
-          if ((c & 3) == 2) acc2 = f2_add(acc2, pp);
-          if ((c & 3) == 3) acc3 = f2_add(acc3, pp);
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        float r0, r1, r2, r3;
-        f2_split(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), r0, r1);
-        (void)r2;
-        (void)r3;
-        d += r0 + r1;
-        // P_t and O_t are still in use by the previous PV until it completes
-        if (j > 0 && !wait_bar(smem_u32(&sm.pv_done[t]), (j - 1) & 1, a.timeout_ns, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {  // O holds earlier tiles: rescale it
-          const uint64_t f22 = f2(factor, factor);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t u[32];
-            tmem_ld32(o_col + c * 32, u);
-            tc_wait_ld();
-            uint32_t lo[16], hi[16];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              float a0, a1;
-              f2_split(f2_mul(f2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), f22), a0, a1);
-              lo[e] = __float_as_uint(a0);
-              lo[e + 1] = __float_as_uint(a1);
-              f2_split(f2_mul(f2(__uint_as_float(u[16 + e]), __uint_as_float(u[17 + e])), f22), a0, a1);
-              hi[e] = __float_as_uint(a0);
-              hi[e + 1] = __float_as_uint(a1);
-            }
-            tmem_st16(o_col + c * 32, lo);
-            tmem_st16(o_col + c * 32 + 16, hi);
+            for (int c = 0; c < 128; ++c)
+              if (key0 + c > limit) s[c] = kNegInf;
           }
+          // row max: four independent 3-input max chains
+          float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+#pragma unroll
+          for (int c = 4; c < 124; c += 8) {
+            m0 = fmax3(m0, s[c], s[c + 1]);
+            m1 = fmax3(m1, s[c + 2], s[c + 3]);
+            m2 = fmax3(m2, s[c + 4], s[c + 5]);
+            m3 = fmax3(m3, s[c + 6], s[c + 7]);
+          }
+          m0 = fmax3(m0, s[124], s[125]);
+          m1 = fmax3(m1, s[126], s[127]);
+          const float mx = fmax3(m0, m1, fmaxf(m2, m3)) * a.scale_log2;
+          const bool grow = mx > m + kRescaleThreshold;
+          float factor = 1.0f;
+          if (grow) {
+            factor = (m == kNegInf) ? 0.0f : ex2(m - mx);
+            m = mx;
+            d *= factor;
+          }
+          const float mu = (m == kNegInf) ? 0.0f : m;
+          const uint64_t negm2 = f2(-mu, -mu);
+          // p = 2^(s * scale - m), packed two per instruction; four partial row sums
+          uint32_t pk[64];
+          uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            float x0, x1;
+            f2_split(f2_fma(f2(s[2 * c], s[2 * c + 1]), scale2, negm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            const uint64_t pp = f2(p0, p1);
+            if ((c & 3) == 0) acc0 = f2_add(acc0, pp);
+            if ((c & 3) == 1) acc1 = f2_add(acc1, pp);
+            if ((c & 3) == 2) acc2 = f2_add(acc2, pp);
+            if ((c & 3) == 3) acc3 = f2_add(acc3, pp);
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          float r0, r1;
+          f2_split(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), r0, r1);
+          d += r0 + r1;
+          // P_t and O_t are still in use by the previous PV until it completes
+          if (j > 0 && !wait_bar(smem_u32(&sm.pv_done[t]), (gg - 1) & 1, a.timeout_ns, abort_flag))
+            return ok = false;
+          tc_fence_after();
+          if (j > 0 && __any_sync(0xffffffffu, grow)) {  // O holds earlier tiles: rescale it
+            const uint64_t f22 = f2(factor, factor);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t u[32];
+              tmem_ld32(o_col + c * 32, u);
+              tc_wait_ld();
+              uint32_t lo[16], hi[16];
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                float a0, a1;
+                f2_split(f2_mul(f2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), f22), a0, a1);
+                lo[e] = __float_as_uint(a0);
+                lo[e + 1] = __float_as_uint(a1);
+                f2_split(f2_mul(f2(__uint_as_float(u[16 + e]), __uint_as_float(u[17 + e])), f22), a0, a1);
+                hi[e] = __float_as_uint(a0);
+                hi[e + 1] = __float_as_uint(a1);
+              }
+              tmem_st16(o_col + c * 32, lo);
+              tmem_st16(o_col + c * 32 + 16, hi);
+            }
+          }
+          tmem_st16_at<0>(p_col + 0, pk);
+          tmem_st16_at<16>(p_col + 16, pk);
+          tmem_st16_at<32>(p_col + 32, pk);
+          tmem_st16_at<48>(p_col + 48, pk);
+          tc_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.p_full[t]));
         }
-        tmem_st16_at<0>(p_col + 0, pk);
-        tmem_st16_at<16>(p_col + 16, pk);
-        tmem_st16_at<32>(p_col + 32, pk);
-        tmem_st16_at<48>(p_col + 48, pk);
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm.p_full[t]));
-      }
-      if (ok && w.n_kv > 0)
-        ok = wait_bar(smem_u32(&sm.pv_done[t]), (w.n_kv - 1) & 1, a.timeout_ns, abort_flag);
-      if (ok) {
+        if (!wait_bar(smem_u32(&sm.pv_done[t]), (g + w.n_kv - 1) & 1, a.timeout_ns, abort_flag))
+          return ok = false;
+        // ---- epilogue: out = O / d (bf16), lse = m + ln d; then O_t is free again
         tc_fence_after();
         const bool row_ok = i < w.q_len;
         const float inv = d > 0.0f ? 1.0f / d : 0.0f;
@@ -410,31 +582,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t u[32];
-          if (w.n_kv > 0) {
-            tmem_ld32(o_col + c * 32, u);
-            tc_wait_ld();
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = 0u;
+          tmem_ld32(o_col + c * 32, u);
+          tc_wait_ld();
+          if (kPersistent && c == 1) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm.o_free[t]));  // the next item's first PV may overwrite O_t
           }
           if (row_ok) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              uint4 pk;
-              pk.x = pack_bf16x2(__uint_as_float(u[8 * e + 0]) * inv, __uint_as_float(u[8 * e + 1]) * inv);
-              pk.y = pack_bf16x2(__uint_as_float(u[8 * e + 2]) * inv, __uint_as_float(u[8 * e + 3]) * inv);
-              pk.z = pack_bf16x2(__uint_as_float(u[8 * e + 4]) * inv, __uint_as_float(u[8 * e + 5]) * inv);
-              pk.w = pack_bf16x2(__uint_as_float(u[8 * e + 6]) * inv, __uint_as_float(u[8 * e + 7]) * inv);
-              reinterpret_cast<uint4*>(out + c * 32)[e] = pk;
+              uint4 pk4;
+              pk4.x = pack_bf16x2(__uint_as_float(u[8 * e + 0]) * inv, __uint_as_float(u[8 * e + 1]) * inv);
+              pk4.y = pack_bf16x2(__uint_as_float(u[8 * e + 2]) * inv, __uint_as_float(u[8 * e + 3]) * inv);
+              pk4.z = pack_bf16x2(__uint_as_float(u[8 * e + 4]) * inv, __uint_as_float(u[8 * e + 5]) * inv);
+              pk4.w = pack_bf16x2(__uint_as_float(u[8 * e + 6]) * inv, __uint_as_float(u[8 * e + 7]) * inv);
+              reinterpret_cast<uint4*>(out + c * 32)[e] = pk4;
             }
           }
         }
         if (row_ok && a.lse)
-          a.lse[static_cast<size_t>(w.q_start + i) * a.hq + h] =
-              d > 0.0f ? (m + lg2(d)) * kLn2 : kNegInf;
-      } else {
-        raise_status(a.status, kStatusTimeout);
-      }
+          a.lse[static_cast<size_t>(w.q_start + i) * a.hq + h] = d > 0.0f ? (m + lg2(d)) * kLn2 : kNegInf;
+        return true;
+      });
+      if (!ok) raise_status(a.status, kStatusTimeout);
     }
   }
 
@@ -443,14 +613,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (*abort_flag && warp == 0 && lane == 0) {
     // some role gave up: copies it never consumed may still be in flight; let
-    // the last tile of every stage (and Q) land before shared memory is released
-    const int issued = sm.issued_tiles;
-    for (int j = max(0, issued - kStages); j < issued; ++j)
-      mbar_wait(smem_u32(&sm.kv_full[j % kStages]), (j / kStages) & 1, 2000000000ull);
-    mbar_wait(smem_u32(&sm.q_full), 0, 2000000000ull);
+    // the last tile of every stage and the last Q loads land before shared
+    // memory is released
+    const int issued = sm.issued_kv, issued_q = sm.issued_q;
+    for (int gg = max(0, issued - kStages); gg < issued; ++gg)
+      mbar_wait(smem_u32(&sm.kv_full[gg % kStages]), (gg / kStages) & 1, 2000000000ull);
+    for (int it = max(0, issued_q - 2); it < issued_q; ++it)
+      mbar_wait(smem_u32(&sm.q_full[it & 1]), (it >> 1) & 1, 2000000000ull);
   }
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
+
+int g_prefill_sms[64] = {};
 
 }  // namespace
 
@@ -458,14 +632,30 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t stream) {
   const int tiles = (a.group % 2 == 0) ? 2 : 1;
   const int n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
-  const long long blocks = static_cast<long long>(n_qb) * (a.hq / tiles) * a.batch;
-  if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const size_t smem = sizeof(PrefillSmem) + 1024;
-  auto kern = a.paged ? sink_prefill_kernel<true> : sink_prefill_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const long long items = static_cast<long long>(n_qb) * (a.hq / tiles) * a.batch;
+  if (items <= 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(qmap, kmap, vmap, a);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_prefill_sms[dev]) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_prefill_sms[dev] = n > 0 ? n : 1;
+  }
+  // Contiguous KV with every sequence at max_q tokens (their sum is then
+  // batch * max_q): items are uniform per query block, so one CTA per item in
+  // heaviest-first order.  Otherwise a persistent grid with the sorted schedule.
+  const bool uniform = !a.paged && static_cast<long long>(a.total_q) == static_cast<long long>(a.batch) * a.max_q;
+  const bool persistent = !uniform || items > 0x7fffffffLL;
+  const int blocks = static_cast<int>(persistent ? (items < g_prefill_sms[dev] ? items : g_prefill_sms[dev]) : items);
+  const size_t smem = (persistent ? sizeof(PrefillSmem) : kSmemOnePerCta) + 1024;
+  auto kern = a.paged ? (persistent ? sink_prefill_kernel<true, true> : sink_prefill_kernel<true, false>)
+                      : (persistent ? sink_prefill_kernel<false, true> : sink_prefill_kernel<false, false>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<blocks, kThreads, smem, stream>>>(qmap, kmap, vmap, a);
   return cudaGetLastError();
 }
 
