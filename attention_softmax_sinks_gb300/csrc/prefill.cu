@@ -363,18 +363,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           sm.issued_q = it + 1;
           const int32_t* ptab = kPaged ? a.page_table + static_cast<size_t>(w.b) * a.max_pages : nullptr;
           const int seq_pages = (w.kv_len + kPageSize - 1) / kPageSize;
+          constexpr int kPagesPerTile = kBlockK / kPageSize;
+          // page ids of tile j are loaded while tile j-1's boxes are issued
+          int ids[kPagesPerTile];
+          auto load_ids = [&](int j, int (&dst)[kPagesPerTile]) {
+#pragma unroll
+            for (int i = 0; i < kPagesPerTile; ++i) {
+              const int lp = min(j * kPagesPerTile + i, seq_pages - 1);  // ragged tail: any valid page
+              dst[i] = ptab[lp];
+            }
+          };
+          if constexpr (kPaged) load_ids(0, ids);
           for (int j = 0; j < w.n_kv; ++j) {
             const int gg = g + j, st = gg % kStages;
+            int next[kPagesPerTile];
+            if constexpr (kPaged) {
+              if (j + 1 < w.n_kv) load_ids(j + 1, next);
+            }
             if (gg >= kStages &&
                 !wait_bar(smem_u32(&sm.kv_empty[st]), ((gg / kStages) - 1) & 1, a.timeout_ns, abort_flag))
               return ok = false;
             const uint32_t bar = smem_u32(&sm.kv_full[st]);
             mbar_arrive_expect_tx(bar, 2 * kTileBytes);
             if constexpr (kPaged) {
-              for (int i = 0; i < kBlockK / kPageSize; ++i) {
-                int lp = j * (kBlockK / kPageSize) + i;
-                if (lp >= seq_pages) lp = seq_pages - 1;  // ragged tail: any valid page, masked later
-                int phys = ptab[lp];
+#pragma unroll
+              for (int i = 0; i < kPagesPerTile; ++i) {
+                int phys = ids[i];
                 if (phys < 0 || phys >= a.num_pages) {
                   raise_status(a.status, kStatusBadPage);
                   phys = 0;
@@ -383,6 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem_u32(sm.k[st]) + i * kPageSize * 128, &kmap, 0, row, bar, keep);
                 tma_load_2d(smem_u32(sm.v[st]) + i * kPageSize * 128, &vmap, 0, row, bar, keep);
               }
+              if (j + 1 < w.n_kv)
+#pragma unroll
+                for (int i = 0; i < kPagesPerTile; ++i) ids[i] = next[i];
             } else {
               tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
               tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
