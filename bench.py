@@ -270,10 +270,11 @@ def run_ours(args, rank, world, device):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
     # ---- causal prefill measured on its own (tensor-core bound kernel)
-    prefill = mixed = None
+    prefill = mixed = graph = None
     if not args.no_prefill:
         prefill = bench_prefill(args, sa, torch, device, pk)
         mixed = bench_mixed(args, sa, torch, device, pk)
+        graph = bench_graph_decode(args, sa, torch, device, pk)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -311,6 +312,8 @@ def run_ours(args, rank, world, device):
         line["prefill"] = prefill
     if mixed is not None:
         line["mixed"] = mixed
+    if graph is not None:
+        line["small_batch_decode"] = graph
     return line
 
 
@@ -361,6 +364,74 @@ def bench_mixed(args, sa, torch, device, pk):
                          "tensor_frac": round(t_tc / (ms * 1e-3), 4), "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
                          "note": "frac = max(FLOPs / peak bf16, bytes / peak HBM) / time"},
             "gpu_launches": len(times)}
+
+
+def bench_graph_decode(args, sa, torch, device, pk):
+    """Small-batch decode, where launch overhead shows: one sequence of 4096 cached tokens per
+    step (64/8 heads, page 16), decode + merge with the library's split count.  32 steps cycle
+    over 32 different sequences of one permuted page pool (256 MiB of KV, larger than L2), run
+    eagerly and as one captured CUDA graph of the same 32 steps."""
+    cfg = DECODE
+    nseq, kvl = 32, cfg["kv_len"]
+    host = workloads.make_decode(cfg["seed"] + 7, [kvl] * nseq, cfg["hq"], cfg["hkv"], cfg["d"],
+                                 cfg["page_size"], cfg["sink_std"])
+    dv = {n: to_dev(host[n], torch, device)
+          for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
+    hq, d = cfg["hq"], cfg["d"]
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    splits = sa.sink_attn_decode_splits(1, cfg["hkv"], kvl, cfg["page_size"], sms)
+    part_o = torch.empty((nseq, splits, hq, d), dtype=torch.float32, device=device)
+    part_l = torch.empty((nseq, splits, hq), dtype=torch.float32, device=device)
+    out = torch.empty((nseq, hq, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((nseq, hq), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def steps():
+        for i in range(nseq):
+            sl = slice(i, i + 1)
+            if splits > 1:
+                sa.sink_attn_decode(dv["q"][sl], dv["k_pages"], dv["v_pages"], dv["page_table"][sl],
+                                    dv["kv_lens"][sl], dv["sinks"], cfg["sm_scale"], num_splits=splits,
+                                    out=part_o[sl], lse=part_l[sl], stream=stream)
+                sa.sink_attn_merge(part_o[sl], part_l[sl], out=out[sl], lse=lse[sl], stream=stream)
+            else:
+                sa.sink_attn_decode(dv["q"][sl], dv["k_pages"], dv["v_pages"], dv["page_table"][sl],
+                                    dv["kv_lens"][sl], dv["sinks"], cfg["sm_scale"], num_splits=1,
+                                    out=out[sl], lse=lse[sl], stream=stream)
+
+    stream.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            steps()
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        steps()
+    torch.cuda.synchronize(device)
+    reps = max(3, min(30, args.steps // 10))
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3 / (reps * nseq)
+
+    eager_us = timed(steps)
+    graph_us = timed(graph.replay)
+    step_bytes = decode_bytes(1, kvl, hq, cfg["hkv"], d, host["page_table"].shape[1])
+    per_step = 2 if splits > 1 else 1
+    return {"workload": "small-batch decode: 1 seq x 4096 cached tokens per step, 64/8 heads, page 16; "
+                        "32 steps over 32 sequences of a 256 MiB page pool (larger than L2)",
+            "num_splits": splits, "launches_per_step": per_step,
+            "eager_us_per_step": round(eager_us, 2), "graph_us_per_step": round(graph_us, 2),
+            "graph_gbs": round(step_bytes / (graph_us * 1e-6) / 1e9, 1),
+            "eager_gbs": round(step_bytes / (eager_us * 1e-6) / 1e9, 1),
+            "gpu_launches": per_step * nseq * (2 * reps + 2)}
 
 
 def bench_prefill(args, sa, torch, device, pk):
