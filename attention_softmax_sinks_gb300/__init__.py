@@ -21,7 +21,8 @@ __all__ = [
     "SinkAttnError", "library_path", "load_library", "sink_attn_prefill", "sink_attn_prefill_paged",
     "sink_attn_decode", "sink_attn_merge", "sink_attn_decode_splits", "sink_attn_device_status",
     "sink_attn_set_wait_timeout_ns", "sink_attn_status_string", "sink_attn_abi_version",
-    "sink_attn_selftest_wait_timeout", "sink_attn_decode_noalloc", "EXPORTED_SYMBOLS",
+    "sink_attn_selftest_wait_timeout", "sink_attn_decode_noalloc", "moe_router_topk_softmax",
+    "qkv_bias_rope", "qkv_bias_rope_append_paged", "GPT_OSS_YARN", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,10 +33,11 @@ EXPORTED_SYMBOLS = (
     "sink_attn_prefill", "sink_attn_prefill_paged", "sink_attn_decode", "sink_attn_merge",
     "sink_attn_decode_splits", "sink_attn_device_status", "sink_attn_set_wait_timeout_ns",
     "sink_attn_status_string", "sink_attn_abi_version", "sink_attn_selftest_wait_timeout",
-    "sink_attn_decode_noalloc",
+    "sink_attn_decode_noalloc", "moe_router_topk_softmax", "qkv_bias_rope",
+    "qkv_bias_rope_append_paged",
 )
 
-_p, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_p, _i, _f, _d, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_longlong
 _SIGNATURES = {
     "sink_attn_prefill": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p, _p]),
     "sink_attn_prefill_paged": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -50,7 +52,16 @@ _SIGNATURES = {
     "sink_attn_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _p]),
     "sink_attn_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p,
                                       _p]),
+    "moe_router_topk_softmax": (_i, [_p, _ll, _i, _i, _p, _p, _p, _p]),
+    "qkv_bias_rope": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p, _p, _p]),
+    "qkv_bias_rope_append_paged": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p,
+                                        _p, _p, _i, _i, _i, _p]),
 }
+
+# YaRN constants of the public GPT-OSS model configuration (the pages name YaRN
+# but give no constants): rotary base, scale factor, original context length,
+# beta_fast, beta_slow.
+GPT_OSS_YARN = dict(rope_base=150000.0, factor=32.0, orig_len=4096, beta_fast=32.0, beta_slow=1.0)
 
 
 class SinkAttnError(RuntimeError):
@@ -264,3 +275,82 @@ def sink_attn_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) ->
     """Launch the bounded-wait diagnostic (records SA_ERR_TIMEOUT in the status word)."""
     _check(load_library().sink_attn_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
            "sink_attn_selftest_wait_timeout")
+
+
+# ----------------------------------------------------------------------------- around attention
+def moe_router_topk_softmax(logits, top_k: int, topk_idx=None, topk_weight=None,
+                            expert_counts=None, return_counts: bool = False, stream=None):
+    """Top-K-then-softmax router over bf16 logits [T, E] (page "GPT-OSS on day 0",
+    section "Kernels for GPT-OSS / MoE").  Returns (idx int32 [T, k], weight bf16
+    [T, k]) and, with return_counts or a given expert_counts, the int32 [E] counts."""
+    _dev(logits, "logits", torch.bfloat16)
+    t, e = logits.shape
+    k = int(top_k)
+    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=logits.device) if topk_idx is None
+                else _dev(topk_idx, "topk_idx", torch.int32))
+    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=logits.device) if topk_weight is None
+                   else _dev(topk_weight, "topk_weight", torch.bfloat16))
+    if expert_counts is None and return_counts:
+        expert_counts = torch.empty((e,), dtype=torch.int32, device=logits.device)
+    elif expert_counts is not None:
+        _dev(expert_counts, "expert_counts", torch.int32)
+    st = load_library().moe_router_topk_softmax(_ptr(logits), t, e, k, _ptr(topk_idx), _ptr(topk_weight),
+                                                _ptr(expert_counts), _stream(stream))
+    _check(st, "moe_router_topk_softmax")
+    if expert_counts is not None:
+        return topk_idx, topk_weight, expert_counts
+    return topk_idx, topk_weight
+
+
+def _rope_params(rope):
+    r = dict(GPT_OSS_YARN if rope is None else rope)
+    return (float(r["rope_base"]), float(r["factor"]), int(r["orig_len"]), float(r["beta_fast"]),
+            float(r["beta_slow"]))
+
+
+def qkv_bias_rope(qkv, bias, cu_seqlens_q, num_qo_heads: int, num_kv_heads: int, kv_lens=None,
+                  rope=None, q_out=None, k_out=None, v_out=None, stream=None):
+    """QKV bias + YaRN rotation of q and k.  qkv bf16 [T, (Hq + 2 Hkv) * 64] -> (q [T, Hq, 64],
+    k [T, Hkv, 64], v [T, Hkv, 64]) bf16.  rope: dict like GPT_OSS_YARN (default)."""
+    _dev(qkv, "qkv", torch.bfloat16)
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    if bias is not None:
+        _dev(bias, "bias", torch.bfloat16)
+    if kv_lens is not None:
+        _dev(kv_lens, "kv_lens", torch.int32)
+    t = qkv.shape[0]
+    hq, hkv, d = int(num_qo_heads), int(num_kv_heads), 64
+    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=qkv.device) if q_out is None else q_out
+    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=qkv.device) if k_out is None else k_out
+    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=qkv.device) if v_out is None else v_out
+    for name, x in (("q_out", q_out), ("k_out", k_out), ("v_out", v_out)):
+        _dev(x, name, torch.bfloat16)
+    st = load_library().qkv_bias_rope(_ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens),
+                                      cu_seqlens_q.numel() - 1, t, hq, hkv, qkv.shape[1] // (hq + 2 * hkv),
+                                      *_rope_params(rope), _ptr(q_out), _ptr(k_out), _ptr(v_out),
+                                      _stream(stream))
+    _check(st, "qkv_bias_rope")
+    return q_out, k_out, v_out
+
+
+def qkv_bias_rope_append_paged(qkv, bias, cu_seqlens_q, kv_lens, paged_k, paged_v, page_table,
+                               num_qo_heads: int, rope=None, q_out=None, stream=None):
+    """QKV bias + YaRN rotation; q returned [T, Hq, 64], k and v written in place into the
+    paged cache [num_pages, Hkv, 16, 64] at each new token's position."""
+    for name, x, dt in (("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("kv_lens", kv_lens, torch.int32), ("paged_k", paged_k, torch.bfloat16),
+                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32)):
+        _dev(x, name, dt)
+    if bias is not None:
+        _dev(bias, "bias", torch.bfloat16)
+    t = qkv.shape[0]
+    num_pages, hkv, page_size, d = paged_k.shape
+    hq = int(num_qo_heads)
+    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=qkv.device) if q_out is None else q_out
+    _dev(q_out, "q_out", torch.bfloat16)
+    st = load_library().qkv_bias_rope_append_paged(
+        _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
+        qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(q_out), _ptr(paged_k), _ptr(paged_v),
+        _ptr(page_table), page_size, page_table.shape[1], num_pages, _stream(stream))
+    _check(st, "qkv_bias_rope_append_paged")
+    return q_out

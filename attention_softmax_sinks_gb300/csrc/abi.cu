@@ -11,8 +11,11 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include "../../include/moe_router.h"
+#include "../../include/qkv_rope.h"
 #include "../../include/sink_attn.h"
 #include "internal.h"
+#include "ops_internal.h"
 #include "ptx.cuh"
 
 namespace {
@@ -137,6 +140,78 @@ __global__ void selftest_wait_kernel(unsigned* status, unsigned long long timeou
   __syncwarp();
   if (threadIdx.x == 0 && !sa::mbar_wait(sa::smem_u32(&bar), 0, timeout_ns))
     sa::raise_status(status, sa::kStatusTimeout);
+}
+
+// YaRN frequencies and temperature (YaRN paper, section 3, "NTK-by-parts"):
+// pairs whose frequency turns at least beta_fast times over the original
+// context keep theta_i, pairs that turn at most beta_slow times use
+// theta_i / factor, with a ramp linear in the pair index between the two
+// (fractional) indices where the number of turns equals beta_fast and beta_slow.
+sa_status yarn_tables(double base, double factor, int orig_len, double beta_fast,
+                      double beta_slow, double* inv_freq, float* mscale) {
+  if (!(base > 1.0) || !std::isfinite(base) || !(factor >= 1.0) || !std::isfinite(factor))
+    return SA_ERR_SHAPE;
+  const int pairs = sa::kMaxRopePairs;
+  for (int i = 0; i < pairs; ++i) inv_freq[i] = std::pow(base, -2.0 * i / sa::kHeadDim);
+  *mscale = 1.0f;
+  if (factor == 1.0) return SA_OK;
+  if (orig_len < 1 || !(beta_slow > 0.0) || !(beta_fast > beta_slow) || !std::isfinite(beta_fast))
+    return SA_ERR_SHAPE;
+  const double kPi = 3.14159265358979323846;
+  auto index_of_turns = [&](double turns) {
+    return (sa::kHeadDim / 2.0) * std::log(orig_len / (2.0 * kPi * turns)) / std::log(base);
+  };
+  const double lo = index_of_turns(beta_fast);
+  const double hi = index_of_turns(beta_slow);
+  for (int i = 0; i < pairs; ++i) {
+    double rho = (i - lo) / (hi - lo);
+    rho = rho < 0.0 ? 0.0 : (rho > 1.0 ? 1.0 : rho);
+    inv_freq[i] = inv_freq[i] * (1.0 - rho) + inv_freq[i] / factor * rho;
+  }
+  *mscale = static_cast<float>(0.1 * std::log(factor) + 1.0);
+  return SA_OK;
+}
+
+sa_status rope_common(const void* qkv, const void* bias, const int32_t* cu_q, const int32_t* kv_lens,
+                      int batch, int total_tokens, int hq, int hkv, int head_dim, double base,
+                      double factor, int orig_len, double beta_fast, double beta_slow, void* q_out,
+                      void* k_out, void* v_out, const int32_t* page_table, int max_pages,
+                      int num_pages, bool paged, cudaStream_t stream) {
+  if (batch < 0 || total_tokens < 0) return SA_ERR_SHAPE;
+  const bool work = batch > 0 && total_tokens > 0;  // empty tensors may carry NULL pointers
+  if (work && (!qkv || !cu_q || !q_out)) return SA_ERR_NULL;
+  if (work && paged && (!kv_lens || !page_table || !k_out || !v_out)) return SA_ERR_NULL;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SA_ERR_SHAPE;
+  if (head_dim != sa::kHeadDim) return SA_ERR_UNSUPPORTED;
+  if (paged && (max_pages <= 0 || num_pages <= 0)) return SA_ERR_SHAPE;
+  if (static_cast<long long>(total_tokens) * (hq + 2 * hkv) * sa::kHeadDim >= (1LL << 40))
+    return SA_ERR_SHAPE;
+  const void* ptrs[] = {qkv, bias, q_out, k_out, v_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return SA_ERR_ALIGNMENT;
+  sa::RopeArgs a{};
+  if (sa_status s = yarn_tables(base, factor, orig_len, beta_fast, beta_slow, a.inv_freq, &a.mscale))
+    return s;
+  if (batch == 0 || total_tokens == 0) return SA_OK;
+  unsigned* status = nullptr;
+  if (sa_status s = status_ptr(&status)) return s;
+  a.qkv = static_cast<const uint16_t*>(qkv);
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.cu_q = cu_q;
+  a.kv_lens = kv_lens;
+  a.q_out = static_cast<uint16_t*>(q_out);
+  a.k_out = static_cast<uint16_t*>(k_out);
+  a.v_out = static_cast<uint16_t*>(v_out);
+  a.page_table = page_table;
+  a.paged = paged ? 1 : 0;
+  a.batch = batch;
+  a.total_tokens = total_tokens;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.status = status;
+  return sa::launch_rope(a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -325,6 +400,48 @@ sa_status sink_attn_prefill_paged(const void* q, const void* paged_k, const void
   return prefill_common(q, paged_k, paged_v, page_table, cu_seqlens_q, kv_lens, sinks, batch,
                         total_q_tokens, max_q_len, num_qo_heads, num_kv_heads, head_dim,
                         max_pages, num_pages, sm_scale, causal, out, lse, stream, true);
+}
+
+sa_status moe_router_topk_softmax(const void* logits, long long num_tokens, int num_experts,
+                                  int top_k, int32_t* topk_idx, void* topk_weight,
+                                  int32_t* expert_counts, cudaStream_t stream) {
+  if (num_tokens < 0 || num_experts < 1 || num_experts > 256) return SA_ERR_SHAPE;
+  if (top_k < 1 || top_k > 8 || top_k > num_experts) return SA_ERR_SHAPE;
+  if (num_tokens > (1LL << 40) / num_experts) return SA_ERR_SHAPE;
+  if (num_tokens > 0 && (!logits || !topk_idx || !topk_weight)) return SA_ERR_NULL;
+  if (expert_counts &&
+      cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * num_experts, stream) != cudaSuccess)
+    return SA_ERR_CUDA;
+  if (num_tokens == 0) return SA_OK;
+  sa::RouterArgs a{static_cast<const uint16_t*>(logits), topk_idx,
+                   static_cast<uint16_t*>(topk_weight), expert_counts, num_tokens, num_experts,
+                   top_k};
+  return sa::launch_router(a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
+sa_status qkv_bias_rope(const void* qkv, const void* bias, const int32_t* cu_seqlens_q,
+                        const int32_t* kv_lens, int batch, int total_tokens, int num_qo_heads,
+                        int num_kv_heads, int head_dim, double rope_base, double factor,
+                        int orig_len, double beta_fast, double beta_slow, void* q_out,
+                        void* k_out, void* v_out, cudaStream_t stream) {
+  return rope_common(qkv, bias, cu_seqlens_q, kv_lens, batch, total_tokens, num_qo_heads,
+                     num_kv_heads, head_dim, rope_base, factor, orig_len, beta_fast, beta_slow,
+                     q_out, k_out, v_out, nullptr, 0, 0, false, stream);
+}
+
+sa_status qkv_bias_rope_append_paged(const void* qkv, const void* bias,
+                                     const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                     int batch, int total_tokens, int num_qo_heads,
+                                     int num_kv_heads, int head_dim, double rope_base,
+                                     double factor, int orig_len, double beta_fast,
+                                     double beta_slow, void* q_out, void* paged_k, void* paged_v,
+                                     const int32_t* page_table, int page_size, int max_pages,
+                                     int num_pages, cudaStream_t stream) {
+  if (page_size != sa::kPageSize && page_size > 0) return SA_ERR_UNSUPPORTED;
+  if (page_size <= 0) return SA_ERR_SHAPE;
+  return rope_common(qkv, bias, cu_seqlens_q, kv_lens, batch, total_tokens, num_qo_heads,
+                     num_kv_heads, head_dim, rope_base, factor, orig_len, beta_fast, beta_slow,
+                     q_out, paged_k, paged_v, page_table, max_pages, num_pages, true, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,42 @@
+// Internal interface of the kernels around attention (router, QKV bias +
+// rotary + K/V write) between abi.cu and their translation units.  Arguments
+// arrive here already validated.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace sa {
+
+struct RouterArgs {
+  const uint16_t* logits;  // bf16 [T, E]
+  int32_t* topk_idx;       // [T, k]
+  uint16_t* topk_w;        // bf16 [T, k]
+  int32_t* counts;         // [E] (already zeroed) or nullptr
+  long long num_tokens;
+  int num_experts, top_k;
+};
+
+constexpr int kMaxRopePairs = kHeadDim / 2;
+
+struct RopeArgs {
+  const uint16_t* qkv;         // bf16 [T, (Hq + 2 Hkv) * 64]
+  const uint16_t* bias;        // bf16 [(Hq + 2 Hkv) * 64] or nullptr
+  const int32_t* cu_q;         // [B + 1]
+  const int32_t* kv_lens;      // [B] or nullptr (kv_len == q_len)
+  uint16_t* q_out;             // bf16 [T, Hq, 64]
+  uint16_t* k_out;             // contiguous: bf16 [T, Hkv, 64]; paged: [num_pages, Hkv, 16, 64]
+  uint16_t* v_out;
+  const int32_t* page_table;   // paged only: [B, max_pages]
+  int paged;
+  int batch, total_tokens, hq, hkv, max_pages, num_pages;
+  float mscale;
+  double inv_freq[kMaxRopePairs];
+  unsigned* status;
+};
+
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream);
+cudaError_t launch_rope(const RopeArgs& a, cudaStream_t stream);
+
+}  // namespace sa

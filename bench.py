@@ -270,11 +270,12 @@ def run_ours(args, rank, world, device):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
     # ---- causal prefill measured on its own (tensor-core bound kernel)
-    prefill = mixed = graph = None
+    prefill = mixed = graph = around = None
     if not args.no_prefill:
         prefill = bench_prefill(args, sa, torch, device, pk)
         mixed = bench_mixed(args, sa, torch, device, pk)
         graph = bench_graph_decode(args, sa, torch, device, pk)
+        around = bench_around_attention(args, sa, torch, device, pk)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -314,6 +315,8 @@ def run_ours(args, rank, world, device):
         line["mixed"] = mixed
     if graph is not None:
         line["small_batch_decode"] = graph
+    if around is not None:
+        line["around_attention"] = around
     return line
 
 
@@ -432,6 +435,61 @@ def bench_graph_decode(args, sa, torch, device, pk):
             "graph_gbs": round(step_bytes / (graph_us * 1e-6) / 1e9, 1),
             "eager_gbs": round(step_bytes / (eager_us * 1e-6) / 1e9, 1),
             "gpu_launches": per_step * nseq * (2 * reps + 2)}
+
+
+def _timed_flushed(torch, device, stream, fn, reps):
+    """Mean CUDA-event time (ms) of fn over reps launches, L2 flushed before each."""
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    for _ in range(3):
+        fn()
+    evs = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(device)
+    return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+
+def bench_around_attention(args, sa, torch, device, pk):
+    """The two HBM-bound steps next to attention, on the causal-prefill batch
+    (4 x 8192 = 32768 tokens): QKV bias + YaRN rotation (64/8 heads) and the
+    Top-K-then-softmax router (128 experts, top 4)."""
+    stream = torch.cuda.current_stream(device)
+    reps = max(5, min(30, args.steps // 10))
+    t, hq, hkv, e, k = 32768, PREFILL["hq"], PREFILL["hkv"], 128, 4
+    cu = to_dev(workloads.cu_seqlens_from([8192] * 4), torch, device)
+    inp = workloads.make_qkv(41, t, hq, hkv)
+    qkv, bias = to_dev(inp["qkv"], torch, device), to_dev(inp["bias"], torch, device)
+    q = torch.empty((t, hq, 64), dtype=torch.bfloat16, device=device)
+    kk = torch.empty((t, hkv, 64), dtype=torch.bfloat16, device=device)
+    vv = torch.empty_like(kk)
+    rope_ms = _timed_flushed(torch, device, stream, lambda: sa.qkv_bias_rope(
+        qkv, bias, cu, hq, hkv, q_out=q, k_out=kk, v_out=vv, stream=stream), reps)
+    rope_bytes = 2 * t * (hq + 2 * hkv) * 64 * 2 + (hq + 2 * hkv) * 64 * 2 + cu.numel() * 4
+    logits = to_dev(workloads.make_router_logits(42, t, e, std=2.0), torch, device)
+    idx = torch.empty((t, k), dtype=torch.int32, device=device)
+    w = torch.empty((t, k), dtype=torch.bfloat16, device=device)
+    counts = torch.empty((e,), dtype=torch.int32, device=device)
+    router_ms = _timed_flushed(torch, device, stream, lambda: sa.moe_router_topk_softmax(
+        logits, k, topk_idx=idx, topk_weight=w, expert_counts=counts, stream=stream), reps)
+    router_bytes = t * e * 2 + t * k * (4 + 2) + e * 4
+
+    def line(name, kernel, ms, nbytes, note):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"workload": note, "kernel": kernel, "us": round(ms * 1e3, 2), "bytes": nbytes,
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                             "frac": round(gbs / pk["hbm"], 4)}}
+    return {"qkv_bias_rope": line("rope", "qkv_rope_kernel", rope_ms, rope_bytes,
+                                  "32768 tokens, 64/8 heads: bias + YaRN (GPT-OSS constants) on q, k; "
+                                  "q, k, v written contiguous; L2 flushed before each launch"),
+            "moe_router": line("router", "router_topk_kernel", router_ms, router_bytes,
+                               "32768 tokens x 128 bf16 logits, top 4, softmax over the selected, "
+                               "expert counts; L2 flushed before each launch"),
+            "gpu_launches": 2 * (reps + 3)}
 
 
 def bench_prefill(args, sa, torch, device, pk):

@@ -2,6 +2,7 @@
 that include/sink_attn.h declares, and rejects bad arguments with a status
 code before touching the GPU (no compute call is made here)."""
 import ctypes
+import glob
 import os
 import re
 import subprocess
@@ -9,7 +10,7 @@ import subprocess
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "sink_attn.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 SA_OK, SA_ERR_NULL, SA_ERR_SHAPE, SA_ERR_UNSUPPORTED = 0, 1, 2, 3
 SA_ERR_ALIGNMENT = 7
@@ -24,9 +25,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(sink_attn_\w+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:sa_status|int|void|const char\*)\s+(\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_four_calls():
@@ -139,3 +142,56 @@ def test_decode_split_heuristic(lib):
     assert f(8, 8, 131072, 16, 152) >= 16      # long context spreads over the GPU
     assert f(0, 8, 4096, 16, 152) == 1
     assert f(64, 8, 4096, 16, 152) == 4        # 512 (sequence, KV head) units: four waves
+
+
+def test_router_rejects_before_launch(lib):
+    f = lib.moe_router_topk_softmax
+    assert f(None, 10, 32, 4, FAKE, FAKE, None, None) == SA_ERR_NULL
+    assert f(FAKE, 10, 32, 4, None, FAKE, None, None) == SA_ERR_NULL
+    assert f(FAKE, 10, 0, 1, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, 10, 257, 4, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, 10, 32, 0, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, 10, 32, 9, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, 10, 3, 4, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, -1, 32, 4, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, 0, 32, 4, FAKE, FAKE, None, None) == SA_OK
+
+
+GPT_OSS = (150000.0, 32.0, 4096, 32.0, 1.0)
+
+
+def _rope(lib, **kw):
+    a = dict(qkv=FAKE, bias=None, cu=FAKE, kv=None, batch=2, t=10, hq=64, hkv=8, d=64, yarn=GPT_OSS,
+             q=FAKE, k=FAKE, v=FAKE)
+    a.update(kw)
+    return lib.qkv_bias_rope(a["qkv"], a["bias"], a["cu"], a["kv"], a["batch"], a["t"], a["hq"], a["hkv"],
+                             a["d"], *a["yarn"], a["q"], a["k"], a["v"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qkv=None), SA_ERR_NULL), (dict(cu=None), SA_ERR_NULL), (dict(q=None), SA_ERR_NULL),
+    (dict(d=128), SA_ERR_UNSUPPORTED), (dict(hq=6, hkv=4), SA_ERR_SHAPE), (dict(batch=-1), SA_ERR_SHAPE),
+    (dict(yarn=(1.0, 32.0, 4096, 32.0, 1.0)), SA_ERR_SHAPE), (dict(yarn=(1e4, 0.5, 4096, 32.0, 1.0)), SA_ERR_SHAPE),
+    (dict(yarn=(1e4, 32.0, 4096, 1.0, 32.0)), SA_ERR_SHAPE), (dict(yarn=(1e4, 32.0, 0, 32.0, 1.0)), SA_ERR_SHAPE),
+    (dict(yarn=(1e4, 1.0, 0, 0.0, 0.0)), SA_OK),   # factor 1: plain rotary, YaRN constants unused
+    (dict(bias=MISALIGNED), SA_ERR_ALIGNMENT), (dict(k=MISALIGNED), SA_ERR_ALIGNMENT),
+    (dict(batch=0), SA_OK), (dict(t=0), SA_OK),
+])
+def test_rope_rejects_before_launch(lib, kw, status):
+    if status == SA_OK and "yarn" in kw:
+        kw = dict(kw, batch=0)       # valid arguments, no work: nothing is launched
+    assert _rope(lib, **kw) == status
+
+
+def test_rope_paged_rejects(lib):
+    f = lib.qkv_bias_rope_append_paged
+    args = [FAKE, None, FAKE, FAKE, 2, 10, 64, 8, 64, *GPT_OSS, FAKE, FAKE, FAKE, FAKE, 16, 8, 64, None]
+    assert f(*args[:3], None, *args[4:]) == SA_ERR_NULL          # kv_lens required
+    bad = list(args); bad[17] = None                           # page table
+    assert f(*bad) == SA_ERR_NULL
+    bad = list(args); bad[18] = 8                              # page size
+    assert f(*bad) == SA_ERR_UNSUPPORTED
+    bad = list(args); bad[20] = 0                              # num_pages
+    assert f(*bad) == SA_ERR_SHAPE
+    ok = list(args); ok[4] = 0
+    assert f(*ok) == SA_OK

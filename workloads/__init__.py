@@ -33,6 +33,7 @@ CHUNK = 1 << 22
 
 # stream ids: one per tensor role, so tensors never share random numbers
 STREAM_Q, STREAM_K, STREAM_V, STREAM_SINK, STREAM_PERM, STREAM_LENS = 1, 2, 3, 4, 5, 6
+STREAM_LOGITS, STREAM_QKV, STREAM_BIAS, STREAM_X, STREAM_W = 7, 8, 9, 10, 11
 
 
 def _round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -198,3 +199,35 @@ def make_mixed(seed: int, q_lens, kv_lens, hq: int, hkv: int, d: int, page_size:
     kv["cu_seqlens_q"] = cu
     kv["sinks"] = sinks_f32(seed, hq, sink_std, sink_fill)
     return kv
+
+
+# --------------------------------------------------------------------------
+# Inputs of the steps around attention (router, QKV projection output).
+# --------------------------------------------------------------------------
+def make_router_logits(seed: int, num_tokens: int, num_experts: int, std: float = 1.0,
+                       levels: int | None = None) -> np.ndarray:
+    """bf16 router logits [T, E].  With ``levels`` the values are integers drawn
+    uniformly from [-levels, levels] (many exact ties)."""
+    if levels is not None:
+        rng = np.random.default_rng([seed, STREAM_LOGITS])
+        x = rng.integers(-levels, levels + 1, (num_tokens, num_experts)).astype(np.float32)
+        return _round_to_bf16_bits(x.ravel()).reshape(num_tokens, num_experts)
+    return normal_bf16(seed, STREAM_LOGITS, (num_tokens, num_experts), std)
+
+
+def make_qkv(seed: int, num_tokens: int, hq: int, hkv: int, d: int = 64, std: float = 1.0,
+             bias_std: float = 0.5) -> dict:
+    """QKV projection output without bias, bf16 [T, (Hq + 2 Hkv) * d] (q heads, then
+    k heads, then v heads), and its bias, bf16 [(Hq + 2 Hkv) * d]."""
+    width = (hq + 2 * hkv) * d
+    return {"qkv": normal_bf16(seed, STREAM_QKV, (num_tokens, width), std),
+            "bias": normal_bf16(seed, STREAM_BIAS, (width,), bias_std)}
+
+
+def make_linear(seed: int, m: int, n: int, k: int, std: float = 1.0, w_std: float | None = None,
+                bias_std: float = 1.0) -> dict:
+    """x bf16 [M, K], W bf16 [N, K] (one row per output feature), bias bf16 [N]."""
+    w_std = 1.0 / math.sqrt(k) if w_std is None else w_std
+    return {"x": normal_bf16(seed, STREAM_X, (m, k), std),
+            "w": normal_bf16(seed, STREAM_W, (n, k), w_std),
+            "bias": normal_bf16(seed, STREAM_BIAS, (n,), bias_std)}
