@@ -22,7 +22,7 @@ __all__ = [
     "sink_attn_decode", "sink_attn_merge", "sink_attn_decode_splits", "sink_attn_device_status",
     "sink_attn_set_wait_timeout_ns", "sink_attn_status_string", "sink_attn_abi_version",
     "sink_attn_selftest_wait_timeout", "sink_attn_decode_noalloc", "moe_router_topk_softmax",
-    "qkv_bias_rope", "qkv_bias_rope_append_paged", "GPT_OSS_YARN", "EXPORTED_SYMBOLS",
+    "qkv_bias_rope", "qkv_bias_rope_append_paged", "linear_bias", "GPT_OSS_YARN", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "sink_attn_decode_splits", "sink_attn_device_status", "sink_attn_set_wait_timeout_ns",
     "sink_attn_status_string", "sink_attn_abi_version", "sink_attn_selftest_wait_timeout",
     "sink_attn_decode_noalloc", "moe_router_topk_softmax", "qkv_bias_rope",
-    "qkv_bias_rope_append_paged",
+    "qkv_bias_rope_append_paged", "linear_bias",
 )
 
 _p, _i, _f, _d, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_longlong
@@ -53,6 +53,7 @@ _SIGNATURES = {
     "sink_attn_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p,
                                       _p]),
     "moe_router_topk_softmax": (_i, [_p, _ll, _i, _i, _p, _p, _p, _p]),
+    "linear_bias": (_i, [_p, _p, _p, _i, _i, _i, _p, _p]),
     "qkv_bias_rope": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p, _p, _p]),
     "qkv_bias_rope_append_paged": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p,
                                         _p, _p, _i, _i, _i, _p]),
@@ -354,3 +355,22 @@ def qkv_bias_rope_append_paged(qkv, bias, cu_seqlens_q, kv_lens, paged_k, paged_
         _ptr(page_table), page_size, page_table.shape[1], num_pages, _stream(stream))
     _check(st, "qkv_bias_rope_append_paged")
     return q_out
+
+
+def linear_bias(x, w, bias=None, out=None, stream=None):
+    """out [M, N] = x [M, K] @ w[N, K]^T + bias[N] on the tcgen05 tensor cores, bf16 in and out,
+    the fp32 accumulator seeded with the bias (page "GPT-OSS on day 0", section "Kernels for
+    GPT-OSS / MoE")."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(w, "w", torch.bfloat16)
+    if bias is not None:
+        _dev(bias, "bias", torch.bfloat16)
+    m, k = x.shape
+    n = w.shape[0]
+    if w.shape[1] != k:
+        raise ValueError(f"w is {tuple(w.shape)}, expected [N, {k}]")
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _dev(out, "out", torch.bfloat16)
+    _check(load_library().linear_bias(_ptr(x), _ptr(w), _ptr(bias), m, n, k, _ptr(out), _stream(stream)),
+           "linear_bias")
+    return out

@@ -21,7 +21,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libsinkattn.so")
-SOURCES = ["abi.cu", "decode.cu", "merge.cu", "prefill.cu", "noalloc.cu", "router.cu", "rope.cu"]
+SOURCES = ["abi.cu", "decode.cu", "merge.cu", "prefill.cu", "noalloc.cu", "router.cu", "rope.cu",
+           "linear.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + os.path.join(ROOT, "include"), "-Xptxas", "-v"]

@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include "../../include/linear_bias.h"
 #include "../../include/moe_router.h"
 #include "../../include/qkv_rope.h"
 #include "../../include/sink_attn.h"
@@ -71,6 +72,20 @@ sa_status map_tokens_heads(CUtensorMap* m, const void* base, long long rows, int
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SA_OK : SA_ERR_CUDA;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of (box_rows rows, 64 columns).
+sa_status map_matrix(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  if (sa_status s = encoder(&enc)) return s;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? SA_OK : SA_ERR_CUDA;
@@ -183,6 +198,7 @@ sa_status rope_common(const void* qkv, const void* bias, const int32_t* cu_q, co
   if (work && paged && (!kv_lens || !page_table || !k_out || !v_out)) return SA_ERR_NULL;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SA_ERR_SHAPE;
   if (head_dim != sa::kHeadDim) return SA_ERR_UNSUPPORTED;
+  if (hq + 2 * hkv > 128) return SA_ERR_UNSUPPORTED;  // one thread per (head row, quarter) per token
   if (paged && (max_pages <= 0 || num_pages <= 0)) return SA_ERR_SHAPE;
   if (static_cast<long long>(total_tokens) * (hq + 2 * hkv) * sa::kHeadDim >= (1LL << 40))
     return SA_ERR_SHAPE;
@@ -400,6 +416,34 @@ sa_status sink_attn_prefill_paged(const void* q, const void* paged_k, const void
   return prefill_common(q, paged_k, paged_v, page_table, cu_seqlens_q, kv_lens, sinks, batch,
                         total_q_tokens, max_q_len, num_qo_heads, num_kv_heads, head_dim,
                         max_pages, num_pages, sm_scale, causal, out, lse, stream, true);
+}
+
+sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int n, int k,
+                      void* out, cudaStream_t stream) {
+  if (m < 0 || n <= 0 || k <= 0) return SA_ERR_SHAPE;
+  if (n % 8 != 0 || k % 8 != 0) return SA_ERR_UNSUPPORTED;
+  if (m == 0) return SA_OK;
+  if (!x || !w || !out) return SA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(out) ||
+      (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)))
+    return SA_ERR_ALIGNMENT;
+  unsigned* status = nullptr;
+  if (sa_status s = status_ptr(&status)) return s;
+  sa::LinearArgs a{};
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.out = static_cast<uint16_t*>(out);
+  a.M = m;
+  a.N = n;
+  a.K = k;
+  a.block_n = sa::linear_tile_n(n);
+  a.tiles_m = (m + 127) / 128;
+  a.tiles_n = (n + a.block_n - 1) / a.block_n;
+  a.status = status;
+  a.timeout_ns = g_timeout_ns;
+  CUtensorMap am, bm;
+  if (sa_status s = map_matrix(&am, x, m, k, 128)) return s;
+  if (sa_status s = map_matrix(&bm, w, n, k, a.block_n)) return s;
+  return sa::launch_linear(am, bm, a, sm_count(), stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
 sa_status moe_router_topk_softmax(const void* logits, long long num_tokens, int num_experts,

@@ -1,0 +1,312 @@
+// Linear layer with bias, out = x W^T + b, on the 5th-generation tensor cores
+// (page "GPT-OSS on day 0": the output projection and the experts carry bias
+// terms; section "Kernels for GPT-OSS / MoE": bias support was added to the
+// expert GEMMs by starting the accumulator registers from the bias values, a
+// one-time step per output (MN) tile).
+//
+// The Blackwell form of that idea: the accumulator lives in tensor memory, so
+// the epilogue warps write the bias row into the TMEM accumulator of the next
+// tile (tcgen05.st) and every MMA of the tile accumulates onto it; there is no
+// zero-initialising first MMA and no bias add in the epilogue.
+//
+// Persistent kernel, one CTA per SM, 256 threads:
+//   warp 0        TMA producer: A (x, 128 x 64) and B (W, BN x 64) boxes,
+//                 128-byte swizzle, into a kStages-deep ring
+//   warp 1        TMEM owner and MMA issuer (one elected thread): per 64-wide
+//                 K step four tcgen05.mma M=128 N=BN K=16, accumulate always on
+//   warps 4..7    epilogue: warp w reads TMEM lanes [32 (w-4), +32) (one output
+//                 row per thread), converts to bf16, stores, then seeds the
+//                 buffer with the bias of the tile that will use it next
+// Two TMEM accumulators alternate, so the epilogue of tile i overlaps the
+// MMAs of tile i + 1.  Tiles are numbered with the N index fastest: the CTAs
+// working at the same time share one 128-row block of x through L2.
+#include <cstdint>
+
+#include "ops_internal.h"
+#include "ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kLinThreads = 256;
+constexpr int kEpiWarp0 = 4;
+
+__device__ __forceinline__ uint64_t sw128_kmajor(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(1024 >> 4) << 16;  // leading byte offset (unused, K-major SW128)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+  d |= 1ull << 46;                               // tcgen05 descriptor version
+  d |= 2ull << 61;                               // 128-byte swizzle
+  return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_kk(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+template <int BN>
+struct LinCfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (200 * 1024) / kStageBytes > 6 ? 6 : (200 * 1024) / kStageBytes;
+  static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + static_cast<size_t>(kStages) * kStageBytes + 256;
+};
+
+struct LinBarriers {
+  uint64_t full[8], empty[8], acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int issued;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Write bias[n0 + c] (c < BN, zero past N) into every lane of the accumulator
+// columns [col, col + BN) owned by this warp's TMEM lane quarter.
+template <int BN>
+__device__ __forceinline__ void seed_bias(uint32_t taddr, const uint16_t* bias, int n0, int N) {
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 16) {
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int n = n0 + c + i;
+      const uint32_t bits = (bias != nullptr && n < N) ? static_cast<uint32_t>(__ldg(bias + n)) : 0u;
+      r[i] = bits << 16;  // bf16 -> fp32 bit pattern
+    }
+    tmem_st16(taddr + c, r);
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kLinThreads, 1)
+linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                   const LinearArgs a) {
+  using C = LinCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  LinBarriers& sb = *reinterpret_cast<LinBarriers*>(tiles + static_cast<size_t>(C::kStages) * C::kStageBytes);
+  volatile int* abort_flag = &sb.abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_total = a.tiles_m * a.tiles_n;
+  constexpr uint32_t kIdesc = idesc_bf16_kk(kBM, BN);
+  const int k_steps = (a.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&sb.full[s]), 1);
+      mbar_init(smem_u32(&sb.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sb.acc_full[b]), 1);
+      mbar_init(smem_u32(&sb.acc_empty[b]), 4);
+    }
+    mbar_init(smem_u32(&sb.drain), 1);
+    sb.abort_flag = 0;
+    sb.issued = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sb.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sb.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&amap);
+      tma_prefetch_desc(&bmap);
+      const uint64_t pol_a = l2_policy_evict_first();  // x: read by the tiles_n CTAs of one row block
+      const uint64_t pol_b = l2_policy_evict_last();   // W: re-read by every row block
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles_total && ok; t += gridDim.x) {
+        const int m0 = (t / a.tiles_n) * kBM;
+        const int n0 = (t % a.tiles_n) * BN;
+        for (int kb = 0; kb < k_steps; ++kb, ++g) {
+          const int s = g % C::kStages;
+          if (g >= C::kStages &&
+              !wait_or_abort(smem_u32(&sb.empty[s]), ((g / C::kStages) - 1) & 1, a.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&sb.full[s]);
+          const uint32_t dst = smem_u32(tiles + static_cast<size_t>(s) * C::kStageBytes);
+          mbar_arrive_expect_tx(bar, C::kStageBytes);
+          tma_load_2d(dst, &amap, kb * kBK, m0, bar, pol_a);
+          tma_load_2d(dst + C::kABytes, &bmap, kb * kBK, n0, bar, pol_b);
+          sb.issued = g + 1;
+        }
+      }
+      if (!ok) raise_status(a.status, kStatusTimeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles_total && ok; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        ok = wait_or_abort(smem_u32(&sb.acc_empty[b]), (i >> 1) & 1, a.timeout_ns, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * BN;
+        for (int kb = 0; kb < k_steps; ++kb, ++g) {
+          const int s = g % C::kStages;
+          ok = wait_or_abort(smem_u32(&sb.full[s]), (g / C::kStages) & 1, a.timeout_ns, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(tiles + static_cast<size_t>(s) * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_ss(d, sw128_kmajor(a_addr + kk * 32), sw128_kmajor(b_addr + kk * 32), kIdesc, 1u);
+          tc_commit(smem_u32(&sb.empty[s]));
+        }
+        if (ok) tc_commit(smem_u32(&sb.acc_full[b]));
+      }
+      if (!ok) raise_status(a.status, kStatusTimeout);
+      // every MMA issued by this thread has finished before TMEM is released
+      tc_commit(smem_u32(&sb.drain));
+      if (!mbar_wait(smem_u32(&sb.drain), 0, a.timeout_ns)) raise_status(a.status, kStatusTimeout);
+    }
+  } else if (warp >= kEpiWarp0) {
+    const int q = warp - kEpiWarp0;                    // TMEM lane quarter
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // seed both accumulators for this CTA's first two tiles
+    for (int j = 0; j < 2; ++j) {
+      const int t = blockIdx.x + j * gridDim.x;
+      if (t < tiles_total) seed_bias<BN>(tmem + lane_base + j * BN, a.bias, (t % a.tiles_n) * BN, a.N);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sb.acc_empty[j]));
+    }
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles_total; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      bool ok = true;
+      if (lane == 0) ok = wait_or_abort(smem_u32(&sb.acc_full[b]), (i >> 1) & 1, a.timeout_ns, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const int m0 = (t / a.tiles_n) * kBM;
+      const int n0 = (t % a.tiles_n) * BN;
+      const int row = m0 + 32 * q + lane;
+      uint16_t* orow = a.out + static_cast<long long>(row) * a.N;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + b * BN + c, r);
+        tc_wait_ld();
+        if (row < a.M) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int n = n0 + c + 8 * v;
+            if (n < a.N) {
+              const uint4 w = make_uint4(
+                  pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                  pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                  pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                  pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+              *reinterpret_cast<uint4*>(orow + n) = w;
+            }
+          }
+        }
+      }
+      // this buffer's next tile starts from its bias
+      const int t2 = t + 2 * gridDim.x;
+      if (t2 < tiles_total) seed_bias<BN>(tmem + lane_base + b * BN, a.bias, (t2 % a.tiles_n) * BN, a.N);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sb.acc_empty[b]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) {
+    // copies still in flight land before the shared memory is released
+    const int issued = sb.issued;
+    for (int s = 0; s < C::kStages && s < issued; ++s) {
+      const int last = issued - 1 - ((issued - 1 - s) % C::kStages);
+      if (!mbar_wait(smem_u32(&sb.full[s]), (last / C::kStages) & 1, a.timeout_ns))
+        raise_status(a.status, kStatusTimeout);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BN>
+cudaError_t launch_linear_t(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
+                            int sms, cudaStream_t stream) {
+  using C = LinCfg<BN>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(linear_bias_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int tiles = a.tiles_m * a.tiles_n;
+  const int grid = tiles < sms ? tiles : sms;
+  linear_bias_kernel<BN><<<grid, kLinThreads, C::kSmem, stream>>>(amap, bmap, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int linear_tile_n(int n) {
+  // fewest estimated cycles per row block: ceil(N / BN) tiles of (BN + 32) each
+  int best = 256;
+  long long best_cost = -1;
+  for (int bn : {256, 192, 128}) {
+    const long long cost = static_cast<long long>((n + bn - 1) / bn) * (bn + 32);
+    if (best_cost < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_linear(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
+                          int sms, cudaStream_t stream) {
+  switch (a.block_n) {
+    case 128: return launch_linear_t<128>(amap, bmap, a, sms, stream);
+    case 192: return launch_linear_t<192>(amap, bmap, a, sms, stream);
+    default: return launch_linear_t<256>(amap, bmap, a, sms, stream);
+  }
+}
+
+}  // namespace sa

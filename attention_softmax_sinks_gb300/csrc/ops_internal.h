@@ -3,6 +3,7 @@
 // arrive here already validated.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -36,6 +37,20 @@ struct RopeArgs {
   unsigned* status;
 };
 
+struct LinearArgs {
+  const uint16_t* bias;  // bf16 [N] or nullptr
+  uint16_t* out;         // bf16 [M, N]
+  int M, N, K;
+  int block_n, tiles_m, tiles_n;
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+// Output tile width (128, 192 or 256) for N output features.
+int linear_tile_n(int n);
+// amap: x [M, K] in boxes of 128 rows x 64; bmap: W [N, K] in boxes of block_n rows x 64.
+cudaError_t launch_linear(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
+                          int sms, cudaStream_t stream);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream);
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t stream);
 

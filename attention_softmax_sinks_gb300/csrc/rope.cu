@@ -8,14 +8,16 @@
 // (prefill) or every decode step, so the rotation lives here and the attention
 // kernels read K as stored.
 //
-// One CTA handles kRopeTokens tokens.  First 32 threads per token compute, for
-// the token's position p and each of the 32 frequency pairs, the angle p * theta
-// in fp64, reduce it to [-pi, pi] in fp64 and take sincosf of the reduced fp32
-// angle; the (cos, sin) table, scaled by the temperature, goes to shared
-// memory with the token's page slot.  Then the CTA streams the token rows
-// (Hq + 2 Hkv head rows of 64 bf16) in 16-byte chunks: a head row is 8 chunks
-// held by 8 consecutive lanes, and a lane pairs feature i with feature i + 32
-// by exchanging its 8 biased values with lane ^ 4.
+// One CTA handles kRopeTokens consecutive tokens.  Thread u of a token owns
+// one head row and one quarter j of its features: features [8j, 8j + 8) and
+// their rotation partners [8j + 32, 8j + 40), loaded as two 16-byte vectors,
+// so no lane exchange is needed; its bias values are loaded once.  First the
+// CTA computes, for each token position p and frequency pair i, the angle
+// p * theta'_i in fp64, reduces it to [-pi, pi] in fp64 and takes sincosf of
+// the reduced fp32 angle; the (cos, sin) table, scaled by the temperature, and
+// each token's page slot go to shared memory.  Then every thread walks the
+// CTA's tokens with the next token's two loads in flight while it rotates and
+// stores the current one.
 #include <cmath>
 #include <cstdint>
 
@@ -25,131 +27,160 @@
 namespace sa {
 namespace {
 
-constexpr int kRopeTokens = 4;
-constexpr int kRopeThreads = 256;
+constexpr int kRopeTokens = 16;
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__global__ void __launch_bounds__(kRopeThreads) qkv_rope_kernel(const RopeArgs a) {
-  __shared__ float2 cs[kRopeTokens][kMaxRopePairs];
-  __shared__ long long dst_row[kRopeTokens];  // paged: (page * Hkv) * 16 + slot row; contiguous: token
-  const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * kRopeTokens;
-  const int rows = a.hq + 2 * a.hkv;
+__device__ __forceinline__ void widen8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_lo(w[i]);
+    f[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
 
-  if (tid < kRopeTokens * kMaxRopePairs) {
-    const int tok = tid / kMaxRopePairs;
-    const int pair = tid % kMaxRopePairs;
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// blockDim.x = units * tpar: units = 4 (Hq + 2 Hkv) threads per token, tpar
+// tokens processed side by side.
+__global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpar) {
+  __shared__ float4 cs4[kRopeTokens][kMaxRopePairs / 2];  // (cos, sin) of pairs 2i, 2i + 1
+  __shared__ long long dst_row[kRopeTokens];  // paged: page * Hkv * 16 + slot; contiguous: token
+  const int rows = a.hq + 2 * a.hkv;
+  const int units = rows * 4;
+  const int tid = threadIdx.x;
+  const int unit = tid % units;
+  const int lane_tok = tid / units;  // < tpar
+  const int row = unit >> 2;
+  const int j = unit & 3;
+  const int t0 = blockIdx.x * kRopeTokens;
+  const int ntok = min(kRopeTokens, a.total_tokens - t0);
+
+  const long long col = static_cast<long long>(row) * kHeadDim + 8 * j;
+  auto load_pair = [&](int tok, uint4& lo, uint4& hi) {
+    const uint16_t* src = a.qkv + static_cast<long long>(t0 + tok) * rows * kHeadDim + col;
+    lo = __ldg(reinterpret_cast<const uint4*>(src));
+    hi = __ldg(reinterpret_cast<const uint4*>(src + 32));
+  };
+  uint4 xl = make_uint4(0, 0, 0, 0), xh = xl;
+  if (lane_tok < ntok) load_pair(lane_tok, xl, xh);  // in flight while the angles are computed
+  float b1[8], b2[8];
+  if (a.bias) {
+    widen8(__ldg(reinterpret_cast<const uint4*>(a.bias + col)), b1);
+    widen8(__ldg(reinterpret_cast<const uint4*>(a.bias + col + 32)), b2);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b1[i] = b2[i] = 0.0f;
+  }
+
+  float* cs = reinterpret_cast<float*>(cs4);
+  for (int e = tid; e < ntok * kMaxRopePairs; e += blockDim.x) {
+    const int tok = e / kMaxRopePairs;
+    const int pair = e % kMaxRopePairs;
     const int t = t0 + tok;
-    if (t < a.total_tokens) {
-      // sequence of token t: the last b with cu_q[b] <= t (empty sequences skipped)
-      int lo = 0, hi = a.batch;  // invariant: cu_q[lo] <= t < cu_q[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(a.cu_q + mid) <= t) lo = mid; else hi = mid;
-      }
-      const int b = lo;
-      const int q_start = __ldg(a.cu_q + b);
-      const int q_len = __ldg(a.cu_q + b + 1) - q_start;
-      const int kv = a.kv_lens ? __ldg(a.kv_lens + b) : q_len;
-      const long long pos = static_cast<long long>(kv) - q_len + (t - q_start);
-      const double ang = static_cast<double>(pos) * a.inv_freq[pair];
-      const double red = ang - kTwoPi * rint(ang * kInvTwoPi);
-      float s, c;
-      sincosf(static_cast<float>(red), &s, &c);
-      cs[tok][pair] = make_float2(c * a.mscale, s * a.mscale);
-      if (pair == 0) {
-        long long dst = t;
-        if (a.paged) {
-          dst = -1;
-          const long long pidx = pos >> 4;
-          if (pos < 0 || pidx >= a.max_pages || kv < q_len) {
-            raise_status(a.status, kStatusBadLen);
-          } else {
-            const int page = __ldg(a.page_table + static_cast<long long>(b) * a.max_pages + pidx);
-            if (page < 0 || page >= a.num_pages) raise_status(a.status, kStatusBadPage);
-            else dst = static_cast<long long>(page) * a.hkv * kPageSize + (pos & 15);
-          }
+    // sequence of token t: the last b with cu_q[b] <= t (empty sequences skipped)
+    int lo = 0, hi = a.batch;  // invariant: cu_q[lo] <= t < cu_q[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(a.cu_q + mid) <= t) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int q_start = __ldg(a.cu_q + b);
+    const int q_len = __ldg(a.cu_q + b + 1) - q_start;
+    const int kv = a.kv_lens ? __ldg(a.kv_lens + b) : q_len;
+    const long long pos = static_cast<long long>(kv) - q_len + (t - q_start);
+    const double ang = static_cast<double>(pos) * a.inv_freq[pair];
+    const double red = ang - kTwoPi * rint(ang * kInvTwoPi);
+    float sn, cn;
+    sincosf(static_cast<float>(red), &sn, &cn);
+    cs[(tok * kMaxRopePairs + pair) * 2] = cn * a.mscale;
+    cs[(tok * kMaxRopePairs + pair) * 2 + 1] = sn * a.mscale;
+    if (pair == 0) {
+      long long dst = t;
+      if (a.paged) {
+        dst = -1;
+        const long long pidx = pos >> 4;
+        if (pos < 0 || pidx >= a.max_pages || kv < q_len) {
+          raise_status(a.status, kStatusBadLen);
+        } else {
+          const int page = __ldg(a.page_table + static_cast<long long>(b) * a.max_pages + pidx);
+          if (page < 0 || page >= a.num_pages) raise_status(a.status, kStatusBadPage);
+          else dst = static_cast<long long>(page) * a.hkv * kPageSize + (pos & 15);
         }
-        dst_row[tok] = dst;
       }
+      dst_row[tok] = dst;
     }
   }
   __syncthreads();
 
-  const int chunks = kRopeTokens * rows * 8;
-  for (int base = 0; base < chunks; base += kRopeThreads) {
-    const int c = base + tid;
-    const int tok = c / (rows * 8);
-    const int t = t0 + tok;
-    const bool live = c < chunks && t < a.total_tokens;
-    const int row = (c >> 3) % rows;
-    const int part = c & 7;
-    float y[8];
-    if (live) {
-      const long long off = (static_cast<long long>(t) * rows + row) * kHeadDim + part * 8;
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.qkv + off));
-      uint4 bb = make_uint4(0, 0, 0, 0);
-      if (a.bias) bb = __ldg(reinterpret_cast<const uint4*>(a.bias + row * kHeadDim + part * 8));
-      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-      const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+  const bool rotate = row < a.hq + a.hkv;
+  const bool is_q = row < a.hq;
+  const bool is_k = !is_q && rotate;
+  const int kvh = is_q ? 0 : (is_k ? row - a.hq : row - a.hq - a.hkv);
+  uint16_t* kv_dst = is_k ? a.k_out : a.v_out;
+  for (int tok = lane_tok; tok < ntok; tok += tpar) {
+    uint4 nl = xl, nh = xh;
+    if (tok + tpar < ntok) load_pair(tok + tpar, nl, nh);
+    float y1[8], y2[8];
+    widen8(xl, y1);
+    widen8(xh, y2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y1[i] += b1[i];
+      y2[i] += b2[i];
+    }
+    float o1[8], o2[8];
+    if (rotate) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        y[2 * i] = bf16_lo(xw[i]) + bf16_lo(bw[i]);
-        y[2 * i + 1] = bf16_hi(xw[i]) + bf16_hi(bw[i]);
+        const float4 r = cs4[tok][4 * j + i];  // pairs 8j + 2i and 8j + 2i + 1
+        o1[2 * i] = fmaf(y1[2 * i], r.x, -y2[2 * i] * r.y);
+        o2[2 * i] = fmaf(y2[2 * i], r.x, y1[2 * i] * r.y);
+        o1[2 * i + 1] = fmaf(y1[2 * i + 1], r.z, -y2[2 * i + 1] * r.w);
+        o2[2 * i + 1] = fmaf(y2[2 * i + 1], r.z, y1[2 * i + 1] * r.w);
       }
     } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = 0.0f;
-    }
-    float o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = __shfl_xor_sync(0xffffffffu, y[i], 4);
-    if (!live) continue;
-    const bool second = part >= 4;
-    if (row < a.hq + a.hkv) {
-      const int p0 = (part & 3) * 8;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float2 r = cs[tok][p0 + i];
-        // first half: a cos - b sin ; second half: b cos + a sin
-        o[i] = second ? fmaf(y[i], r.x, o[i] * r.y) : fmaf(y[i], r.x, -o[i] * r.y);
+        o1[i] = y1[i];
+        o2[i] = y2[i];
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = y[i];
     }
-    const uint4 out = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                                 pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-    if (row < a.hq) {
-      *reinterpret_cast<uint4*>(a.q_out + (static_cast<long long>(t) * a.hq + row) * kHeadDim +
-                                part * 8) = out;
-    } else {
-      const bool is_k = row < a.hq + a.hkv;
-      const int kvh = is_k ? row - a.hq : row - a.hq - a.hkv;
-      uint16_t* dst = is_k ? a.k_out : a.v_out;
+    const int t = t0 + tok;
+    uint16_t* dst = nullptr;
+    if (is_q) {
+      dst = a.q_out + (static_cast<long long>(t) * a.hq + row) * kHeadDim + 8 * j;
+    } else if (kv_dst != nullptr && dst_row[tok] >= 0) {
       const long long r = dst_row[tok];
-      if (dst == nullptr || r < 0) continue;
-      long long off;
-      if (a.paged) {
-        // r = page * Hkv * 16 + slot: head kvh of that page starts kvh * 16 rows later
-        off = (r + static_cast<long long>(kvh) * kPageSize) * kHeadDim + part * 8;
-      } else {
-        off = (r * a.hkv + kvh) * kHeadDim + part * 8;
-      }
-      *reinterpret_cast<uint4*>(dst + off) = out;
+      // paged: r = page * Hkv * 16 + slot, head kvh of that page starts kvh * 16 rows later
+      const long long off = a.paged ? (r + static_cast<long long>(kvh) * kPageSize) * kHeadDim
+                                    : (r * a.hkv + kvh) * kHeadDim;
+      dst = kv_dst + off + 8 * j;
     }
+    if (dst) {
+      *reinterpret_cast<uint4*>(dst) = pack8(o1);
+      *reinterpret_cast<uint4*>(dst + 32) = pack8(o2);
+    }
+    xl = nl;
+    xh = nh;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t stream) {
+  const int units = 4 * (a.hq + 2 * a.hkv);
+  int tpar = 256 / units;
+  tpar = tpar < 1 ? 1 : (tpar > kRopeTokens ? kRopeTokens : tpar);
   const int blocks = (a.total_tokens + kRopeTokens - 1) / kRopeTokens;
-  qkv_rope_kernel<<<blocks, kRopeThreads, 0, stream>>>(a);
+  qkv_rope_kernel<<<blocks, units * tpar, 0, stream>>>(a, tpar);
   return cudaGetLastError();
 }
 

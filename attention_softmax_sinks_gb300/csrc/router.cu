@@ -2,7 +2,8 @@
 // GPT-OSS / MoE": the softmax runs over the K selected experts only, and the
 // expert weights are computed in bf16).
 //
-// One warp per token row.  The bf16 logits are turned into 32-bit keys that
+// One warp per token row (a warp walks rows grid-stride and loads the next
+// row's logits before ranking the current one).  The bf16 logits are turned into 32-bit keys that
 // sort like the values (high 16 bits: the bf16 pattern mapped to an unsigned
 // order, -0 folded onto +0; low 16 bits: 0xFFFF - expert, so that among equal
 // logits the lower expert index is the larger key).  K rounds of a warp-wide
@@ -18,7 +19,7 @@
 namespace sa {
 namespace {
 
-constexpr int kRouterWarps = 8;
+constexpr int kRouterWarps = 32;
 constexpr int kMaxTopK = 8;
 
 __device__ __forceinline__ uint32_t order16(uint32_t bits) {
@@ -42,15 +43,20 @@ router_topk_kernel(const RouterArgs a) {
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const long long stride = static_cast<long long>(gridDim.x) * kRouterWarps;
-  for (long long t = static_cast<long long>(blockIdx.x) * kRouterWarps + (threadIdx.x >> 5);
-       t < a.num_tokens; t += stride) {
+  auto load_keys = [&](long long t, uint32_t (&key)[kPerLane]) {
     const uint16_t* row = a.logits + t * E;
-    uint32_t key[kPerLane];
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) {
       const int e = lane + 32 * j;
-      key[j] = e < E ? ((order16(__ldg(row + e)) << 16) | (0xFFFFu - e)) : 0u;
+      key[j] = (t < a.num_tokens && e < E) ? ((order16(__ldg(row + e)) << 16) | (0xFFFFu - e)) : 0u;
     }
+  };
+  long long t = static_cast<long long>(blockIdx.x) * kRouterWarps + (threadIdx.x >> 5);
+  uint32_t key[kPerLane];
+  load_keys(t, key);
+  for (; t < a.num_tokens; t += stride) {
+    uint32_t next[kPerLane];
+    load_keys(t + stride, next);  // the next row's logits are in flight while this row is ranked
     uint32_t pick[kMaxTopK];
 #pragma unroll
     for (int r = 0; r < kMaxTopK; ++r) {
@@ -85,6 +91,8 @@ router_topk_kernel(const RouterArgs a) {
         if (a.counts) atomicAdd(&hist[e], 1);
       }
     }
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) key[j] = next[j];
   }
   if (a.counts) {
     __syncthreads();
@@ -98,8 +106,10 @@ cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t stream) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // one 1024-thread block per SM at most: few blocks keep the global count
+  // atomics (one per expert per block) off the critical path
   const long long need = (a.num_tokens + kRouterWarps - 1) / kRouterWarps;
-  const long long cap = static_cast<long long>(sms) * 8;
+  const long long cap = static_cast<long long>(sms);
   const int blocks = static_cast<int>(need < cap ? need : cap);
   router_topk_kernel<kPerLane><<<blocks, kRouterWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();

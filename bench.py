@@ -276,6 +276,7 @@ def run_ours(args, rank, world, device):
         mixed = bench_mixed(args, sa, torch, device, pk)
         graph = bench_graph_decode(args, sa, torch, device, pk)
         around = bench_around_attention(args, sa, torch, device, pk)
+        around["linear_bias"] = bench_linear(args, sa, torch, device, pk)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -492,6 +493,32 @@ def bench_around_attention(args, sa, torch, device, pk):
             "gpu_launches": 2 * (reps + 3)}
 
 
+def bench_linear(args, sa, torch, device, pk):
+    """Bias-seeded tcgen05 linear layer at the attention output projection of the
+    causal-prefill batch: 32768 tokens x (64 heads x 64) = 4096 inputs -> 2880 features
+    (GPT-OSS hidden size, page "GPT-OSS on day 0", section "Performance tweaks").
+    cuBLAS (torch's bf16 linear with bias) is timed beside it for context only."""
+    stream = torch.cuda.current_stream(device)
+    m, n, k = 32768, 2880, 4096
+    d = workloads.make_linear(61, m, n, k)
+    x, w, b = (to_dev(d[key], torch, device) for key in ("x", "w", "bias"))
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+    reps = max(5, min(30, args.steps // 10))
+    ms = _timed_flushed(torch, device, stream, lambda: sa.linear_bias(x, w, b, out=out, stream=stream), reps)
+    ref_ms = _timed_flushed(torch, device, stream, lambda: torch.nn.functional.linear(x, w, b), reps)
+    flops = 2.0 * m * n * k
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "output projection of 32768 tokens: [32768, 4096] x [2880, 4096]^T + bias, bf16, "
+                        "fp32 accumulator seeded with the bias; L2 flushed before each launch",
+            "kernel": "linear_bias_kernel", "ms": round(ms, 4), "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tf / pk["bf16"], 4),
+                         "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)"},
+            "cublas_context": {"ms": round(ref_ms, 4), "tflops": round(flops / (ref_ms * 1e-3) / 1e12, 2),
+                               "note": "torch.nn.functional.linear (cuBLAS), not on this library's path"},
+            "gpu_launches": reps + 3}
+
+
 def bench_prefill(args, sa, torch, device, pk):
     cfg = PREFILL
     lens = [cfg["seqlen"]] * cfg["batch"]
@@ -611,6 +638,9 @@ def run_profile_case(case):
 
     decode:  32 sequences x 4096 tokens (256 MiB of KV, larger than L2), 64/8 heads, 4 splits.
     prefill: 1 x 8192 tokens causal, 64/8 heads.
+    linear:  [16384, 4096] x [2880, 4096]^T + bias (half the bench's output-projection rows).
+    rope:    32768 tokens, 64/8 heads, bias + YaRN.
+    router:  32768 tokens x 128 experts, top 4, counts.
     """
     import torch
     import attention_softmax_sinks_gb300 as sa
@@ -628,6 +658,22 @@ def run_profile_case(case):
             po, pl = sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
                                          dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=4)
             sa.sink_attn_merge(po, pl)
+    elif case == "linear":
+        d = workloads.make_linear(61, 16384, 2880, 4096)
+        x, w, b = (to_dev(d[key], torch, device) for key in ("x", "w", "bias"))
+        out = torch.empty((16384, 2880), dtype=torch.bfloat16, device=device)
+        for _ in range(5):
+            sa.linear_bias(x, w, b, out=out)
+    elif case == "rope":
+        cu = to_dev(workloads.cu_seqlens_from([8192] * 4), torch, device)
+        inp = workloads.make_qkv(41, 32768, 64, 8)
+        qkv, bias = to_dev(inp["qkv"], torch, device), to_dev(inp["bias"], torch, device)
+        for _ in range(5):
+            sa.qkv_bias_rope(qkv, bias, cu, 64, 8)
+    elif case == "router":
+        logits = to_dev(workloads.make_router_logits(42, 32768, 128, std=2.0), torch, device)
+        for _ in range(5):
+            sa.moe_router_topk_softmax(logits, 4, return_counts=True)
     else:
         cfg = PREFILL
         host = workloads.make_prefill(cfg["seed"], [cfg["seqlen"]], cfg["hq"], cfg["hkv"], cfg["d"],
@@ -648,7 +694,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
-    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill", "linear", "rope", "router"], default=None,
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:

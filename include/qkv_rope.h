@@ -22,7 +22,8 @@
  * Input qkv is the projection output without bias, bf16 [T, (Hq + 2 Hkv) * 64]
  * (all query heads, then key heads, then value heads); bias bf16
  * [(Hq + 2 Hkv) * 64] or NULL is added first (in fp32).  q and k are rotated,
- * v is not; results are rounded once to bf16.  head_dim is 64.
+ * v is not; results are rounded once to bf16.  head_dim is 64 and
+ * Hq + 2 Hkv <= 128 (SA_ERR_UNSUPPORTED otherwise).
  *
  * Conventions of sink_attn.h apply (device pointers, 16-byte alignment,
  * asynchronous on `stream`, no allocation, status codes).

@@ -171,6 +171,7 @@ def _rope(lib, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(qkv=None), SA_ERR_NULL), (dict(cu=None), SA_ERR_NULL), (dict(q=None), SA_ERR_NULL),
     (dict(d=128), SA_ERR_UNSUPPORTED), (dict(hq=6, hkv=4), SA_ERR_SHAPE), (dict(batch=-1), SA_ERR_SHAPE),
+    (dict(hq=128, hkv=8), SA_ERR_UNSUPPORTED),
     (dict(yarn=(1.0, 32.0, 4096, 32.0, 1.0)), SA_ERR_SHAPE), (dict(yarn=(1e4, 0.5, 4096, 32.0, 1.0)), SA_ERR_SHAPE),
     (dict(yarn=(1e4, 32.0, 4096, 1.0, 32.0)), SA_ERR_SHAPE), (dict(yarn=(1e4, 32.0, 0, 32.0, 1.0)), SA_ERR_SHAPE),
     (dict(yarn=(1e4, 1.0, 0, 0.0, 0.0)), SA_OK),   # factor 1: plain rotary, YaRN constants unused
@@ -195,3 +196,16 @@ def test_rope_paged_rejects(lib):
     assert f(*bad) == SA_ERR_SHAPE
     ok = list(args); ok[4] = 0
     assert f(*ok) == SA_OK
+
+
+def test_linear_rejects_before_launch(lib):
+    f = lib.linear_bias
+    assert f(FAKE, FAKE, None, -1, 64, 64, FAKE, None) == SA_ERR_SHAPE
+    assert f(FAKE, FAKE, None, 4, 0, 64, FAKE, None) == SA_ERR_SHAPE
+    assert f(FAKE, FAKE, None, 4, 60, 64, FAKE, None) == SA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, None, 4, 64, 20, FAKE, None) == SA_ERR_UNSUPPORTED
+    assert f(None, FAKE, None, 4, 64, 64, FAKE, None) == SA_ERR_NULL
+    assert f(FAKE, FAKE, None, 4, 64, 64, None, None) == SA_ERR_NULL
+    assert f(MISALIGNED, FAKE, None, 4, 64, 64, FAKE, None) == SA_ERR_ALIGNMENT
+    assert f(FAKE, FAKE, ctypes.c_void_p(0x10001), 4, 64, 64, FAKE, None) == SA_ERR_ALIGNMENT
+    assert f(None, None, None, 0, 64, 64, None, None) == SA_OK
