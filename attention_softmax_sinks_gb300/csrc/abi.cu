@@ -459,7 +459,7 @@ sa_status moe_router_topk_softmax(const void* logits, long long num_tokens, int 
   if (num_tokens == 0) return SA_OK;
   sa::RouterArgs a{static_cast<const uint16_t*>(logits), topk_idx,
                    static_cast<uint16_t*>(topk_weight), expert_counts, num_tokens, num_experts,
-                   top_k};
+                   top_k, (num_experts % 8 == 0 && aligned16(logits)) ? 1 : 0};
   return sa::launch_router(a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 

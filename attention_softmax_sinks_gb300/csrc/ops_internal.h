@@ -17,6 +17,7 @@ struct RouterArgs {
   int32_t* counts;         // [E] (already zeroed) or nullptr
   long long num_tokens;
   int num_experts, top_k;
+  int vec16;               // rows read as 16-byte vectors (E % 8 == 0, 16-byte aligned base)
 };
 
 constexpr int kMaxRopePairs = kHeadDim / 2;

@@ -2,15 +2,19 @@
 // GPT-OSS / MoE": the softmax runs over the K selected experts only, and the
 // expert weights are computed in bf16).
 //
-// One warp per token row (a warp walks rows grid-stride and loads the next
-// row's logits before ranking the current one).  The bf16 logits are turned into 32-bit keys that
-// sort like the values (high 16 bits: the bf16 pattern mapped to an unsigned
-// order, -0 folded onto +0; low 16 bits: 0xFFFF - expert, so that among equal
-// logits the lower expert index is the larger key).  K rounds of a warp-wide
-// unsigned max (one redux.sync each) pick the experts, largest first.  The
-// softmax over the K selected logits runs in fp32 in every lane and lane r
-// stores pick r: its expert index, its weight rounded to bf16, and one count
-// into a shared-memory histogram that is added to the global counts at the end.
+// Four threads per token row.  The bf16 logits become 32-bit keys that sort like
+// the values (high 16 bits: the bf16 pattern mapped to an unsigned order, -0
+// folded onto +0; low 16 bits: 0xFFFF - expert, so that among equal logits the
+// lower expert index is the larger key).  Thread j of a row streams every
+// fourth 8-expert chunk of it in 16-byte vectors and keeps its K largest keys
+// in a sorted register list: each key bubbles through the list with K unsigned
+// max/min pairs, no branches.  Two shuffle rounds (partners j ^ 1, then j ^ 2)
+// merge the four lists; every key is unique, so the merged list is the row's
+// Top-K.  The softmax over the K selected logits runs in fp32; thread 0 of the
+// row stores the K expert indices, the K weights rounded to bf16, and adds K
+// counts to a shared-memory histogram that is added to the global counts at
+// the end.  At most one block per SM walks the rows, so each global count
+// receives at most one add per SM.
 #include <cstdint>
 
 #include "ops_internal.h"
@@ -19,8 +23,9 @@
 namespace sa {
 namespace {
 
-constexpr int kRouterWarps = 32;
-constexpr int kMaxTopK = 8;
+constexpr int kRouterThreads = 1024;
+constexpr int kSplit = 4;  // threads per token row
+constexpr int kMaxChunks = 256 / 8 / kSplit;  // 16-byte chunks per thread at 256 experts
 
 __device__ __forceinline__ uint32_t order16(uint32_t bits) {
   if (bits == 0x8000u) bits = 0;  // -0 == +0
@@ -33,66 +38,87 @@ __device__ __forceinline__ float value_of(uint32_t key) {
   return __uint_as_float(bits << 16);
 }
 
-template <int kPerLane>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-router_topk_kernel(const RouterArgs a) {
+template <int K>
+__device__ __forceinline__ void offer(uint32_t (&best)[K], uint32_t key) {
+#pragma unroll
+  for (int r = 0; r < K; ++r) {  // best[] stays sorted, largest first
+    const uint32_t hi = max(best[r], key);
+    key = min(best[r], key);
+    best[r] = hi;
+  }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kRouterThreads) router_topk_kernel(const RouterArgs a) {
   __shared__ int hist[256];
   const int E = a.num_experts;
-  const int K = a.top_k;
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const long long stride = static_cast<long long>(gridDim.x) * kRouterWarps;
-  auto load_keys = [&](long long t, uint32_t (&key)[kPerLane]) {
-    const uint16_t* row = a.logits + t * E;
+  const int j = threadIdx.x % kSplit;
+  const long long rows_per_pass = static_cast<long long>(gridDim.x) * (kRouterThreads / kSplit);
+  const long long passes = (a.num_tokens + rows_per_pass - 1) / rows_per_pass;  // same for every thread
+  for (long long pass = 0; pass < passes; ++pass) {
+    const long long t = pass * rows_per_pass + static_cast<long long>(blockIdx.x) * (kRouterThreads / kSplit) +
+                        threadIdx.x / kSplit;
+    const bool live = t < a.num_tokens;  // the four threads of a row agree
+    uint32_t best[K];
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = (t < a.num_tokens && e < E) ? ((order16(__ldg(row + e)) << 16) | (0xFFFFu - e)) : 0u;
-    }
-  };
-  long long t = static_cast<long long>(blockIdx.x) * kRouterWarps + (threadIdx.x >> 5);
-  uint32_t key[kPerLane];
-  load_keys(t, key);
-  for (; t < a.num_tokens; t += stride) {
-    uint32_t next[kPerLane];
-    load_keys(t + stride, next);  // the next row's logits are in flight while this row is ranked
-    uint32_t pick[kMaxTopK];
+    for (int r = 0; r < K; ++r) best[r] = 0;  // below every real key
+    if (live) {
+      const uint16_t* row = a.logits + t * E;
+      if (a.vec16) {
+        // every load of the row is issued before any key is ranked
+        const uint4* v = reinterpret_cast<const uint4*>(row);
+        uint4 buf[kMaxChunks];
 #pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      pick[r] = 0;
-      if (r < K) {
-        uint32_t best = key[0];
+        for (int q = 0; q < kMaxChunks; ++q) {
+          const int c = j + q * kSplit;
+          buf[q] = c < E / 8 ? __ldg(v + c) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int j = 1; j < kPerLane; ++j) best = key[j] > best ? key[j] : best;
-        const uint32_t w = __reduce_max_sync(0xffffffffu, best);
-        pick[r] = w;
+        for (int q = 0; q < kMaxChunks; ++q) {
+          const int c = j + q * kSplit;
+          if (c < E / 8) {
+            const uint32_t ws[4] = {buf[q].x, buf[q].y, buf[q].z, buf[q].w};
 #pragma unroll
-        for (int j = 0; j < kPerLane; ++j) key[j] = key[j] == w ? 0u : key[j];
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t e = 8 * c + 2 * i;
+              offer<K>(best, (order16(ws[i] & 0xFFFFu) << 16) | (0xFFFFu - e));
+              offer<K>(best, (order16(ws[i] >> 16) << 16) | (0xFFFFu - e - 1));
+            }
+          }
+        }
+      } else {
+        for (int e = j; e < E; e += kSplit) offer<K>(best, (order16(__ldg(row + e)) << 16) | (0xFFFFu - e));
       }
     }
-    const float m = value_of(pick[0]);
-    float ex[kMaxTopK];
-    float sum = 0.0f;
+    // merge the four lists of the row (all 32 lanes take part in the shuffles)
 #pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      ex[r] = 0.0f;
-      if (r < K) {
-        ex[r] = expf(value_of(pick[r]) - m);
+    for (int o = 1; o < kSplit; o <<= 1) {
+      uint32_t other[K];
+#pragma unroll
+      for (int r = 0; r < K; ++r) other[r] = __shfl_xor_sync(0xffffffffu, best[r], o);
+#pragma unroll
+      for (int r = 0; r < K; ++r) offer<K>(best, other[r]);
+    }
+    if (live && j == 0) {
+      const float m = value_of(best[0]);
+      float ex[K];
+      float sum = 0.0f;
+#pragma unroll
+      for (int r = 0; r < K; ++r) {
+        ex[r] = expf(value_of(best[r]) - m);
         sum += ex[r];
       }
-    }
+      const float inv = 1.0f / sum;
 #pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      if (r < K && lane == r) {
-        const int e = static_cast<int>(0xFFFFu - (pick[r] & 0xFFFFu));
+      for (int r = 0; r < K; ++r) {
+        const int e = static_cast<int>(0xFFFFu - (best[r] & 0xFFFFu));
         a.topk_idx[t * K + r] = e;
-        a.topk_w[t * K + r] = static_cast<uint16_t>(pack_bf16x2(ex[r] / sum, 0.0f) & 0xFFFFu);
+        a.topk_w[t * K + r] = static_cast<uint16_t>(pack_bf16x2(ex[r] * inv, 0.0f) & 0xFFFFu);
         if (a.counts) atomicAdd(&hist[e], 1);
       }
     }
-#pragma unroll
-    for (int j = 0; j < kPerLane; ++j) key[j] = next[j];
   }
   if (a.counts) {
     __syncthreads();
@@ -101,25 +127,23 @@ router_topk_kernel(const RouterArgs a) {
   }
 }
 
-template <int kPerLane>
+template <int K>
 cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t stream) {
+  // At most one block per SM: every block adds its histogram to the global
+  // counts once, and same-address atomics serialise in L2, so the block count
+  // (not the token count) sets the cost of the counts.
   int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // one 1024-thread block per SM at most: few blocks keep the global count
-  // atomics (one per expert per block) off the critical path
-  const long long need = (a.num_tokens + kRouterWarps - 1) / kRouterWarps;
-  const long long cap = static_cast<long long>(sms);
-  const int blocks = static_cast<int>(need < cap ? need : cap);
-  router_topk_kernel<kPerLane><<<blocks, kRouterWarps * 32, 0, stream>>>(a);
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long need = (a.num_tokens * kSplit + kRouterThreads - 1) / kRouterThreads;
+  const int blocks = static_cast<int>(need < sms ? need : sms);
+  router_topk_kernel<K><<<blocks, kRouterThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
-  const int per_lane = (a.num_experts + 31) / 32;
-  switch (per_lane) {
+  switch (a.top_k) {
     case 1: return launch_router_t<1>(a, stream);
     case 2: return launch_router_t<2>(a, stream);
     case 3: return launch_router_t<3>(a, stream);

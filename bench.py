@@ -479,15 +479,17 @@ def bench_around_attention(args, sa, torch, device, pk):
         logits, k, topk_idx=idx, topk_weight=w, expert_counts=counts, stream=stream), reps)
     router_bytes = t * e * 2 + t * k * (4 + 2) + e * 4
 
-    def line(name, kernel, ms, nbytes, note):
+    def line(src, kernel, ms, nbytes, note):
         gbs = nbytes / (ms * 1e-3) / 1e9
         return {"workload": note, "kernel": kernel, "us": round(ms * 1e3, 2), "bytes": nbytes,
                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                             "frac": round(gbs / pk["hbm"], 4)}}
-    return {"qkv_bias_rope": line("rope", "qkv_rope_kernel", rope_ms, rope_bytes,
+                             "frac": round(gbs / pk["hbm"], 4),
+                             "traffic": recorded_traffic(kernel, (src, "ops_internal.h", "ptx.cuh")),
+                             "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}}
+    return {"qkv_bias_rope": line("rope.cu", "qkv_rope_kernel", rope_ms, rope_bytes,
                                   "32768 tokens, 64/8 heads: bias + YaRN (GPT-OSS constants) on q, k; "
                                   "q, k, v written contiguous; L2 flushed before each launch"),
-            "moe_router": line("router", "router_topk_kernel", router_ms, router_bytes,
+            "moe_router": line("router.cu", "router_topk_kernel", router_ms, router_bytes,
                                "32768 tokens x 128 bf16 logits, top 4, softmax over the selected, "
                                "expert counts; L2 flushed before each launch"),
             "gpu_launches": 2 * (reps + 3)}
@@ -513,7 +515,10 @@ def bench_linear(args, sa, torch, device, pk):
             "kernel": "linear_bias_kernel", "ms": round(ms, 4), "flops": flops,
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                          "frac": round(tf / pk["bf16"], 4),
-                         "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)"},
+                         "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)",
+                         "traffic": recorded_traffic("linear_bias_kernel", ("linear.cu", "ops_internal.h", "ptx.cuh")),
+                         "traffic_unit": "bytes per launch",
+                         "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"},
             "cublas_context": {"ms": round(ref_ms, 4), "tflops": round(flops / (ref_ms * 1e-3) / 1e12, 2),
                                "note": "torch.nn.functional.linear (cuBLAS), not on this library's path"},
             "gpu_launches": reps + 3}
@@ -638,7 +643,7 @@ def run_profile_case(case):
 
     decode:  32 sequences x 4096 tokens (256 MiB of KV, larger than L2), 64/8 heads, 4 splits.
     prefill: 1 x 8192 tokens causal, 64/8 heads.
-    linear:  [16384, 4096] x [2880, 4096]^T + bias (half the bench's output-projection rows).
+    linear:  [32768, 4096] x [2880, 4096]^T + bias (the bench's output projection, ~470 MB).
     rope:    32768 tokens, 64/8 heads, bias + YaRN.
     router:  32768 tokens x 128 experts, top 4, counts.
     """
@@ -659,9 +664,9 @@ def run_profile_case(case):
                                          dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=4)
             sa.sink_attn_merge(po, pl)
     elif case == "linear":
-        d = workloads.make_linear(61, 16384, 2880, 4096)
+        d = workloads.make_linear(61, 32768, 2880, 4096)
         x, w, b = (to_dev(d[key], torch, device) for key in ("x", "w", "bias"))
-        out = torch.empty((16384, 2880), dtype=torch.bfloat16, device=device)
+        out = torch.empty((32768, 2880), dtype=torch.bfloat16, device=device)
         for _ in range(5):
             sa.linear_bias(x, w, b, out=out)
     elif case == "rope":

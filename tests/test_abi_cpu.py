@@ -209,3 +209,13 @@ def test_linear_rejects_before_launch(lib):
     assert f(MISALIGNED, FAKE, None, 4, 64, 64, FAKE, None) == SA_ERR_ALIGNMENT
     assert f(FAKE, FAKE, ctypes.c_void_p(0x10001), 4, 64, 64, FAKE, None) == SA_ERR_ALIGNMENT
     assert f(None, None, None, 0, 64, 64, None, None) == SA_OK
+
+
+def test_library_has_no_unresolved_internal_symbols(lib):
+    """Every kernel launcher the C ABI calls is linked in (a missing definition
+    would only show when the library is loaded on the GPU machine)."""
+    import attention_softmax_sinks_gb300 as sa
+    nm = subprocess.run(["nm", "-D", "--undefined-only", sa.library_path()], capture_output=True, text=True)
+    if nm.returncode != 0:
+        pytest.skip("nm unavailable")
+    assert "_ZN2sa" not in nm.stdout

@@ -77,3 +77,20 @@ def test_router_prefill_sized_batch_sampled():
     bits = workloads.make_router_logits(24, 32768, 128, std=2.0)
     rows = np.random.default_rng(5).choice(32768, 512, replace=False)
     _check(sa, bits, 4, rows=np.sort(rows))
+
+
+def test_router_unaligned_logits_take_the_scalar_path():
+    """Logits that start 2 bytes past a 16-byte boundary (a column slice of a wider
+    tensor) are read element by element; the result is the same."""
+    sa = require_gpu()
+    bits = workloads.make_router_logits(25, 300, 129, std=2.0)
+    lg = bf16(bits)[:, 1:]                       # [300, 128] view, row stride 129
+    rows = lg.contiguous()                         # reference: aligned copy
+    idx_a, w_a = sa.moe_router_topk_softmax(rows, 4)
+    off = torch.empty(300 * 128 + 1, dtype=torch.bfloat16, device="cuda")
+    shifted = off[1:].view(300, 128)               # 2-byte offset from the allocation
+    shifted.copy_(rows)
+    idx_b, w_b = sa.moe_router_topk_softmax(shifted, 4)
+    assert torch.equal(idx_a, idx_b) and torch.equal(w_a, w_b)
+    ridx, _ = moe.router_topk_softmax(bits[:, 1:], 4)
+    assert np.array_equal(idx_b.cpu().numpy(), ridx)
