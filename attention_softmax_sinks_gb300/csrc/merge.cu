@@ -3,9 +3,10 @@
 // The split rule comes from the page "GPT-OSS on day 0", section "Kernels for
 // GPT-OSS / Sink Attention" (the sink-seeded max belongs to the first block
 // only); this is the log-sum-exp combine that undoes the split.  One warp per
-// (sequence, head): lanes read the split lse values, a shuffle max, then each
-// lane accumulates two of the 64 output dims over the splits with coalesced
-// float2 loads (256 contiguous bytes per split per warp).
+// (sequence, head): lanes read the split lse values, a shuffle max, each lane
+// turns one split's lse into its weight, and every lane accumulates two of the
+// 64 output dims over the splits with coalesced float2 loads (256 contiguous
+// bytes per split per warp), the weights broadcast by shuffle.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -44,16 +45,27 @@ __global__ void __launch_bounds__(kMergeWarps * 32) sink_merge_kernel(const Merg
   float z = 0.0f;
   float2 acc = make_float2(0.0f, 0.0f);
   if (M != kNegInf) {
+    // Lane i computes the weight of split s0 + i and hands it to the warp by
+    // shuffle, so the partial-output loads do not wait on a global load of
+    // their weight and pipeline across splits.  A split with weight 0 (lse
+    // -inf, or below a +inf one) holds o = 0 (decode writes empty splits as
+    // zeros), so it adds nothing.
     const float* o_p = a.partial_o + (static_cast<size_t>(b) * S * a.heads + h) * kHeadDim + 2 * lane;
-    for (int s = 0; s < S; ++s) {
-      const float w = split_weight(lse_p[static_cast<size_t>(s) * a.heads], M);
-      if (w != 0.0f) {
-        const float2 v = *reinterpret_cast<const float2*>(o_p + static_cast<size_t>(s) * a.heads * kHeadDim);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        z += w;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int n = min(32, S - s0);
+      const float w_mine = lane < n ? split_weight(lse_p[static_cast<size_t>(s0 + lane) * a.heads], M) : 0.0f;
+      z += w_mine;
+#pragma unroll 8
+      for (int i = 0; i < n; ++i) {
+        const float w = __shfl_sync(0xffffffffu, w_mine, i);
+        const float2 v =
+            *reinterpret_cast<const float2*>(o_p + static_cast<size_t>(s0 + i) * a.heads * kHeadDim);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
       }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
   }
   const float inv = z > 0.0f ? 1.0f / z : 0.0f;
   uint16_t* out = static_cast<uint16_t*>(a.out) + static_cast<size_t>(row) * kHeadDim + 2 * lane;
