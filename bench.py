@@ -606,6 +606,67 @@ def cpu_baseline(budget_s=12.0):
                       f"paged-decode workload, {secs:.1f} s, fp64 numpy, 1 thread"}
 
 
+def cpu_baselines_per_row(budget_s=3.0):
+    """The oracle timed beside every other measured row, on bounded samples of the same
+    workloads (single thread, fp64): prefill rows, QKV bias + YaRN tokens, router rows,
+    linear-layer rows.  Values in the unit of the row's own measurement."""
+    import oracle
+    from oracle import moe, rope
+    res = {}
+    # prefill: rows of sequence 0 of the causal-prefill workload at spread positions
+    cfg = PREFILL
+    data = workloads.make_prefill(cfg["seed"], [cfg["seqlen"]], cfg["hq"], cfg["hkv"], cfg["d"], cfg["sink_std"])
+    g = cfg["hq"] // cfg["hkv"]
+    kf = oracle.widen_bf16(data["k"][:, 0])
+    vf = oracle.widen_bf16(data["v"][:, 0])
+    rng = np.random.default_rng(9)
+    flops, t0, n = 0.0, time.perf_counter(), 0
+    while time.perf_counter() - t0 < budget_s:
+        i = int(rng.integers(0, cfg["seqlen"]))
+        h = int(rng.integers(0, g))
+        oracle.attention_with_sink(oracle.widen_bf16(data["q"][i:i + 1, h]), kf[:i + 1], vf[:i + 1],
+                                   float(data["sinks"][h]), cfg["sm_scale"])
+        flops += 4.0 * cfg["d"] * (i + 1)
+        n += 1
+    secs = time.perf_counter() - t0
+    res["prefill"] = {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                      "sample": f"{n} causal query rows of one 8192-token sequence, {secs:.1f} s"}
+    # QKV bias + YaRN: 256 tokens
+    inp = workloads.make_qkv(41, 256, cfg["hq"], cfg["hkv"])
+    inv = rope.yarn_inv_freq(64, 150000.0, 32.0, 4096, 32.0, 1.0)
+    cu = workloads.cu_seqlens_from([256])
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < budget_s / 3 or reps == 0:
+        rope.qkv_bias_rope(inp["qkv"], inp["bias"], cu, None, cfg["hq"], cfg["hkv"], 64, inv, rope.yarn_mscale(32.0))
+        reps += 1
+    secs = time.perf_counter() - t0
+    nbytes = reps * 2 * 256 * (cfg["hq"] + 2 * cfg["hkv"]) * 64 * 2
+    res["qkv_bias_rope"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": f"{reps} x 256 tokens, {secs:.1f} s"}
+    # router: 256 rows of 128 logits, top 4
+    lg = workloads.make_router_logits(42, 256, 128, std=2.0)
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < budget_s / 3 or reps == 0:
+        moe.router_topk_softmax(lg, 4)
+        reps += 1
+    secs = time.perf_counter() - t0
+    res["moe_router"] = {"value": round(reps * 256 * (128 * 2 + 4 * 6) / secs / 1e9, 6), "unit": "GB/s",
+                         "cores": 1, "kind": "oracle", "sample": f"{reps} x 256 rows, {secs:.1f} s"}
+    # linear: 64 rows of the output projection
+    d = workloads.make_linear(61, 64, 2880, 4096)
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < budget_s / 3 or reps == 0:
+        moe.linear_bias(d["x"], d["w"], d["bias"])
+        reps += 1
+    secs = time.perf_counter() - t0
+    res["linear_bias"] = {"value": round(reps * 2.0 * 64 * 2880 * 4096 / secs / 1e12, 6), "unit": "TFLOP/s",
+                          "cores": 1, "kind": "oracle", "sample": f"{reps} x 64 rows of [., 4096] x [2880, 4096]^T, {secs:.1f} s"}
+    return res
+
+
 def run_reference(args):
     cfg = DECODE
     host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * cfg["batch"], cfg["hq"], cfg["hkv"],
@@ -728,6 +789,12 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
+            per_row = cpu_baselines_per_row()
+            if "prefill" in line:
+                line["prefill"]["cpu_baseline"] = per_row["prefill"]
+            for key in ("qkv_bias_rope", "moe_router", "linear_bias"):
+                if "around_attention" in line and key in line["around_attention"]:
+                    line["around_attention"][key]["cpu_baseline"] = per_row[key]
         print(json.dumps(line), flush=True)
 
 

@@ -11,6 +11,7 @@ import torch
 
 import workloads
 from gpu_common import bf16, host, require_gpu
+from oracle import widen_bf16
 from oracle import moe
 
 pytestmark = pytest.mark.gpu
@@ -94,3 +95,43 @@ def test_router_unaligned_logits_take_the_scalar_path():
     assert torch.equal(idx_a, idx_b) and torch.equal(w_a, w_b)
     ridx, _ = moe.router_topk_softmax(bits[:, 1:], 4)
     assert np.array_equal(idx_b.cpu().numpy(), ridx)
+
+
+def test_router_with_projection_against_the_oracle_router():
+    """The whole router: bias-seeded linear layer (router projection, bf16 logits) then
+    Top-K softmax, against the oracle's composite (fp64 projection rounded to bf16).
+
+    The decision rides on bf16 logits rounded from an fp32 (GPU) or fp64 (oracle) sum,
+    which may land on different sides of a rounding boundary: the unique part is every
+    row whose K-th and (K+1)-th oracle logits differ by more than twice the bound on
+    the GPU logit error; there the experts and weights must match.  On the other rows
+    the selection must be valid: no unselected expert beats a selected one by more than
+    that bound, and the weights still form a descending softmax."""
+    sa = require_gpu()
+    t, e, hidden, k = 2048, 128, 2880, 4
+    d = workloads.make_linear(26, t, e, hidden, std=1.0, w_std=0.05, bias_std=0.5)
+    logits = sa.linear_bias(bf16(d["x"]), bf16(d["w"]), bf16(d["bias"]))
+    idx, w = sa.moe_router_topk_softmax(logits, k)
+    gidx, gw = idx.cpu().numpy(), host(w)
+    ridx, rw, rlog = moe.router(d["x"], d["w"], d["bias"], k)
+    exact = moe.linear_bias(d["x"], d["w"], d["bias"])
+    mag = np.abs(widen_bf16(d["x"])) @ np.abs(widen_bf16(d["w"])).T
+    # GPU logit error: fp32 accumulation (K 2^-23 sum|x w|) plus the bf16 rounding (2^-8 |l|)
+    eb = (hidden * 2.0 ** -23 * mag + 2.0 ** -8 * np.abs(exact)).max(axis=1)
+    srt = -np.sort(-rlog, axis=1)
+    # unique rows: the K+1 largest logits (and so the selection and its order) are
+    # separated by more than the logit error on both sides
+    unique = np.all(-np.diff(srt[:, :k + 1], axis=1) > 2 * eb[:, None], axis=1)
+    assert unique.sum() >= 256, "too few unambiguous rows to test"
+    assert np.array_equal(gidx[unique], ridx[unique])
+    # a logit error of up to eb moves a softmax weight by at most (e^(2 eb) - 1) of itself
+    tol = (np.expm1(2 * eb[unique])[:, None] + W_REL) * np.abs(rw[unique]) + 1e-12
+    assert np.all(np.abs(gw[unique] - rw[unique]) <= tol)
+    for row in np.where(~unique)[0]:
+        sel = set(gidx[row].tolist())
+        assert len(sel) == k
+        worst_sel = min(exact[row, list(sel)])
+        best_unsel = max(exact[row, [c for c in range(e) if c not in sel]])
+        assert best_unsel <= worst_sel + 2 * eb[row]
+        assert np.all(np.diff(gw[row]) <= 0) and abs(gw[row].sum() - 1.0) <= k * 2.0 ** -8
+    print(f"router end to end: {int(unique.sum())} of {t} rows unambiguous, all match")
