@@ -54,7 +54,8 @@ struct LinCfg {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 6 ? 6 : (200 * 1024) / kStageBytes;
-  static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;
+  static constexpr int kAccStride = BN <= 128 ? 128 : 256;  // TMEM columns between the two accumulators
+  static constexpr int kTmemCols = 2 * kAccStride;
   static constexpr size_t kSmem = 1024 /*alignment slack*/ + static_cast<size_t>(kStages) * kStageBytes + 256;
 };
 
@@ -173,7 +174,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
         ok = wait_or_abort(smem_u32(&sb.acc_empty[b]), (i >> 1) & 1, a.timeout_ns, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + b * BN;
+        const uint32_t d = tmem + b * C::kAccStride;
         for (int kb = 0; kb < k_steps; ++kb, ++g) {
           const int s = g % C::kStages;
           ok = wait_or_abort(smem_u32(&sb.full[s]), (g / C::kStages) & 1, a.timeout_ns, abort_flag);
@@ -199,7 +200,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
     // seed both accumulators for this CTA's first two tiles
     for (int j = 0; j < 2; ++j) {
       const int t = blockIdx.x + j * gridDim.x;
-      if (t < tiles_total) seed_bias<BN>(tmem + lane_base + j * BN, a.bias, (t % a.tiles_n) * BN, a.N);
+      if (t < tiles_total) seed_bias<BN>(tmem + lane_base + j * C::kAccStride, a.bias, (t % a.tiles_n) * BN, a.N);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -217,29 +218,34 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
       const int n0 = (t % a.tiles_n) * BN;
       const int row = m0 + 32 * q + lane;
       uint16_t* orow = a.out + static_cast<long long>(row) * a.N;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + b * BN + c, r);
-        tc_wait_ld();
-        if (row < a.M) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int n = n0 + c + 8 * v;
-            if (n < a.N) {
-              const uint4 w = make_uint4(
-                  pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
-                  pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-                  pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-                  pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
-              *reinterpret_cast<uint4*>(orow + n) = w;
-            }
-          }
+      const uint32_t acc = tmem + lane_base + b * C::kAccStride;
+      auto store8 = [&](const uint32_t* r, int n) {  // 8 fp32 accumulators -> 8 bf16 at column n
+        if (row < a.M && n < a.N) {
+          const uint4 w = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                     pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                     pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                     pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+          *reinterpret_cast<uint4*>(orow + n) = w;
         }
+      };
+#pragma unroll 1
+      for (int c = 0; c + 32 <= BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(acc + c, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int v = 0; v < 4; ++v) store8(r + 8 * v, n0 + c + 8 * v);
+      }
+      if constexpr (BN % 32 == 16) {  // last 16 columns
+        uint32_t r[16];
+        tmem_ld16(acc + BN - 16, r);
+        tc_wait_ld();
+        store8(r, n0 + BN - 16);
+        store8(r + 8, n0 + BN - 8);
       }
       // this buffer's next tile starts from its bias
       const int t2 = t + 2 * gridDim.x;
-      if (t2 < tiles_total) seed_bias<BN>(tmem + lane_base + b * BN, a.bias, (t2 % a.tiles_n) * BN, a.N);
+      if (t2 < tiles_total) seed_bias<BN>(tmem + lane_base + b * C::kAccStride, a.bias, (t2 % a.tiles_n) * BN, a.N);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -290,7 +296,7 @@ int linear_tile_n(int n) {
   // fewest estimated cycles per row block: ceil(N / BN) tiles of (BN + 32) each
   int best = 256;
   long long best_cost = -1;
-  for (int bn : {256, 192, 128}) {
+  for (int bn : {256, 240, 192, 128}) {
     const long long cost = static_cast<long long>((n + bn - 1) / bn) * (bn + 32);
     if (best_cost < 0 || cost < best_cost) {
       best = bn;
@@ -305,6 +311,7 @@ cudaError_t launch_linear(const CUtensorMap& amap, const CUtensorMap& bmap, cons
   switch (a.block_n) {
     case 128: return launch_linear_t<128>(amap, bmap, a, sms, stream);
     case 192: return launch_linear_t<192>(amap, bmap, a, sms, stream);
+    case 240: return launch_linear_t<240>(amap, bmap, a, sms, stream);
     default: return launch_linear_t<256>(amap, bmap, a, sms, stream);
   }
 }

@@ -47,7 +47,7 @@ struct LinearArgs {
   unsigned long long timeout_ns;
 };
 
-// Output tile width (128, 192 or 256) for N output features.
+// Output tile width (128, 192, 240 or 256) for N output features.
 int linear_tile_n(int n);
 // amap: x [M, K] in boxes of 128 rows x 64; bmap: W [N, K] in boxes of block_n rows x 64.
 cudaError_t launch_linear(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
