@@ -62,14 +62,14 @@ sa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return SA_OK;
 }
 
-// [rows, heads, 64] bf16 tensor read in boxes of (box_rows tokens, 1 head, 64 dims).
+// [rows, heads, 64] bf16 tensor read in boxes of (box_rows tokens, box_heads heads, 64 dims).
 sa_status map_tokens_heads(CUtensorMap* m, const void* base, long long rows, int heads,
-                           int box_rows) {
+                           int box_rows, int box_heads = 1) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   if (sa_status s = encoder(&enc)) return s;
   cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(heads) * 64 * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -382,8 +382,15 @@ static sa_status prefill_common(const void* q, const void* k, const void* v,
   a.scale_log2 = sm_scale * kLog2e;
   a.timeout_ns = g_timeout_ns;
   if (sa_status s = status_ptr(&a.status)) return s;
-  CUtensorMap qm, km, vm;
+  CUtensorMap qm, qpm, km, vm;
   if (sa_status s = map_tokens_heads(&qm, q, total_q, hq, 128)) return s;
+  // packed short sequences (group >= 4): boxes of 128 / G tokens x the G heads of a group
+  const int group = hq / hkv;
+  if (group >= 4) {
+    if (sa_status s = map_tokens_heads(&qpm, q, total_q, hq, 128 / group, group)) return s;
+  } else {
+    qpm = qm;
+  }
   if (paged) {
     if (sa_status s = map_pages(&km, k, num_pages, hkv)) return s;
     if (sa_status s = map_pages(&vm, v, num_pages, hkv)) return s;
@@ -391,7 +398,7 @@ static sa_status prefill_common(const void* q, const void* k, const void* v,
     if (sa_status s = map_tokens_heads(&km, k, total_q, hkv, 128)) return s;
     if (sa_status s = map_tokens_heads(&vm, v, total_q, hkv, 128)) return s;
   }
-  return sa::launch_prefill(qm, km, vm, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+  return sa::launch_prefill(qm, qpm, km, vm, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
 sa_status sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks,

@@ -50,7 +50,8 @@ struct PrefillArgs {
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
                           cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
-cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
+// qpmap: Q in boxes of (128 / group tokens, group heads), used for packed short sequences.
+cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace sa

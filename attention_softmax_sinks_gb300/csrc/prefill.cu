@@ -16,6 +16,13 @@
 //    grid is persistent (one CTA per SM) except when every sequence has the
 //    same length and contiguous KV: then one CTA per item, heaviest first, and
 //    the hardware's block scheduler balances.
+//  * GQA packing (persistent schedule, group G >= 4).  A sequence with at most
+//    2 * 128 / G new tokens (a decode row, a short chunk) would fill one row of
+//    each 128-row tile per head; instead it becomes one item per KV head whose
+//    two tiles hold 128 / G tokens x all G query heads of the group (row r:
+//    token r / G, head r % G), which share the K/V tiles.  Q arrives through a
+//    second tensor map with (64, G, 128 / G) boxes.  Items per pair then vary,
+//    so the CTA keeps an exclusive prefix sum of the sorted pairs' item counts.
 //  * warp 0, lane 0 -- TMA producer: Q for two query heads (two 128x64 tiles,
 //    double-buffered across items), then K and V tiles of 128 keys into a
 //    4-stage ring shared by consecutive items (128-byte swizzle; contiguous
@@ -75,7 +82,9 @@ struct __align__(1024) PrefillSmem {
   // Only the persistent schedule uses what follows; a one-item-per-CTA launch
   // allocates shared memory up to here (a smaller carve-out leaves more L1).
   alignas(1024) uint8_t q1[2][kTileBytes];  // Q of odd items [query tile]
-  unsigned long long sortkey[kMaxPairs];    // (KV tiles << 32) | (~pair): heaviest first
+  unsigned long long sortkey[kMaxPairs];    // (KV tiles << 32) | packed << 31 | (2^31 - 1 - pair)
+  int item_prefix[kMaxPairs + 1];           // items before sorted pair rank r
+  int warp_sum[kThreads / 32];
 };
 constexpr size_t kSmemOnePerCta = offsetof(PrefillSmem, q1);
 
@@ -121,6 +130,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t
 
 struct WorkItem {
   int b, h0, q0, q_start, q_len, kv_len, n_kv;
+  int kvh;     // KV head of the item
+  int packed;  // rows are (token r / G, head r % G) of a short sequence
 };
 
 struct Schedule {
@@ -156,23 +167,47 @@ __device__ __forceinline__ int block_tiles(const PrefillArgs& a, int q0, int q_l
   return (kv_end + kBlockK - 1) / kBlockK;
 }
 
-// Work item k of the schedule (k < n_pairs * n_hg).  n_kv == 0 marks an item
-// with nothing to do (only possible in the unsorted fallback order).
+// A sequence of q_len new tokens is packed (see the schedule notes) when the
+// group has at least 4 query heads and its tokens fit the two tiles of one item.
+__device__ __forceinline__ bool packs(const PrefillArgs& a, int q_len) {
+  return a.group >= 4 && q_len <= 2 * (kBlockQ / a.group);
+}
+
+__device__ __forceinline__ unsigned long long pair_key(int tiles, bool packed, int pair) {
+  return (static_cast<unsigned long long>(tiles) << 32) | (packed ? 0x80000000ull : 0ull) |
+         static_cast<unsigned long long>(0x7fffffffu - static_cast<uint32_t>(pair));
+}
+
+// Work item k of the schedule.  n_kv == 0 marks an item with nothing to do
+// (only possible in the unsorted fallback order).
 __device__ __forceinline__ WorkItem item_at(const PrefillArgs& a, const PrefillSmem& sm,
                                             const Schedule& sc, int k) {
-  const int rank = k / sc.n_hg, hg = k % sc.n_hg;
-  int b, qb;
+  int b, qb, slot;
+  bool packed = false;
   if (sm.sorted) {
-    const int pair = static_cast<int>(~static_cast<uint32_t>(sm.sortkey[rank] & 0xffffffffu));
+    // sorted pair rank: the last rank whose prefix is <= k
+    int lo = 0, hi = sm.n_pairs;  // item_prefix[lo] <= k < item_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sm.item_prefix[mid] <= k) lo = mid; else hi = mid;
+    }
+    const unsigned long long key = sm.sortkey[lo];
+    const int pair = static_cast<int>(0x7fffffffu - static_cast<uint32_t>(key & 0x7fffffffu));
+    packed = (key & 0x80000000ull) != 0;
+    slot = k - sm.item_prefix[lo];
     b = pair / sc.n_qb;
     qb = pair % sc.n_qb;
   } else {  // reverse query-block order
+    const int rank = k / sc.n_hg;
+    slot = k % sc.n_hg;
     qb = sc.n_qb - 1 - rank / a.batch;
     b = rank % a.batch;
   }
   WorkItem w;
   w.b = b;
-  w.h0 = hg * sc.tiles;
+  w.packed = packed ? 1 : 0;
+  w.kvh = packed ? slot : (slot * sc.tiles) / a.group;
+  w.h0 = packed ? slot * a.group : slot * sc.tiles;
   w.q0 = qb * kBlockQ;
   int qs, q_len, kv_len;
   const bool good = seq_lengths(a, b, qs, q_len, kv_len);
@@ -197,6 +232,7 @@ __device__ __forceinline__ int snake_item(int r, int n_items) {
 template <bool kPaged, bool kPersistent>
 __global__ void __launch_bounds__(kThreads, 1)
     sink_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap qpmap,
                         const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -220,10 +256,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = p / sc.n_qb, qb = p % sc.n_qb;
           int qs, q_len, kv_len;
           int tiles = 0;
-          if (seq_lengths(a, b, qs, q_len, kv_len)) tiles = block_tiles(a, qb * kBlockQ, q_len, kv_len);
-          else if (qb == 0 && blockIdx.x == 0) raise_status(a.status, kStatusBadLen);
-          key = tiles > 0 ? (static_cast<unsigned long long>(tiles) << 32) | (~static_cast<uint32_t>(p))
-                          : 0ull;
+          bool packed = false;
+          if (seq_lengths(a, b, qs, q_len, kv_len)) {
+            tiles = block_tiles(a, qb * kBlockQ, q_len, kv_len);
+            packed = packs(a, q_len);
+          } else if (qb == 0 && blockIdx.x == 0) {
+            raise_status(a.status, kStatusBadLen);
+          }
+          key = tiles > 0 ? pair_key(tiles, packed, p) : 0ull;
         }
         sm.sortkey[p] = key;
       }
@@ -250,6 +290,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.n_pairs = n;
         sm.sorted = 1;
       }
+      __syncthreads();
+      // exclusive prefix of the items per sorted pair (Hkv for a packed pair, n_hg
+      // otherwise): each thread sums up to ceil(n / 384) consecutive ranks, then a
+      // shuffle scan within the warp and a scan of the warp totals
+      {
+        const int n = sm.n_pairs;
+        const int per = (n + kThreads - 1) / kThreads;  // <= 3
+        const int r0 = threadIdx.x * per;
+        int part[3] = {0, 0, 0};
+        int sum = 0;
+        for (int e = 0; e < per; ++e) {
+          const int r = r0 + e;
+          const int c = r < n ? ((sm.sortkey[r] & 0x80000000ull) ? a.hkv : sc.n_hg) : 0;
+          part[e] = sum;
+          sum += c;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        if (lane == 31) sm.warp_sum[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w2 = 0; w2 < warp; ++w2) base += sm.warp_sum[w2];
+        const int excl = base + incl - sum;
+        for (int e = 0; e < per; ++e)
+          if (r0 + e < n) sm.item_prefix[r0 + e] = excl + part[e];
+        if (threadIdx.x == kThreads - 1) sm.item_prefix[n] = base + incl;
+      }
     } else if (threadIdx.x == 0) {
       // too many pairs to sort on chip: reverse query-block order (empty items skipped)
       sm.n_pairs = pairs;
@@ -261,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    n_items = sm.n_pairs * sc.n_hg;
+    n_items = sm.sorted ? sm.item_prefix[sm.n_pairs] : sm.n_pairs * sc.n_hg;
     if (static_cast<int>(blockIdx.x) >= n_items) return;  // uniform; before any barrier or TMEM use
   } else {
     // one item per CTA, reverse query-block order (heaviest first for causal blocks)
@@ -345,21 +416,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&qmap);
+        if (kPersistent) tma_prefetch_desc(&qpmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
         const uint64_t keep = l2_policy_evict_last();  // K/V are re-read by the group's other heads
         const uint64_t once = l2_policy_evict_first();
         bool ok = true;
         for_items([&](const WorkItem& w, int it, int g) {
-          const int kvh = w.h0 / a.group;
+          const int kvh = w.kvh;
           const int qb = it & 1;
           if (it >= 2 &&
               !wait_bar(smem_u32(&sm.q_empty[qb]), ((it >> 1) - 1) & 1, a.timeout_ns, abort_flag))
             return ok = false;
           const uint32_t qbar = smem_u32(&sm.q_full[qb]);
           mbar_arrive_expect_tx(qbar, ntiles * kTileBytes);
-          for (int t = 0; t < ntiles; ++t)
-            tma_load_3d(smem_u32(q_tile(sm, qb, t)), &qmap, 0, w.h0 + t, w.q_start + w.q0, qbar, once);
+          for (int t = 0; t < ntiles; ++t) {
+            if (kPersistent && w.packed)  // 128 / G tokens x the G heads of the group
+              tma_load_3d(smem_u32(q_tile(sm, qb, t)), &qpmap, 0, w.h0, w.q_start + t * (kBlockQ / a.group),
+                          qbar, once);
+            else
+              tma_load_3d(smem_u32(q_tile(sm, qb, t)), &qmap, 0, w.h0 + t, w.q_start + w.q0, qbar, once);
+          }
           sm.issued_q = it + 1;
           const int32_t* ptab = kPaged ? a.page_table + static_cast<size_t>(w.b) * a.max_pages : nullptr;
           const int seq_pages = (w.kv_len + kPageSize - 1) / kPageSize;
@@ -488,8 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t scale2 = f2(a.scale_log2, a.scale_log2);
       bool ok = true;
       for_items([&](const WorkItem& w, int it, int g) {
-        const int h = w.h0 + t;
-        const int i = w.q0 + r;           // query index within the sequence
+        // head and query index (within the sequence) of TMEM lane r
+        const int h = w.packed ? w.h0 + r % a.group : w.h0 + t;
+        const int i = w.packed ? t * (kBlockQ / a.group) + r / a.group : w.q0 + r;
         const int limit = a.causal ? min(i + w.kv_len - w.q_len, w.kv_len - 1) : w.kv_len - 1;
         const float sink = a.sinks[h] * kLog2e;
         float m = sink;                                 // running max (log2 units)
@@ -645,7 +723,7 @@ int g_prefill_sms[64] = {};
 
 }  // namespace
 
-cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
+cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t stream) {
   const int tiles = (a.group % 2 == 0) ? 2 : 1;
   const int n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
@@ -672,7 +750,7 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
                       : (persistent ? sink_prefill_kernel<false, true> : sink_prefill_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<blocks, kThreads, smem, stream>>>(qmap, kmap, vmap, a);
+  kern<<<blocks, kThreads, smem, stream>>>(qmap, qpmap, kmap, vmap, a);
   return cudaGetLastError();
 }
 
