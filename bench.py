@@ -270,10 +270,11 @@ def run_ours(args, rank, world, device):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
     # ---- causal prefill measured on its own (tensor-core bound kernel)
-    prefill = mixed = graph = around = None
+    prefill = mixed = graph = around = long_dec = None
     if not args.no_prefill:
         prefill = bench_prefill(args, sa, torch, device, pk)
         mixed = bench_mixed(args, sa, torch, device, pk)
+        long_dec = bench_long_decode(args, sa, torch, device, pk)
         graph = bench_graph_decode(args, sa, torch, device, pk)
         around = bench_around_attention(args, sa, torch, device, pk)
         around["linear_bias"] = bench_linear(args, sa, torch, device, pk)
@@ -314,6 +315,8 @@ def run_ours(args, rank, world, device):
         line["prefill"] = prefill
     if mixed is not None:
         line["mixed"] = mixed
+    if long_dec is not None:
+        line["long_decode"] = long_dec
     if graph is not None:
         line["small_batch_decode"] = graph
     if around is not None:
@@ -368,6 +371,64 @@ def bench_mixed(args, sa, torch, device, pk):
                          "tensor_frac": round(t_tc / (ms * 1e-3), 4), "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
                          "note": "frac = max(FLOPs / peak bf16, bytes / peak HBM) / time"},
             "gpu_launches": len(times)}
+
+
+def bench_long_decode(args, sa, torch, device, pk):
+    """Long-context split decode: 8 sequences x 131072 cached tokens (2 GiB of KV, far larger
+    than L2), 64/8 heads, 32 splits then the merge; events around each decode launch."""
+    cfg = workloads.WORKLOADS["long_decode"]
+    b, kvl, hq, d = cfg["batch"], cfg["kv_len"], cfg["hq"], cfg["d"]
+    host = workloads.make_decode(cfg["seed"], [kvl] * b, hq, cfg["hkv"], d, cfg["page_size"], cfg["sink_std"])
+    dv = {n: to_dev(host[n], torch, device) for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
+    del host
+    s = cfg["num_splits"]
+    po = torch.empty((b, s, hq, d), dtype=torch.float32, device=device)
+    pl = torch.empty((b, s, hq), dtype=torch.float32, device=device)
+    out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((b, hq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def decode():
+        sa.sink_attn_decode(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"], dv["kv_lens"],
+                            dv["sinks"], cfg["sm_scale"], num_splits=s, out=po, lse=pl, stream=stream)
+
+    def step():
+        decode()
+        sa.sink_attn_merge(po, pl, out=out, lse=lse, stream=stream)
+
+    for _ in range(3):
+        step()
+    reps = max(5, min(30, args.steps // 10))
+    torch.cuda.synchronize(device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        step()
+    t1.record(stream)
+    evs = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        decode()
+        e1.record(stream)
+        sa.sink_attn_merge(po, pl, out=out, lse=lse, stream=stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(device)
+    step_ms = t0.elapsed_time(t1) / reps
+    dec_ms = sum(a.elapsed_time(c) for a, c in evs) / reps
+    nbytes = decode_bytes(b, kvl, hq, cfg["hkv"], d, dv["page_table"].shape[1])
+    ach = nbytes / (dec_ms * 1e-3) / 1e9
+    del dv
+    torch.cuda.empty_cache()
+    return {"workload": "long_decode: 8 seqs x 131072 cached tokens, 64/8 heads, page 16, permuted pages, "
+                        "32 splits + merge (2 GiB of KV per step, larger than L2)",
+            "num_splits": s, "step_us": round(step_ms * 1e3, 1), "gbs": round(nbytes / (step_ms * 1e-3) / 1e9, 1),
+            "roofline": {"bound": "hbm", "kernel": "sink_decode_kernel", "achieved": round(ach, 1),
+                         "peak": pk["hbm"], "unit": "GB/s", "frac": round(ach / pk["hbm"], 4),
+                         "kernel_us": round(dec_ms * 1e3, 1),
+                         "traffic": recorded_traffic("sink_decode_kernel_long", ("decode.cu", "ptx.cuh", "internal.h")),
+                         "traffic_source": "profiles/traffic.txt (ncu capture of 2 of the 8 sequences, x4)"},
+            "gpu_launches": 2 * (2 * reps + 3)}
 
 
 def bench_graph_decode(args, sa, torch, device, pk):
@@ -703,6 +764,7 @@ def run_profile_case(case):
     """Small launches of one kernel for ncu captures: 2 warm-up launches, then 3.
 
     decode:  32 sequences x 4096 tokens (256 MiB of KV, larger than L2), 64/8 heads, 4 splits.
+    decode_long: 2 sequences x 131072 tokens (512 MiB of KV), 64/8 heads, 32 splits.
     prefill: 1 x 8192 tokens causal, 64/8 heads.
     linear:  [32768, 4096] x [2880, 4096]^T + bias (the bench's output projection, ~470 MB).
     rope:    32768 tokens, 64/8 heads, bias + YaRN.
@@ -723,6 +785,16 @@ def run_profile_case(case):
         for _ in range(5):
             po, pl = sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
                                          dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=4)
+            sa.sink_attn_merge(po, pl)
+    elif case == "decode_long":
+        cfg = workloads.WORKLOADS["long_decode"]
+        host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * 2, cfg["hq"], cfg["hkv"], cfg["d"],
+                                     cfg["page_size"], cfg["sink_std"])
+        dev = {n: to_dev(host[n], torch, device)
+               for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
+        for _ in range(5):
+            po, pl = sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
+                                         dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=cfg["num_splits"])
             sa.sink_attn_merge(po, pl)
     elif case == "linear":
         d = workloads.make_linear(61, 32768, 2880, 4096)
@@ -760,7 +832,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
-    ap.add_argument("--profile", choices=["decode", "prefill", "linear", "rope", "router"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "linear", "rope", "router"], default=None,
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:
