@@ -270,10 +270,11 @@ def run_ours(args, rank, world, device):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
 
     # ---- causal prefill measured on its own (tensor-core bound kernel)
-    prefill = mixed = graph = around = long_dec = None
+    prefill = mixed = graph = around = long_dec = tiny = None
     if not args.no_prefill:
         prefill = bench_prefill(args, sa, torch, device, pk)
         mixed = bench_mixed(args, sa, torch, device, pk)
+        tiny = bench_tiny_prefill(args, sa, torch, device, pk)
         long_dec = bench_long_decode(args, sa, torch, device, pk)
         graph = bench_graph_decode(args, sa, torch, device, pk)
         around = bench_around_attention(args, sa, torch, device, pk)
@@ -315,6 +316,8 @@ def run_ours(args, rank, world, device):
         line["prefill"] = prefill
     if mixed is not None:
         line["mixed"] = mixed
+    if tiny is not None:
+        line["tiny_prefill"] = tiny
     if long_dec is not None:
         line["long_decode"] = long_dec
     if graph is not None:
@@ -371,6 +374,56 @@ def bench_mixed(args, sa, torch, device, pk):
                          "tensor_frac": round(t_tc / (ms * 1e-3), 4), "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
                          "note": "frac = max(FLOPs / peak bf16, bytes / peak HBM) / time"},
             "gpu_launches": len(times)}
+
+
+def bench_tiny_prefill(args, sa, torch, device, pk):
+    """The small parity case (1 x 128 tokens, causal, 4 query / 1 KV head): launch latency
+    dominates, so it is reported as time per call; the roofline fraction is tiny by nature."""
+    cfg = workloads.WORKLOADS["tiny_prefill"]
+    host = workloads.make_prefill(cfg["seed"], [cfg["seqlen"]], cfg["hq"], cfg["hkv"], cfg["d"], cfg["sink_std"])
+    q, k, v, sinks, cu = (to_dev(host[n], torch, device) for n in ("q", "k", "v", "sinks", "cu_seqlens"))
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def run():
+        sa.sink_attn_prefill(q, k, v, sinks, cu, cfg["seqlen"], cfg["sm_scale"], causal=True, out=out, lse=lse,
+                             stream=stream)
+
+    for _ in range(10):
+        run()
+    reps = 200
+
+    def timed(fn, n):
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3
+
+    us = timed(run, reps) / reps
+    # the same calls captured once into a CUDA graph: device time without host enqueue gaps
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(20):
+                sa.sink_attn_prefill(q, k, v, sinks, cu, cfg["seqlen"], cfg["sm_scale"], causal=True, out=out,
+                                     lse=lse, stream=side)
+    torch.cuda.synchronize(device)
+    us_graph = timed(graph.replay, 10) / 200
+    flops = prefill_flops(1, cfg["seqlen"], cfg["hq"], cfg["d"])
+    tf = flops / (us_graph * 1e-6) / 1e12
+    return {"workload": "tiny_prefill: 1 x 128 tokens, causal, 4 query / 1 KV head, head_dim 64",
+            "us_per_call": round(us, 2), "us_per_call_graph": round(us_graph, 2), "flops": flops,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 4), "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tf / pk["bf16"], 6),
+                         "note": "latency bound (8.4 MFLOP per call); achieved from the graph replay"},
+            "gpu_launches": reps + 10 + 200}
 
 
 def bench_long_decode(args, sa, torch, device, pk):
