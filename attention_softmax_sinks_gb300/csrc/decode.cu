@@ -65,6 +65,19 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
+  const uint32_t ring_w = smem_u32(ring + warp * kStages * kSlotBytes);
+  const uint32_t full_w = smem_u32(full + warp * kStages);
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(full_w + 8 * s, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  __syncwarp();
+  // Launched with programmatic stream serialisation: the set-up above may overlap
+  // the kernel before this one; every read of an input comes after this wait.
+  pdl_wait_primary();
 
   int kv_len = a.kv_lens[b];
   const int cap = a.max_pages * kPageSize;
@@ -82,17 +95,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int my_first = p_begin + warp;
   const int my_count = my_first < p_end ? (p_end - my_first + kWarps - 1) / kWarps : 0;
 
-  const uint32_t ring_w = smem_u32(ring + warp * kStages * kSlotBytes);
-  const uint32_t full_w = smem_u32(full + warp * kStages);
   const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
-
-  if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(full_w + 8 * s, 1);
-    fence_barrier_init();
-    tma_prefetch_desc(&kmap);
-    tma_prefetch_desc(&vmap);
-  }
-  __syncwarp();
 
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int j) {  // lane 0 only
@@ -376,22 +379,22 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   auto kern = a.group <= 8 ? sink_decode_kernel<1> : sink_decode_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (!clustered) {
-    kern<<<grid, kWarps * 32, smem, stream>>>(kmap, vmap, a);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the grid may start while the previous kernel
+  // on the stream finishes; the kernel waits for it before reading any input
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = clustered ? a.cluster : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = clustered ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

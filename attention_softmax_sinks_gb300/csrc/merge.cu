@@ -27,6 +27,9 @@ __device__ __forceinline__ float split_weight(float lse_s, float M) {
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32) sink_merge_kernel(const MergeArgs a) {
+  // the next decode grid may start its set-up now (it waits for this grid
+  // before reading anything)
+  pdl_launch_dependents();
   // launched with programmatic stream serialisation: the partials come from the
   // preceding decode grid, so wait for it before reading them
   pdl_wait_primary();
