@@ -355,7 +355,7 @@ def bench_mixed(args, sa, torch, device, pk):
         run()
     times = []
     for _ in range(max(5, min(30, args.steps))):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         run()
@@ -552,6 +552,14 @@ def bench_graph_decode(args, sa, torch, device, pk):
             "gpu_launches": per_step * nseq * (2 * reps + 2)}
 
 
+def flush_l2(buf):
+    """Evict L2 before a timed launch: write a buffer larger than L2, then read it back.
+    The read pushes the written (dirty) lines out to DRAM before the timed region starts
+    and leaves only clean lines, so the timed kernel does not pay for their write-back."""
+    buf.zero_()
+    buf.sum()
+
+
 def _timed_flushed(torch, device, stream, fn, reps):
     """Mean CUDA-event time (ms) of fn over reps launches, L2 flushed before each."""
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
@@ -559,7 +567,7 @@ def _timed_flushed(torch, device, stream, fn, reps):
         fn()
     evs = []
     for _ in range(reps):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         fn()
@@ -602,10 +610,10 @@ def bench_around_attention(args, sa, torch, device, pk):
                              "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}}
     return {"qkv_bias_rope": line("rope.cu", "qkv_rope_kernel", rope_ms, rope_bytes,
                                   "32768 tokens, 64/8 heads: bias + YaRN (GPT-OSS constants) on q, k; "
-                                  "q, k, v written contiguous; L2 flushed before each launch"),
+                                  "q, k, v written contiguous; L2 flushed (written, then read back) before each launch"),
             "moe_router": line("router.cu", "router_topk_kernel", router_ms, router_bytes,
                                "32768 tokens x 128 bf16 logits, top 4, softmax over the selected, "
-                               "expert counts; L2 flushed before each launch"),
+                               "expert counts; L2 flushed (written, then read back) before each launch"),
             "gpu_launches": 2 * (reps + 3)}
 
 
@@ -625,7 +633,7 @@ def bench_linear(args, sa, torch, device, pk):
     flops = 2.0 * m * n * k
     tf = flops / (ms * 1e-3) / 1e12
     return {"workload": "output projection of 32768 tokens: [32768, 4096] x [2880, 4096]^T + bias, bf16, "
-                        "fp32 accumulator seeded with the bias; L2 flushed before each launch",
+                        "fp32 accumulator seeded with the bias; L2 flushed (written, then read back) before each launch",
             "kernel": "linear_bias_kernel", "ms": round(ms, 4), "flops": flops,
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                          "frac": round(tf / pk["bf16"], 4),
@@ -660,7 +668,7 @@ def bench_prefill(args, sa, torch, device, pk):
     steps = max(5, min(50, args.steps))
     times = []
     for _ in range(steps):
-        flush.zero_()  # evict the previous launch's K/V from L2
+        flush_l2(flush)  # evict the previous launch's K/V from L2
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         run()
@@ -673,7 +681,7 @@ def bench_prefill(args, sa, torch, device, pk):
     return {"workload": "causal_prefill: 4 x 8192 tokens, causal, 64 query / 8 KV heads, head_dim 64, "
                         "sinks N(0, 2), out + fp32 lse",
             "value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(avg, 4),
-            "flops": flops, "l2": "flushed (256 MiB write) before every launch",
+            "flops": flops, "l2": "flushed (256 MiB write, then read back) before every launch",
             "roofline": {"bound": "tensor", "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2),
                          "peak": pk["bf16"], "unit": "TFLOP/s", "frac": round(tflops / pk["bf16"], 4),
                          "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)",
