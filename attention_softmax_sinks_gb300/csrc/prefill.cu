@@ -23,11 +23,11 @@
 //    token r / G, head r % G), which share the K/V tiles.  Q arrives through a
 //    second tensor map with (64, G, 128 / G) boxes.  Items per pair then vary,
 //    so the CTA keeps an exclusive prefix sum of the sorted pairs' item counts.
-//  * warp 0, lane 0 -- TMA producer: Q for two query heads (two 128x64 tiles,
+//  * warp 0 -- TMA producer: Q for two query heads (two 128x64 tiles,
 //    double-buffered across items), then K and V tiles of 128 keys into a
 //    4-stage ring shared by consecutive items (128-byte swizzle; contiguous
-//    tensors by one 3-D box, paged caches by eight 16-row page boxes through
-//    the page table).
+//    tensors by one 3-D box from lane 0, paged caches by eight 16-row page
+//    boxes through the page table, one page per lane).
 //  * warps 1 and 2, lane 0 -- one tcgen05 issuer per query tile t:
 //    S_t = Q_t K^T (M=128, N=128, K=64) into TMEM and O_t += P_t V with P_t
 //    read from TMEM (M=128, N=64, K=128); completion through tcgen05.commit.
@@ -414,20 +414,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<120>();
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer
+      // The whole warp walks the items in step; lane 0 waits on barriers (and
+      // shares the outcome), arms them and loads Q.  A paged K/V tile is eight
+      // 16-row page boxes: lane i < 8 holds the page id of box i (one coalesced
+      // load, a tile ahead) and issues that page's K and V copies.
       if (lane == 0) {
         tma_prefetch_desc(&qmap);
         if (kPersistent) tma_prefetch_desc(&qpmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
-        const uint64_t keep = l2_policy_evict_last();  // K/V are re-read by the group's other heads
-        const uint64_t once = l2_policy_evict_first();
-        bool ok = true;
-        for_items([&](const WorkItem& w, int it, int g) {
-          const int kvh = w.kvh;
-          const int qb = it & 1;
-          if (it >= 2 &&
-              !wait_bar(smem_u32(&sm.q_empty[qb]), ((it >> 1) - 1) & 1, a.timeout_ns, abort_flag))
-            return ok = false;
+      }
+      const uint64_t keep = l2_policy_evict_last();  // K/V are re-read by the group's other heads
+      const uint64_t once = l2_policy_evict_first();
+      auto warp_wait = [&](uint32_t bar, uint32_t parity) {
+        int r = 1;
+        if (lane == 0) r = wait_bar(bar, parity, a.timeout_ns, abort_flag) ? 1 : 0;
+        return __shfl_sync(0xffffffffu, r, 0) != 0;
+      };
+      bool ok = true;
+      for_items([&](const WorkItem& w, int it, int g) {
+        const int kvh = w.kvh;
+        const int qb = it & 1;
+        if (it >= 2 && !warp_wait(smem_u32(&sm.q_empty[qb]), ((it >> 1) - 1) & 1)) return ok = false;
+        if (lane == 0) {
           const uint32_t qbar = smem_u32(&sm.q_full[qb]);
           mbar_arrive_expect_tx(qbar, ntiles * kTileBytes);
           for (int t = 0; t < ntiles; ++t) {
@@ -438,55 +447,48 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(smem_u32(q_tile(sm, qb, t)), &qmap, 0, w.h0 + t, w.q_start + w.q0, qbar, once);
           }
           sm.issued_q = it + 1;
-          const int32_t* ptab = kPaged ? a.page_table + static_cast<size_t>(w.b) * a.max_pages : nullptr;
-          const int seq_pages = (w.kv_len + kPageSize - 1) / kPageSize;
-          constexpr int kPagesPerTile = kBlockK / kPageSize;
-          // page ids of tile j are loaded while tile j-1's boxes are issued
-          int ids[kPagesPerTile];
-          auto load_ids = [&](int j, int (&dst)[kPagesPerTile]) {
-#pragma unroll
-            for (int i = 0; i < kPagesPerTile; ++i) {
-              const int lp = min(j * kPagesPerTile + i, seq_pages - 1);  // ragged tail: any valid page
-              dst[i] = ptab[lp];
-            }
-          };
-          if constexpr (kPaged) load_ids(0, ids);
-          for (int j = 0; j < w.n_kv; ++j) {
-            const int gg = g + j, st = gg % kStages;
-            int next[kPagesPerTile];
-            if constexpr (kPaged) {
-              if (j + 1 < w.n_kv) load_ids(j + 1, next);
-            }
-            if (gg >= kStages &&
-                !wait_bar(smem_u32(&sm.kv_empty[st]), ((gg / kStages) - 1) & 1, a.timeout_ns, abort_flag))
-              return ok = false;
-            const uint32_t bar = smem_u32(&sm.kv_full[st]);
-            mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-            if constexpr (kPaged) {
-#pragma unroll
-              for (int i = 0; i < kPagesPerTile; ++i) {
-                int phys = ids[i];
-                if (phys < 0 || phys >= a.num_pages) {
-                  raise_status(a.status, kStatusBadPage);
-                  phys = 0;
-                }
-                const int row = (phys * a.hkv + kvh) * kPageSize;
-                tma_load_2d(smem_u32(sm.k[st]) + i * kPageSize * 128, &kmap, 0, row, bar, keep);
-                tma_load_2d(smem_u32(sm.v[st]) + i * kPageSize * 128, &vmap, 0, row, bar, keep);
-              }
-              if (j + 1 < w.n_kv)
-#pragma unroll
-                for (int i = 0; i < kPagesPerTile; ++i) ids[i] = next[i];
-            } else {
-              tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
-              tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
-            }
-            sm.issued_kv = gg + 1;
+        }
+        const int32_t* ptab = kPaged ? a.page_table + static_cast<size_t>(w.b) * a.max_pages : nullptr;
+        const int seq_pages = (w.kv_len + kPageSize - 1) / kPageSize;
+        constexpr int kPagesPerTile = kBlockK / kPageSize;
+        auto load_id = [&](int j) {  // page id of box `lane` of tile j (lanes < 8)
+          if (lane >= kPagesPerTile) return 0;
+          const int lp = min(j * kPagesPerTile + lane, seq_pages - 1);  // ragged tail: any valid page
+          return ptab[lp];
+        };
+        int id = 0;
+        if constexpr (kPaged) id = load_id(0);
+        for (int j = 0; j < w.n_kv; ++j) {
+          const int gg = g + j, st = gg % kStages;
+          int next = 0;
+          if constexpr (kPaged) {
+            if (j + 1 < w.n_kv) next = load_id(j + 1);  // in flight while tile j is issued
           }
-          return true;
-        });
-        if (!ok) raise_status(a.status, kStatusTimeout);
-      }
+          if (gg >= kStages && !warp_wait(smem_u32(&sm.kv_empty[st]), ((gg / kStages) - 1) & 1))
+            return ok = false;
+          const uint32_t bar = smem_u32(&sm.kv_full[st]);
+          if (lane == 0) mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+          if constexpr (kPaged) {
+            if (lane < kPagesPerTile) {
+              int phys = id;
+              if (phys < 0 || phys >= a.num_pages) {
+                raise_status(a.status, kStatusBadPage);
+                phys = 0;
+              }
+              const int row = (phys * a.hkv + kvh) * kPageSize;
+              tma_load_2d(smem_u32(sm.k[st]) + lane * kPageSize * 128, &kmap, 0, row, bar, keep);
+              tma_load_2d(smem_u32(sm.v[st]) + lane * kPageSize * 128, &vmap, 0, row, bar, keep);
+            }
+            id = next;
+          } else if (lane == 0) {
+            tma_load_3d(smem_u32(sm.k[st]), &kmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
+            tma_load_3d(smem_u32(sm.v[st]), &vmap, 0, kvh, w.q_start + j * kBlockK, bar, keep);
+          }
+          if (lane == 0) sm.issued_kv = gg + 1;
+        }
+        return true;
+      });
+      if (!ok && lane == 0) raise_status(a.status, kStatusTimeout);
     } else if (warp == 1 || warp == 2) {
       // ---------------------------------------------------------- MMA issuers
       // Warp 1 issues query tile 0's MMAs, warp 2 tile 1's: the two tiles run

@@ -827,6 +827,7 @@ def run_profile_case(case):
     decode:  32 sequences x 4096 tokens (256 MiB of KV, larger than L2), 64/8 heads, 4 splits.
     decode_long: 2 sequences x 131072 tokens (512 MiB of KV), 64/8 heads, 32 splits.
     prefill: 1 x 8192 tokens causal, 64/8 heads.
+    prefill_persistent: 8192 + 8191 tokens causal (the persistent schedule), 64/8 heads.
     linear:  [32768, 4096] x [2880, 4096]^T + bias (the bench's output projection, ~470 MB).
     rope:    32768 tokens, 64/8 heads, bias + YaRN.
     router:  32768 tokens x 128 experts, top 4, counts.
@@ -857,6 +858,13 @@ def run_profile_case(case):
             po, pl = sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
                                          dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=cfg["num_splits"])
             sa.sink_attn_merge(po, pl)
+    elif case == "prefill_persistent":
+        cfg = PREFILL
+        lens = [cfg["seqlen"], cfg["seqlen"] - 1]  # not uniform: the persistent schedule
+        host = workloads.make_prefill(cfg["seed"], lens, cfg["hq"], cfg["hkv"], cfg["d"], cfg["sink_std"])
+        q, k, v, sinks, cu = (to_dev(host[n], torch, device) for n in ("q", "k", "v", "sinks", "cu_seqlens"))
+        for _ in range(5):
+            sa.sink_attn_prefill(q, k, v, sinks, cu, cfg["seqlen"], cfg["sm_scale"], causal=True)
     elif case == "linear":
         d = workloads.make_linear(61, 32768, 2880, 4096)
         x, w, b = (to_dev(d[key], torch, device) for key in ("x", "w", "bias"))
@@ -893,7 +901,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
-    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "linear", "rope", "router"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_persistent", "linear", "rope",
+                                          "router"], default=None,
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:
