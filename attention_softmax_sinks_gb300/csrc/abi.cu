@@ -434,8 +434,6 @@ sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int
   if (!aligned16(x) || !aligned16(w) || !aligned16(out) ||
       (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)))
     return SA_ERR_ALIGNMENT;
-  unsigned* status = nullptr;
-  if (sa_status s = status_ptr(&status)) return s;
   sa::LinearArgs a{};
   a.bias = static_cast<const uint16_t*>(bias);
   a.out = static_cast<uint16_t*>(out);
@@ -445,6 +443,9 @@ sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int
   a.block_n = sa::linear_tile_n(n);
   a.tiles_m = (m + 127) / 128;
   a.tiles_n = (n + a.block_n - 1) / a.block_n;
+  if (static_cast<long long>(a.tiles_m) * a.tiles_n >= (1LL << 31)) return SA_ERR_SHAPE;
+  unsigned* status = nullptr;
+  if (sa_status s = status_ptr(&status)) return s;
   a.status = status;
   a.timeout_ns = g_timeout_ns;
   CUtensorMap am, bm;

@@ -219,3 +219,8 @@ def test_library_has_no_unresolved_internal_symbols(lib):
     if nm.returncode != 0:
         pytest.skip("nm unavailable")
     assert "_ZN2sa" not in nm.stdout
+
+
+def test_linear_rejects_tile_count_overflow(lib):
+    # 2^31 - 1 rows x 2^30 features: more output tiles than an int holds
+    assert lib.linear_bias(FAKE, FAKE, None, 2**31 - 1, 2**30, 64, FAKE, None) == SA_ERR_SHAPE
