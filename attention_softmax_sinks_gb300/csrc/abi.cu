@@ -427,7 +427,7 @@ sa_status sink_attn_prefill_paged(const void* q, const void* paged_k, const void
 
 sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int n, int k,
                       void* out, cudaStream_t stream) {
-  if (m < 0 || n <= 0 || k <= 0) return SA_ERR_SHAPE;
+  if (m < 0 || n <= 0 || k <= 0 || n > (1 << 30) || k > (1 << 30)) return SA_ERR_SHAPE;
   if (n % 8 != 0 || k % 8 != 0) return SA_ERR_UNSUPPORTED;
   if (m == 0) return SA_OK;
   if (!x || !w || !out) return SA_ERR_NULL;
@@ -441,9 +441,11 @@ sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int
   a.N = n;
   a.K = k;
   a.block_n = sa::linear_tile_n(n);
-  a.tiles_m = (m + 127) / 128;
-  a.tiles_n = (n + a.block_n - 1) / a.block_n;
-  if (static_cast<long long>(a.tiles_m) * a.tiles_n >= (1LL << 31)) return SA_ERR_SHAPE;
+  const long long tiles_m = (static_cast<long long>(m) + 127) / 128;
+  const long long tiles_n = (static_cast<long long>(n) + a.block_n - 1) / a.block_n;
+  if (tiles_m * tiles_n >= (1LL << 31)) return SA_ERR_SHAPE;
+  a.tiles_m = static_cast<int>(tiles_m);
+  a.tiles_n = static_cast<int>(tiles_n);
   unsigned* status = nullptr;
   if (sa_status s = status_ptr(&status)) return s;
   a.status = status;
