@@ -22,7 +22,8 @@
  *  any m >= 0.  x, w, out 16-byte aligned.
  *
  * Conventions of sink_attn.h apply (device pointers, asynchronous on
- * `stream`, no allocation).  Status: SA_ERR_SHAPE (m < 0, n or k <= 0),
+ * `stream`, no allocation).  Status: SA_ERR_SHAPE (m < 0, n or k <= 0 or > 2^30,
+ * more than 2^31 - 1 output tiles),
  * SA_ERR_UNSUPPORTED (n or k not a multiple of 8), SA_ERR_NULL,
  * SA_ERR_ALIGNMENT, SA_ERR_CUDA / SA_ERR_LAUNCH; m == 0 launches nothing.
  * A device wait that runs out of time (sink_attn_set_wait_timeout_ns) stops
