@@ -32,6 +32,9 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kLinThreads = 256;
 constexpr int kEpiWarp0 = 4;
+// Drains (MMAs before TMEM is freed, copies before shared memory is released)
+// always wait up to this long, even when the caller set a shorter wait budget.
+constexpr unsigned long long kDrainTimeoutNs = 2000000000ull;
 
 __device__ __forceinline__ uint64_t sw128_kmajor(uint32_t saddr) {
   uint64_t d = 0;
@@ -192,7 +195,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
       if (!ok) raise_status(a.status, kStatusTimeout);
       // every MMA issued by this thread has finished before TMEM is released
       tc_commit(smem_u32(&sb.drain));
-      if (!mbar_wait(smem_u32(&sb.drain), 0, a.timeout_ns)) raise_status(a.status, kStatusTimeout);
+      if (!mbar_wait(smem_u32(&sb.drain), 0, kDrainTimeoutNs)) raise_status(a.status, kStatusTimeout);
     }
   } else if (warp >= kEpiWarp0) {
     const int q = warp - kEpiWarp0;                    // TMEM lane quarter
@@ -260,7 +263,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
     const int issued = sb.issued;
     for (int s = 0; s < C::kStages && s < issued; ++s) {
       const int last = issued - 1 - ((issued - 1 - s) % C::kStages);
-      if (!mbar_wait(smem_u32(&sb.full[s]), (last / C::kStages) & 1, a.timeout_ns))
+      if (!mbar_wait(smem_u32(&sb.full[s]), (last / C::kStages) & 1, kDrainTimeoutNs))
         raise_status(a.status, kStatusTimeout);
     }
   }

@@ -100,3 +100,26 @@ def test_zero_wait_budget_unwinds_cleanly():
     ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"], 0.125, True)
     assert_close(host(o), host(l), ro, rl, "prefill after zero budget")
     _decode_ok(sa)
+
+
+def test_zero_wait_budget_linear_unwinds_cleanly():
+    """The linear layer's waits give up at once under a zero budget; its drains (MMAs
+    before TMEM is freed, copies before shared memory is released) still wait, so the
+    kernel ends cleanly and the next call with the normal budget is correct."""
+    from oracle import moe
+    sa = require_gpu()
+    sa.sink_attn_device_status(True)
+    d = workloads.make_linear(81, 1024, 2880, 1024)
+    x, w, b = bf16(d["x"]), bf16(d["w"]), bf16(d["bias"])
+    try:
+        sa.sink_attn_set_wait_timeout_ns(0)
+        sa.linear_bias(x, w, b)
+        assert sa.sink_attn_device_status(True) in (SA_OK, SA_ERR_TIMEOUT)
+    finally:
+        sa.sink_attn_set_wait_timeout_ns(2_000_000_000)
+    out = sa.linear_bias(x, w, b)
+    rows = [0, 1, 511, 1023]
+    ref = moe.linear_bias(d["x"][rows], d["w"], d["bias"])
+    got = host(out)[rows]
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-2)
+    assert sa.sink_attn_device_status(True) == SA_OK
