@@ -22,7 +22,8 @@ __all__ = [
     "sink_attn_decode", "sink_attn_merge", "sink_attn_decode_splits", "sink_attn_device_status",
     "sink_attn_set_wait_timeout_ns", "sink_attn_status_string", "sink_attn_abi_version",
     "sink_attn_selftest_wait_timeout", "sink_attn_decode_noalloc", "moe_router_topk_softmax",
-    "qkv_bias_rope", "qkv_bias_rope_append_paged", "linear_bias", "GPT_OSS_YARN", "EXPORTED_SYMBOLS",
+    "qkv_bias_rope", "qkv_bias_rope_append_paged", "linear_bias", "moe_router", "GPT_OSS_YARN",
+    "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "sink_attn_decode_splits", "sink_attn_device_status", "sink_attn_set_wait_timeout_ns",
     "sink_attn_status_string", "sink_attn_abi_version", "sink_attn_selftest_wait_timeout",
     "sink_attn_decode_noalloc", "moe_router_topk_softmax", "qkv_bias_rope",
-    "qkv_bias_rope_append_paged", "linear_bias",
+    "qkv_bias_rope_append_paged", "linear_bias", "moe_router",
 )
 
 _p, _i, _f, _d, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_longlong
@@ -54,6 +55,7 @@ _SIGNATURES = {
                                       _p]),
     "moe_router_topk_softmax": (_i, [_p, _ll, _i, _i, _p, _p, _p, _p]),
     "linear_bias": (_i, [_p, _p, _p, _i, _i, _i, _p, _p]),
+    "moe_router": (_i, [_p, _p, _p, _i, _i, _i, _i, _p, _p, _p, _p]),
     "qkv_bias_rope": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p, _p, _p]),
     "qkv_bias_rope_append_paged": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p,
                                         _p, _p, _i, _i, _i, _p]),
@@ -374,3 +376,32 @@ def linear_bias(x, w, bias=None, out=None, stream=None):
     _check(load_library().linear_bias(_ptr(x), _ptr(w), _ptr(bias), m, n, k, _ptr(out), _stream(stream)),
            "linear_bias")
     return out
+
+
+def moe_router(x, w_router, bias, top_k: int, topk_idx=None, topk_weight=None, expert_counts=None,
+               return_counts: bool = False, stream=None):
+    """Router projection + bias + bf16 logits + Top-K softmax in one tcgen05 kernel:
+    x [T, hidden] bf16, w_router [E, hidden] bf16, bias [E] bf16 or None.  Returns
+    (idx int32 [T, k], weight bf16 [T, k]) and the int32 [E] counts when asked."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(w_router, "w_router", torch.bfloat16)
+    if bias is not None:
+        _dev(bias, "bias", torch.bfloat16)
+    t, hidden = x.shape
+    e = w_router.shape[0]
+    if w_router.shape[1] != hidden:
+        raise ValueError(f"w_router is {tuple(w_router.shape)}, expected [E, {hidden}]")
+    k = int(top_k)
+    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=x.device) if topk_idx is None
+                else _dev(topk_idx, "topk_idx", torch.int32))
+    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=x.device) if topk_weight is None
+                   else _dev(topk_weight, "topk_weight", torch.bfloat16))
+    if expert_counts is None and return_counts:
+        expert_counts = torch.empty((e,), dtype=torch.int32, device=x.device)
+    elif expert_counts is not None:
+        _dev(expert_counts, "expert_counts", torch.int32)
+    _check(load_library().moe_router(_ptr(x), _ptr(w_router), _ptr(bias), t, hidden, e, k, _ptr(topk_idx),
+                                     _ptr(topk_weight), _ptr(expert_counts), _stream(stream)), "moe_router")
+    if expert_counts is not None:
+        return topk_idx, topk_weight, expert_counts
+    return topk_idx, topk_weight

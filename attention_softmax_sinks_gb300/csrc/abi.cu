@@ -456,6 +456,43 @@ sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int
   return sa::launch_linear(am, bm, a, sm_count(), stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
+sa_status moe_router(const void* x, const void* w_router, const void* bias, int num_tokens,
+                     int hidden, int num_experts, int top_k, int32_t* topk_idx, void* topk_weight,
+                     int32_t* expert_counts, cudaStream_t stream) {
+  if (num_tokens < 0 || hidden <= 0 || hidden > (1 << 30)) return SA_ERR_SHAPE;
+  if (num_experts < 1 || num_experts > 256) return SA_ERR_SHAPE;
+  if (top_k < 1 || top_k > 8 || top_k > num_experts) return SA_ERR_SHAPE;
+  if (hidden % 8 != 0) return SA_ERR_UNSUPPORTED;
+  if (num_tokens > 0 && (!x || !w_router || !topk_idx || !topk_weight)) return SA_ERR_NULL;
+  if (num_tokens > 0 && (!aligned16(x) || !aligned16(w_router) ||
+                         (bias && (reinterpret_cast<uintptr_t>(bias) & 1u))))
+    return SA_ERR_ALIGNMENT;
+  if (expert_counts &&
+      cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * num_experts, stream) != cudaSuccess)
+    return SA_ERR_CUDA;
+  if (num_tokens == 0) return SA_OK;
+  unsigned* status = nullptr;
+  if (sa_status s = status_ptr(&status)) return s;
+  sa::LinearArgs a{};
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.M = num_tokens;
+  a.N = num_experts;
+  a.K = hidden;
+  a.block_n = num_experts <= 32 ? 32 : num_experts <= 64 ? 64 : num_experts <= 128 ? 128 : 256;
+  a.tiles_m = (num_tokens + 127) / 128;
+  a.tiles_n = 1;
+  a.status = status;
+  a.timeout_ns = g_timeout_ns;
+  a.topk_idx = topk_idx;
+  a.topk_w = static_cast<uint16_t*>(topk_weight);
+  a.counts = expert_counts;
+  a.top_k = top_k;
+  CUtensorMap am, bm;
+  if (sa_status s = map_matrix(&am, x, num_tokens, hidden, 128)) return s;
+  if (sa_status s = map_matrix(&bm, w_router, num_experts, hidden, a.block_n)) return s;
+  return sa::launch_linear_router(am, bm, a, sm_count(), stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
 sa_status moe_router_topk_softmax(const void* logits, long long num_tokens, int num_experts,
                                   int top_k, int32_t* topk_idx, void* topk_weight,
                                   int32_t* expert_counts, cudaStream_t stream) {

@@ -20,6 +20,16 @@
 // Two TMEM accumulators alternate, so the epilogue of tile i overlaps the
 // MMAs of tile i + 1.  Tiles are numbered with the N index fastest: the CTAs
 // working at the same time share one 128-row block of x through L2.
+//
+// Router form (kRouter): the MoE router projection (N = experts <= 256, one
+// column tile) whose epilogue takes the page's Top-K-then-softmax router
+// instead of storing logits: the thread that owns a token row rounds each
+// logit to bf16, ranks it in a sorted register list of eight packed keys
+// (bf16 order in the high half, 0xFFFF - expert in the low half, so equal
+// logits keep the lower expert first), and writes the K selected experts,
+// their softmax weights (fp32, stored as bf16) and per-expert counts (shared
+// histogram, added to the global counts once per CTA).  The arithmetic is that
+// of the plain layer followed by the standalone router, bit for bit.
 #include <cstdint>
 
 #include "ops_internal.h"
@@ -59,7 +69,7 @@ struct LinCfg {
   static constexpr int kStages = (200 * 1024) / kStageBytes > 6 ? 6 : (200 * 1024) / kStageBytes;
   static constexpr int kAccStride = BN <= 128 ? 128 : 256;  // TMEM columns between the two accumulators
   static constexpr int kTmemCols = 2 * kAccStride;
-  static constexpr size_t kSmem = 1024 /*alignment slack*/ + static_cast<size_t>(kStages) * kStageBytes + 256;
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + static_cast<size_t>(kStages) * kStageBytes + 2048;
 };
 
 struct LinBarriers {
@@ -67,6 +77,7 @@ struct LinBarriers {
   uint32_t tmem_base;
   int abort_flag;
   int issued;
+  int hist[256];  // router form: expert counts of this CTA
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
@@ -82,6 +93,28 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
       *abort_flag = 1;
       return false;
     }
+  }
+}
+
+__device__ __forceinline__ uint32_t order16(uint32_t bits) {  // bf16 bits -> unsigned order
+  if (bits == 0x8000u) bits = 0;                               // -0 == +0
+  return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  const uint32_t o = key >> 16;
+  const uint32_t bits = (o & 0x8000u) ? (o & 0x7FFFu) : (~o & 0xFFFFu);
+  return __uint_as_float(bits << 16);
+}
+
+constexpr int kRouterSlots = 8;  // largest supported top_k
+
+__device__ __forceinline__ void offer(uint32_t (&best)[kRouterSlots], uint32_t key) {
+#pragma unroll
+  for (int r = 0; r < kRouterSlots; ++r) {  // best[] stays sorted, largest first
+    const uint32_t hi = max(best[r], key);
+    key = min(best[r], key);
+    best[r] = hi;
   }
 }
 
@@ -102,7 +135,7 @@ __device__ __forceinline__ void seed_bias(uint32_t taddr, const uint16_t* bias, 
   }
 }
 
-template <int BN>
+template <int BN, bool kRouter>
 __global__ void __launch_bounds__(kLinThreads, 1)
 linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                    const LinearArgs a) {
@@ -131,6 +164,8 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
     sb.issued = 0;
     fence_barrier_init();
   }
+  if constexpr (kRouter)
+    for (int e = threadIdx.x; e < 256; e += kLinThreads) sb.hist[e] = 0;
   if (warp == 1) {
     tmem_alloc(smem_u32(&sb.tmem_base), C::kTmemCols);
     tmem_relinquish();
@@ -222,6 +257,51 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
       const int row = m0 + 32 * q + lane;
       uint16_t* orow = a.out + static_cast<long long>(row) * a.N;
       const uint32_t acc = tmem + lane_base + b * C::kAccStride;
+      if constexpr (kRouter) {
+        // logits of token `row`: bf16-rounded, ranked into the eight largest keys
+        uint32_t best[kRouterSlots];
+#pragma unroll
+        for (int r = 0; r < kRouterSlots; ++r) best[r] = 0;  // below every real key
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r32[32];
+          tmem_ld32(acc + c, r32);
+          tc_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 32; ++v) {
+            const int e = c + v;
+            if (e < a.N) {
+              const uint32_t bits = pack_bf16x2(__uint_as_float(r32[v]), 0.0f) & 0xFFFFu;
+              offer(best, (order16(bits) << 16) | (0xFFFFu - static_cast<uint32_t>(e)));
+            }
+          }
+        }
+        if (row < a.M) {
+          const int K = a.top_k;
+          const float mx = key_value(best[0]);
+          float ex[kRouterSlots];
+          float sum = 0.0f;
+#pragma unroll
+          for (int r = 0; r < kRouterSlots; ++r) {
+            ex[r] = 0.0f;
+            if (r < K) {
+              ex[r] = expf(key_value(best[r]) - mx);
+              sum += ex[r];
+            }
+          }
+          const float inv = 1.0f / sum;
+#pragma unroll
+          for (int r = 0; r < kRouterSlots; ++r) {
+            if (r < K) {
+              const int e = static_cast<int>(0xFFFFu - (best[r] & 0xFFFFu));
+              a.topk_idx[static_cast<long long>(row) * K + r] = e;
+              a.topk_w[static_cast<long long>(row) * K + r] =
+                  static_cast<uint16_t>(pack_bf16x2(ex[r] * inv, 0.0f) & 0xFFFFu);
+              if (a.counts) atomicAdd(&sb.hist[e], 1);
+            }
+          }
+        }
+      } else {
       auto store8 = [&](const uint32_t* r, int n) {  // 8 fp32 accumulators -> 8 bf16 at column n
         if (row < a.M && n < a.N) {
           const uint4 w = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
@@ -246,6 +326,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
         store8(r, n0 + BN - 16);
         store8(r + 8, n0 + BN - 8);
       }
+      }
       // this buffer's next tile starts from its bias
       const int t2 = t + 2 * gridDim.x;
       if (t2 < tiles_total) seed_bias<BN>(tmem + lane_base + b * C::kAccStride, a.bias, (t2 % a.tiles_n) * BN, a.N);
@@ -268,13 +349,18 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
     }
   }
   __syncthreads();
+  if constexpr (kRouter) {
+    if (a.counts)
+      for (int e = threadIdx.x; e < a.N; e += kLinThreads)
+        if (sb.hist[e]) atomicAdd(a.counts + e, sb.hist[e]);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-template <int BN>
+template <int BN, bool kRouter = false>
 cudaError_t launch_linear_t(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
                             int sms, cudaStream_t stream) {
   using C = LinCfg<BN>;
@@ -282,18 +368,28 @@ cudaError_t launch_linear_t(const CUtensorMap& amap, const CUtensorMap& bmap, co
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_bias_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::kSmem));
+    cudaError_t e = cudaFuncSetAttribute(linear_bias_kernel<BN, kRouter>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int tiles = a.tiles_m * a.tiles_n;
   const int grid = tiles < sms ? tiles : sms;
-  linear_bias_kernel<BN><<<grid, kLinThreads, C::kSmem, stream>>>(amap, bmap, a);
+  linear_bias_kernel<BN, kRouter><<<grid, kLinThreads, C::kSmem, stream>>>(amap, bmap, a);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_linear_router(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
+                                 int sms, cudaStream_t stream) {
+  switch (a.block_n) {
+    case 32: return launch_linear_t<32, true>(amap, bmap, a, sms, stream);
+    case 64: return launch_linear_t<64, true>(amap, bmap, a, sms, stream);
+    case 128: return launch_linear_t<128, true>(amap, bmap, a, sms, stream);
+    default: return launch_linear_t<256, true>(amap, bmap, a, sms, stream);
+  }
+}
 
 int linear_tile_n(int n) {
   // fewest estimated cycles per row block: ceil(N / BN) tiles of (BN + 32) each

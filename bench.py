@@ -600,6 +600,17 @@ def bench_around_attention(args, sa, torch, device, pk):
     router_ms = _timed_flushed(torch, device, stream, lambda: sa.moe_router_topk_softmax(
         logits, k, topk_idx=idx, topk_weight=w, expert_counts=counts, stream=stream), reps)
     router_bytes = t * e * 2 + t * k * (4 + 2) + e * 4
+    # the whole router: projection of 2880-wide hidden states + bias, then Top-K softmax,
+    # fused into one kernel and as the two-kernel path
+    rd = workloads.make_linear(43, t, e, 2880, std=1.0, w_std=0.05, bias_std=0.5)
+    hx, rw, rb = (to_dev(rd[key], torch, device) for key in ("x", "w", "bias"))
+    rlog = torch.empty((t, e), dtype=torch.bfloat16, device=device)
+    fused_ms = _timed_flushed(torch, device, stream, lambda: sa.moe_router(
+        hx, rw, rb, k, topk_idx=idx, topk_weight=w, expert_counts=counts, stream=stream), reps)
+    two_ms = _timed_flushed(torch, device, stream, lambda: (
+        sa.linear_bias(hx, rw, rb, out=rlog, stream=stream),
+        sa.moe_router_topk_softmax(rlog, k, topk_idx=idx, topk_weight=w, expert_counts=counts, stream=stream)),
+        reps)
 
     def line(src, kernel, ms, nbytes, note):
         gbs = nbytes / (ms * 1e-3) / 1e9
@@ -614,7 +625,15 @@ def bench_around_attention(args, sa, torch, device, pk):
             "moe_router": line("router.cu", "router_topk_kernel", router_ms, router_bytes,
                                "32768 tokens x 128 bf16 logits, top 4, softmax over the selected, "
                                "expert counts; L2 flushed (written, then read back) before each launch"),
-            "gpu_launches": 2 * (reps + 3)}
+            "moe_router_fused": {"workload": "router of 32768 tokens: [32768, 2880] x [128, 2880]^T + bias, "
+                                             "bf16 logits, top 4 softmax, counts; L2 flushed before each call",
+                                 "fused_us": round(fused_ms * 1e3, 2), "two_kernels_us": round(two_ms * 1e3, 2),
+                                 "kernel": "linear_bias_kernel (router epilogue)",
+                                 "roofline": {"bound": "hbm", "achieved": round(t * 2880 * 2 / (fused_ms * 1e-3) / 1e9, 1),
+                                              "peak": pk["hbm"], "unit": "GB/s",
+                                              "frac": round(t * 2880 * 2 / (fused_ms * 1e-3) / 1e9 / pk["hbm"], 4),
+                                              "note": "bytes = the hidden states read once (189 MB)"}},
+            "gpu_launches": 2 * (reps + 3) + 3 * (reps + 3)}
 
 
 def bench_linear(args, sa, torch, device, pk):

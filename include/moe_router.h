@@ -43,6 +43,26 @@ sa_status moe_router_topk_softmax(const void* logits, long long num_tokens, int 
                                   int top_k, int32_t* topk_idx, void* topk_weight,
                                   int32_t* expert_counts, cudaStream_t stream);
 
+/*
+ * The whole router in one tcgen05 kernel: logits = x W_router^T + bias (the
+ * accumulator seeded with the bias, as in linear_bias.h), each logit rounded to
+ * bf16, then the Top-K softmax above, in the epilogue of the kernel that owns
+ * the token's row; no logits are written.  The results are bit-identical to
+ * linear_bias followed by moe_router_topk_softmax.
+ *
+ *  x         bf16 [num_tokens, hidden], 16-byte aligned
+ *  w_router  bf16 [num_experts, hidden] (one row per expert), 16-byte aligned
+ *  bias      bf16 [num_experts] or NULL
+ *  outputs as for moe_router_topk_softmax (expert_counts cleared by the call).
+ *  1 <= num_experts <= 256, 1 <= top_k <= min(8, num_experts), hidden a
+ *  multiple of 8 (<= 2^30).  Status codes as above; num_tokens == 0 launches
+ *  nothing.  A device wait that runs out (sink_attn_set_wait_timeout_ns) ends
+ *  the kernel cleanly and sets SA_ERR_TIMEOUT in the device status word.
+ */
+sa_status moe_router(const void* x, const void* w_router, const void* bias, int num_tokens,
+                     int hidden, int num_experts, int top_k, int32_t* topk_idx, void* topk_weight,
+                     int32_t* expert_counts, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

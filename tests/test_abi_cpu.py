@@ -224,3 +224,14 @@ def test_library_has_no_unresolved_internal_symbols(lib):
 def test_linear_rejects_tile_count_overflow(lib):
     # 2^31 - 1 rows x 2^30 features: more output tiles than an int holds
     assert lib.linear_bias(FAKE, FAKE, None, 2**31 - 1, 2**30, 64, FAKE, None) == SA_ERR_SHAPE
+
+
+def test_fused_router_rejects_before_launch(lib):
+    f = lib.moe_router
+    assert f(FAKE, FAKE, None, 10, 2880, 0, 1, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, FAKE, None, 10, 2880, 257, 4, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, FAKE, None, 10, 2880, 128, 9, FAKE, FAKE, None, None) == SA_ERR_SHAPE
+    assert f(FAKE, FAKE, None, 10, 2884, 128, 4, FAKE, FAKE, None, None) == SA_ERR_UNSUPPORTED
+    assert f(None, FAKE, None, 10, 2880, 128, 4, FAKE, FAKE, None, None) == SA_ERR_NULL
+    assert f(MISALIGNED, FAKE, None, 10, 2880, 128, 4, FAKE, FAKE, None, None) == SA_ERR_ALIGNMENT
+    assert f(None, None, None, 0, 2880, 128, 4, None, None, None, None) == SA_OK

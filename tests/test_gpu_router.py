@@ -135,3 +135,20 @@ def test_router_with_projection_against_the_oracle_router():
         assert best_unsel <= worst_sel + 2 * eb[row]
         assert np.all(np.diff(gw[row]) <= 0) and abs(gw[row].sum() - 1.0) <= k * 2.0 ** -8
     print(f"router end to end: {int(unique.sum())} of {t} rows unambiguous, all match")
+
+
+@pytest.mark.parametrize("t,e,hidden,k", [(2048, 128, 2880, 4), (1000, 32, 2880, 4), (129, 64, 512, 2),
+                                          (300, 256, 256, 8), (1, 128, 2880, 1), (777, 104, 640, 3)])
+def test_fused_router_is_projection_then_topk(t, e, hidden, k):
+    """moe_router (projection with bias seeded in TMEM, bf16 logits, Top-K softmax in the
+    epilogue) equals linear_bias followed by moe_router_topk_softmax bit for bit, counts
+    included; the two-kernel path is tied to the oracle by the tests above."""
+    sa = require_gpu()
+    d = workloads.make_linear(27, t, e, hidden, std=1.0, w_std=0.05, bias_std=0.5)
+    x, w, b = bf16(d["x"]), bf16(d["w"]), bf16(d["bias"])
+    idx_f, w_f, c_f = sa.moe_router(x, w, b, k, return_counts=True)
+    logits = sa.linear_bias(x, w, b)
+    idx_u, w_u, c_u = sa.moe_router_topk_softmax(logits, k, return_counts=True)
+    assert torch.equal(idx_f, idx_u) and torch.equal(w_f, w_u) and torch.equal(c_f, c_u)
+    assert int(c_f.sum()) == t * k
+    assert sa.sink_attn_device_status(True) == 0
