@@ -87,3 +87,29 @@ def test_long_single_sequence_prefill():
     gl = host(l)[[r[0] for r in rows], [r[1] for r in rows]]
     assert_close(go, gl, ro, rl, "32k prefill sampled")
     assert sa.sink_attn_device_status(True) == 0
+
+
+def test_positive_infinite_sink_everywhere():
+    """sink = +inf takes all the probability: out = 0 and lse = +inf on every path
+    (prefill, paged prefill, unsplit decode, split decode + merge), as the oracle says."""
+    sa = require_gpu()
+    data = workloads.make_prefill(91, [130, 7], 8, 1, 64, sink_fill=np.inf)
+    o, l = sa.sink_attn_prefill(bf16(data["q"]), bf16(data["k"]), bf16(data["v"]), dev(data["sinks"]),
+                                dev(data["cu_seqlens"]), 130, 0.125)
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"], 0.125, True)
+    assert np.all(ro == 0) and np.all(np.isposinf(rl))
+    assert np.all(host(o) == 0) and np.all(np.isposinf(host(l)))
+    d = workloads.make_decode(92, [1, 40, 3000], 64, 8, 64, sink_fill=np.inf)
+    args = [bf16(d["q"]), bf16(d["k_pages"]), bf16(d["v_pages"]), dev(d["page_table"]), dev(d["kv_lens"]),
+            dev(d["sinks"])]
+    o1, l1 = sa.sink_attn_decode(*args, 0.125, num_splits=1)
+    po, pl = sa.sink_attn_decode(*args, 0.125, num_splits=4)
+    mo, ml = sa.sink_attn_merge(po, pl)
+    for out, lse in ((o1, l1), (mo, ml)):
+        assert np.all(host(out) == 0) and np.all(np.isposinf(host(lse)))
+    m = workloads.make_mixed(93, [1, 20], [50, 300], 64, 8, 64, sink_fill=np.inf)
+    o2, l2 = sa.sink_attn_prefill_paged(bf16(m["q"]), bf16(m["k_pages"]), bf16(m["v_pages"]),
+                                        dev(m["page_table"]), dev(m["cu_seqlens_q"]), dev(m["kv_lens"]),
+                                        dev(m["sinks"]), 20, 0.125)
+    assert np.all(host(o2) == 0) and np.all(np.isposinf(host(l2)))
+    assert sa.sink_attn_device_status(True) == 0
