@@ -384,9 +384,9 @@ static sa_status prefill_common(const void* q, const void* k, const void* v,
   if (sa_status s = status_ptr(&a.status)) return s;
   CUtensorMap qm, qpm, km, vm;
   if (sa_status s = map_tokens_heads(&qm, q, total_q, hq, 128)) return s;
-  // packed short sequences (group >= 4): boxes of 128 / G tokens x the G heads of a group
+  // packed short sequences (G = 4, 8, 16): boxes of 128 / G tokens x the G heads of a group
   const int group = hq / hkv;
-  if (group >= 4) {
+  if (group >= 4 && 128 % group == 0) {
     if (sa_status s = map_tokens_heads(&qpm, q, total_q, hq, 128 / group, group)) return s;
   } else {
     qpm = qm;

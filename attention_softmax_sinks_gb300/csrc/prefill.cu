@@ -16,7 +16,7 @@
 //    grid is persistent (one CTA per SM) except when every sequence has the
 //    same length and contiguous KV: then one CTA per item, heaviest first, and
 //    the hardware's block scheduler balances.
-//  * GQA packing (persistent schedule, group G >= 4).  A sequence with at most
+//  * GQA packing (persistent schedule, group G = 4, 8 or 16).  A sequence with at most
 //    2 * 128 / G new tokens (a decode row, a short chunk) would fill one row of
 //    each 128-row tile per head; instead it becomes one item per KV head whose
 //    two tiles hold 128 / G tokens x all G query heads of the group (row r:
@@ -168,9 +168,10 @@ __device__ __forceinline__ int block_tiles(const PrefillArgs& a, int q0, int q_l
 }
 
 // A sequence of q_len new tokens is packed (see the schedule notes) when the
-// group has at least 4 query heads and its tokens fit the two tiles of one item.
+// group has at least 4 query heads and divides the 128 tile rows (G = 4, 8, 16),
+// and its tokens fit the two tiles of one item.
 __device__ __forceinline__ bool packs(const PrefillArgs& a, int q_len) {
-  return a.group >= 4 && q_len <= 2 * (kBlockQ / a.group);
+  return a.group >= 4 && kBlockQ % a.group == 0 && q_len <= 2 * (kBlockQ / a.group);
 }
 
 __device__ __forceinline__ unsigned long long pair_key(int tiles, bool packed, int pair) {

@@ -140,3 +140,19 @@ def test_page_permutation_is_bit_exact():
         o1, l1, _ = _run(sa, d1, 0.125, splits)
         o2, l2, _ = _run(sa, d2, 0.125, splits)
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("hq,hkv", [(6, 2), (24, 2), (40, 8), (12, 1)])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_odd_groups(hq, hkv, splits):
+    """Group sizes 3, 12, 5, 12: the 8-wide MMA tiles are partly masked (two tiles above 8)."""
+    sa = require_gpu()
+    kv = [1, 17, 600, 2049]
+    d = workloads.make_decode(19, kv, hq, hkv, 64)
+    o, l, _ = _run(sa, d, 0.125, splits)
+    if splits > 1:
+        o, l = sa.sink_attn_merge(o, l)
+    ro, rl = oracle.decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["kv_lens"],
+                           d["sinks"], 0.125)
+    assert_close(host(o), host(l), ro, rl, f"decode group {hq // hkv} splits={splits}")
+    assert sa.sink_attn_device_status(True) == 0

@@ -67,3 +67,25 @@ def test_many_decode_rows_in_one_call():
     gl = host(l)[[r[0] for r in rows], [r[1] for r in rows]]
     assert_close(go, gl, ro, rl, "many decode rows")
     assert sa.sink_attn_device_status(True) == 0
+
+
+@pytest.mark.parametrize("hq,hkv", [(24, 2), (6, 2), (40, 8), (12, 1)])
+def test_groups_that_do_not_divide_the_tile(hq, hkv):
+    """Group sizes 12, 3, 5 and 12 (odd, or not dividing 128): short sequences are not
+    packed and take the head-pair (or single-head) items; results match the oracle."""
+    sa = require_gpu()
+    q_lens = [1, 3, 9, 20, 40, 130]
+    kv_lens = [1, 100, 9, 700, 40, 200]
+    d = workloads.make_mixed(75, q_lens, kv_lens, hq, hkv, 64)
+    o, l = sa.sink_attn_prefill_paged(bf16(d["q"]), bf16(d["k_pages"]), bf16(d["v_pages"]),
+                                      dev(d["page_table"]), dev(d["cu_seqlens_q"]), dev(d["kv_lens"]),
+                                      dev(d["sinks"]), max(q_lens), 0.125, causal=True)
+    ro, rl = oracle.prefill_paged(d["q"], d["k_pages"], d["v_pages"], d["page_table"],
+                                  d["cu_seqlens_q"], d["kv_lens"], d["sinks"], 0.125, True)
+    assert_close(host(o), host(l), ro, rl, f"group {hq // hkv} paged")
+    c = workloads.make_prefill(76, q_lens, hq, hkv, 64)
+    o2, l2 = sa.sink_attn_prefill(bf16(c["q"]), bf16(c["k"]), bf16(c["v"]), dev(c["sinks"]),
+                                  dev(c["cu_seqlens"]), max(q_lens), 0.125)
+    ro2, rl2 = oracle.prefill(c["q"], c["k"], c["v"], c["sinks"], c["cu_seqlens"], 0.125, True)
+    assert_close(host(o2), host(l2), ro2, rl2, f"group {hq // hkv} contiguous")
+    assert sa.sink_attn_device_status(True) == 0
