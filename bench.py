@@ -372,7 +372,9 @@ def bench_mixed(args, sa, torch, device, pk):
             "ms": round(ms, 4), "flops": flops, "bytes": nbytes, "decode_rows": int((q == 1).sum()),
             "roofline": {"bound": bound, "frac": round(max(t_tc, t_hbm) / (ms * 1e-3), 4),
                          "tensor_frac": round(t_tc / (ms * 1e-3), 4), "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
-                         "note": "frac = max(FLOPs / peak bf16, bytes / peak HBM) / time"},
+                         "note": "frac = max(FLOPs / peak bf16, bytes / peak HBM) / time",
+                         "traffic": recorded_traffic("sink_prefill_kernel_mixed", ("prefill.cu", "ptx.cuh", "internal.h")),
+                         "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"},
             "gpu_launches": len(times)}
 
 
@@ -847,6 +849,7 @@ def run_profile_case(case):
     decode_long: 2 sequences x 131072 tokens (512 MiB of KV), 64/8 heads, 32 splits.
     prefill: 1 x 8192 tokens causal, 64/8 heads.
     prefill_persistent: 8192 + 8191 tokens causal (the persistent schedule), 64/8 heads.
+    mixed:   the ragged mixed batch (32 sequences, paged, GQA-packed decode rows).
     linear:  [32768, 4096] x [2880, 4096]^T + bias (the bench's output projection, ~470 MB).
     rope:    32768 tokens, 64/8 heads, bias + YaRN.
     router:  32768 tokens x 128 experts, top 4, counts.
@@ -884,6 +887,16 @@ def run_profile_case(case):
         q, k, v, sinks, cu = (to_dev(host[n], torch, device) for n in ("q", "k", "v", "sinks", "cu_seqlens"))
         for _ in range(5):
             sa.sink_attn_prefill(q, k, v, sinks, cu, cfg["seqlen"], cfg["sm_scale"], causal=True)
+    elif case == "mixed":
+        cfg = workloads.WORKLOADS["ragged_mixed"]
+        q_lens, kv_lens = workloads.ragged_mixed_lengths(cfg["seed"] + 2, cfg["num_seqs"], cfg["max_kv"])
+        host = workloads.make_mixed(cfg["seed"], q_lens, kv_lens, cfg["hq"], cfg["hkv"], cfg["d"],
+                                    cfg["page_size"], cfg["sink_std"])
+        dv = {n: to_dev(host[n], torch, device)
+              for n in ("q", "k_pages", "v_pages", "page_table", "cu_seqlens_q", "kv_lens", "sinks")}
+        for _ in range(5):
+            sa.sink_attn_prefill_paged(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"], dv["cu_seqlens_q"],
+                                       dv["kv_lens"], dv["sinks"], int(q_lens.max()), cfg["sm_scale"], causal=True)
     elif case == "linear":
         d = workloads.make_linear(61, 32768, 2880, 4096)
         x, w, b = (to_dev(d[key], torch, device) for key in ("x", "w", "bias"))
@@ -920,8 +933,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
-    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_persistent", "linear", "rope",
-                                          "router"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_persistent", "mixed", "linear",
+                                          "rope", "router"], default=None,
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:

@@ -172,3 +172,35 @@ def test_qkv_rope_prefill_sized_sampled():
     _assert_rot(host(q)[rows], rq, pq, ms, "q 32k")
     _assert_rot(host(k)[rows], rk, pk, ms, "k 32k")
     _assert_rot(host(v)[rows], rv, np.zeros_like(rv), 0.0, "v 32k")
+
+
+def test_append_then_decode_step():
+    """One decode step as a serving loop runs it: the new token's QKV gets its bias and
+    YaRN rotation and its K/V are appended to the paged cache (qkv_bias_rope_append_paged),
+    then attention with sinks reads the cache (split decode + merge).  The oracle builds
+    its own cache: fp64 rotation rounded to bf16, appended by the oracle, then its decode."""
+    from oracle import moe
+    import oracle
+    sa = require_gpu()
+    hq, hkv = 64, 8
+    kv_lens = np.array([1, 17, 300, 4096], dtype=np.int32)     # including the new token
+    b = len(kv_lens)
+    base = workloads.make_decode(94, list(kv_lens), hq, hkv, 64)
+    cu = np.arange(b + 1, dtype=np.int32)                        # one new token per sequence
+    inp = workloads.make_qkv(95, b, hq, hkv)
+    p = _params(sa)
+    gk, gv = bf16(base["k_pages"]), bf16(base["v_pages"])
+    q = sa.qkv_bias_rope_append_paged(bf16(inp["qkv"]), bf16(inp["bias"]), dev(cu), dev(kv_lens), gk, gv,
+                                      dev(base["page_table"]), hq, rope=p)
+    po, pl = sa.sink_attn_decode(q, gk, gv, dev(base["page_table"]), dev(kv_lens), dev(base["sinks"]), 0.125,
+                                 num_splits=3)
+    out, lse = sa.sink_attn_merge(po, pl)
+    inv, ms = _oracle_tables(p)
+    rq, rk, rv = orope.qkv_bias_rope(inp["qkv"], inp["bias"], cu, kv_lens, hq, hkv, 64, inv, ms)
+    bits = lambda x: moe.bf16_bits(moe.round_to_bf16(x))
+    kp, vp = orope.append_paged_kv(base["k_pages"], base["v_pages"], base["page_table"], cu, kv_lens,
+                                   moe.round_to_bf16(rk), moe.round_to_bf16(rv))
+    ro, rl = oracle.decode(bits(rq), bits(kp), bits(vp), base["page_table"], kv_lens, base["sinks"], 0.125)
+    from gpu_common import assert_close
+    assert_close(host(out), host(lse), ro, rl, "append then decode")
+    assert sa.sink_attn_device_status(True) == 0
