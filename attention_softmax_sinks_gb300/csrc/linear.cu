@@ -32,7 +32,7 @@
 // of the plain layer followed by the standalone router, bit for bit.
 #include <cstdint>
 
-#include "ops_internal.h"
+#include "linear_args.h"
 #include "ptx.cuh"
 
 namespace sa {

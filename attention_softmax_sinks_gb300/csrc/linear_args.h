@@ -1,0 +1,34 @@
+// Launcher interface of the bias-seeded linear layer and its router form
+// (linear.cu).  Arguments arrive already validated by abi.cu.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sa {
+
+struct LinearArgs {
+  const uint16_t* bias;  // bf16 [N] or nullptr
+  uint16_t* out;         // bf16 [M, N] (plain linear layer)
+  int M, N, K;
+  int block_n, tiles_m, tiles_n;
+  unsigned* status;
+  unsigned long long timeout_ns;
+  // fused router (N = experts <= block_n, one column tile): per row, the Top-K of
+  // the bf16-rounded logits, softmax weights and per-expert counts
+  int32_t* topk_idx;     // [M, top_k]
+  uint16_t* topk_w;      // bf16 [M, top_k]
+  int32_t* counts;       // [N] (zeroed by the caller) or nullptr
+  int top_k;
+};
+
+// Output tile width (128, 192, 240 or 256) for N output features.
+int linear_tile_n(int n);
+// amap: x [M, K] in boxes of 128 rows x 64; bmap: W [N, K] in boxes of block_n rows x 64.
+cudaError_t launch_linear(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
+                          int sms, cudaStream_t stream);
+// Router projection + Top-K softmax in the epilogue; a.block_n must be 32, 64, 128 or 256.
+cudaError_t launch_linear_router(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
+                                 int sms, cudaStream_t stream);
+
+}  // namespace sa

@@ -21,7 +21,7 @@
 #include <cmath>
 #include <cstdint>
 
-#include "ops_internal.h"
+#include "rope_args.h"
 #include "ptx.cuh"
 
 namespace sa {

@@ -17,7 +17,7 @@
 // receives at most one add per SM.
 #include <cstdint>
 
-#include "ops_internal.h"
+#include "router_args.h"
 #include "ptx.cuh"
 
 namespace sa {

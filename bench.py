@@ -614,17 +614,19 @@ def bench_around_attention(args, sa, torch, device, pk):
         sa.moe_router_topk_softmax(rlog, k, topk_idx=idx, topk_weight=w, expert_counts=counts, stream=stream)),
         reps)
 
-    def line(src, kernel, ms, nbytes, note):
+    def line(srcs, kernel, ms, nbytes, note):
         gbs = nbytes / (ms * 1e-3) / 1e9
         return {"workload": note, "kernel": kernel, "us": round(ms * 1e3, 2), "bytes": nbytes,
                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                              "frac": round(gbs / pk["hbm"], 4),
-                             "traffic": recorded_traffic(kernel, (src, "ops_internal.h", "ptx.cuh")),
+                             "traffic": recorded_traffic(kernel, srcs),
                              "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}}
-    return {"qkv_bias_rope": line("rope.cu", "qkv_rope_kernel", rope_ms, rope_bytes,
+    return {"qkv_bias_rope": line(("rope.cu", "rope_args.h", "internal.h", "ptx.cuh"), "qkv_rope_kernel", rope_ms,
+                                  rope_bytes,
                                   "32768 tokens, 64/8 heads: bias + YaRN (GPT-OSS constants) on q, k; "
                                   "q, k, v written contiguous; L2 flushed (written, then read back) before each launch"),
-            "moe_router": line("router.cu", "router_topk_kernel", router_ms, router_bytes,
+            "moe_router": line(("router.cu", "router_args.h", "ptx.cuh"), "router_topk_kernel", router_ms,
+                               router_bytes,
                                "32768 tokens x 128 bf16 logits, top 4, softmax over the selected, "
                                "expert counts; L2 flushed (written, then read back) before each launch"),
             "moe_router_fused": {"workload": "router of 32768 tokens: [32768, 2880] x [128, 2880]^T + bias, "
@@ -659,7 +661,7 @@ def bench_linear(args, sa, torch, device, pk):
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                          "frac": round(tf / pk["bf16"], 4),
                          "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)",
-                         "traffic": recorded_traffic("linear_bias_kernel", ("linear.cu", "ops_internal.h", "ptx.cuh")),
+                         "traffic": recorded_traffic("linear_bias_kernel", ("linear.cu", "linear_args.h", "ptx.cuh")),
                          "traffic_unit": "bytes per launch",
                          "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"},
             "cublas_context": {"ms": round(ref_ms, 4), "tflops": round(flops / (ref_ms * 1e-3) / 1e12, 2),
