@@ -285,9 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncthreads();
         }
       }
+      // pairs with work: the non-zero keys (they sort first), counted by the whole block
+      int n = 0;
+      for (int p0 = 0; p0 < pairs; p0 += kThreads) {
+        const int p = p0 + static_cast<int>(threadIdx.x);
+        n += __syncthreads_count(p < pairs && sm.sortkey[p] != 0ull);
+      }
       if (threadIdx.x == 0) {
-        int n = 0;
-        while (n < pairs && sm.sortkey[n] != 0ull) ++n;
         sm.n_pairs = n;
         sm.sorted = 1;
       }
