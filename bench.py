@@ -855,6 +855,7 @@ def run_profile_case(case):
     linear:  [32768, 4096] x [2880, 4096]^T + bias (the bench's output projection, ~470 MB).
     rope:    32768 tokens, 64/8 heads, bias + YaRN.
     router:  32768 tokens x 128 experts, top 4, counts.
+    router_fused: the router projection [32768, 2880] x [128, 2880]^T + bias with the Top-K epilogue.
     """
     import torch
     import attention_softmax_sinks_gb300 as sa
@@ -899,6 +900,11 @@ def run_profile_case(case):
         for _ in range(5):
             sa.sink_attn_prefill_paged(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"], dv["cu_seqlens_q"],
                                        dv["kv_lens"], dv["sinks"], int(q_lens.max()), cfg["sm_scale"], causal=True)
+    elif case == "router_fused":
+        d = workloads.make_linear(43, 32768, 128, 2880, std=1.0, w_std=0.05, bias_std=0.5)
+        x, w, b = (to_dev(d[key], torch, device) for key in ("x", "w", "bias"))
+        for _ in range(5):
+            sa.moe_router(x, w, b, 4, return_counts=True)
     elif case == "linear":
         d = workloads.make_linear(61, 32768, 2880, 4096)
         x, w, b = (to_dev(d[key], torch, device) for key in ("x", "w", "bias"))
@@ -936,7 +942,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_persistent", "mixed", "linear",
-                                          "rope", "router"], default=None,
+                                          "rope", "router", "router_fused"], default=None,
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
     if args.profile:
