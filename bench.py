@@ -636,7 +636,10 @@ def bench_around_attention(args, sa, torch, device, pk):
                                  "roofline": {"bound": "hbm", "achieved": round(t * 2880 * 2 / (fused_ms * 1e-3) / 1e9, 1),
                                               "peak": pk["hbm"], "unit": "GB/s",
                                               "frac": round(t * 2880 * 2 / (fused_ms * 1e-3) / 1e9 / pk["hbm"], 4),
-                                              "note": "bytes = the hidden states read once (189 MB)"}},
+                                              "note": "bytes = the hidden states read once (189 MB)",
+                                              "traffic": recorded_traffic("linear_bias_kernel_router",
+                                                                          ("linear.cu", "linear_args.h", "ptx.cuh")),
+                                              "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}},
             "gpu_launches": 2 * (reps + 3) + 3 * (reps + 3)}
 
 
