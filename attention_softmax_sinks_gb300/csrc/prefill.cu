@@ -412,11 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // Producer / MMA warpgroup needs few registers; the softmax warpgroups hold a
-  // whole 128-wide score row each.  128*120 + 256*192 = 384*168 (launch total).
+  // whole 128-wide score row each.  128*56 + 256*224 = 384*168 (launch total).
   // Each setmaxnreg sits inside its own role branch so the compiler can give
   // every region its own budget.
   if (warp < 4) {
-    regs_dec<120>();
+    regs_dec<56>();
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer
       // The whole warp walks the items in step; lane 0 waits on barriers (and
@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    regs_inc<192>();
+    regs_inc<224>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - 4) >> 2;      // query tile of this warpgroup
     const int qw = warp & 3;            // TMEM lane quarter
