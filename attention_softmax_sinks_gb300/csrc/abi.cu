@@ -444,16 +444,18 @@ sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int
   const long long tiles_m = (static_cast<long long>(m) + 127) / 128;
   const long long tiles_n = (static_cast<long long>(n) + a.block_n - 1) / a.block_n;
   if (tiles_m * tiles_n >= (1LL << 31)) return SA_ERR_SHAPE;
-  a.tiles_m = static_cast<int>(tiles_m);
   a.tiles_n = static_cast<int>(tiles_n);
   unsigned* status = nullptr;
   if (sa_status s = status_ptr(&status)) return s;
   a.status = status;
   a.timeout_ns = g_timeout_ns;
+  const int sms = sm_count();
+  a.m_sub = sa::linear_m_sub(m, n, a.block_n, sms);  // tiles_m above bounds the count for m_sub = 2
+  a.tiles_m = static_cast<int>((tiles_m + a.m_sub - 1) / a.m_sub);
   CUtensorMap am, bm;
   if (sa_status s = map_matrix(&am, x, m, k, 128)) return s;
   if (sa_status s = map_matrix(&bm, w, n, k, a.block_n)) return s;
-  return sa::launch_linear(am, bm, a, sm_count(), stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+  return sa::launch_linear(am, bm, a, sms, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
 sa_status moe_router(const void* x, const void* w_router, const void* bias, int num_tokens,
@@ -479,7 +481,9 @@ sa_status moe_router(const void* x, const void* w_router, const void* bias, int 
   a.N = num_experts;
   a.K = hidden;
   a.block_n = num_experts <= 32 ? 32 : num_experts <= 64 ? 64 : num_experts <= 128 ? 128 : 256;
-  a.tiles_m = (num_tokens + 127) / 128;
+  const int sms = sm_count();
+  a.m_sub = sa::linear_m_sub(num_tokens, num_experts, a.block_n, sms);
+  a.tiles_m = (num_tokens + 128 * a.m_sub - 1) / (128 * a.m_sub);
   a.tiles_n = 1;
   a.status = status;
   a.timeout_ns = g_timeout_ns;
@@ -490,7 +494,7 @@ sa_status moe_router(const void* x, const void* w_router, const void* bias, int 
   CUtensorMap am, bm;
   if (sa_status s = map_matrix(&am, x, num_tokens, hidden, 128)) return s;
   if (sa_status s = map_matrix(&bm, w_router, num_experts, hidden, a.block_n)) return s;
-  return sa::launch_linear_router(am, bm, a, sm_count(), stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+  return sa::launch_linear_router(am, bm, a, sms, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
 sa_status moe_router_topk_softmax(const void* logits, long long num_tokens, int num_experts,

@@ -9,27 +9,35 @@
 // tile (tcgen05.st) and every MMA of the tile accumulates onto it; there is no
 // zero-initialising first MMA and no bias add in the epilogue.
 //
-// Persistent kernel, one CTA per SM, 256 threads:
-//   warp 0        TMA producer: A (x, 128 x 64) and B (W, BN x 64) boxes,
-//                 128-byte swizzle, into a kStages-deep ring
+// Persistent kernel, one CTA per SM; an output tile is MT x 128 rows by BN
+// columns (MT = 1 or 2 sub-tiles of 128 rows), 128 + 128 MT threads:
+//   warp 0        TMA producer: MT A boxes (x, 128 x 64 each) and one B box
+//                 (W, BN x 64), 128-byte swizzle, into a kStages-deep ring
 //   warp 1        TMEM owner and MMA issuer (one elected thread): per 64-wide
-//                 K step four tcgen05.mma M=128 N=BN K=16, accumulate always on
-//   warps 4..7    epilogue: warp w reads TMEM lanes [32 (w-4), +32) (one output
+//                 K step and sub-tile four tcgen05.mma M=128 N=BN K=16,
+//                 accumulate always on; the MT sub-tiles read the same B stage
+//   warps 4..     epilogue, four warps per sub-tile: warp w reads TMEM lanes
+//                 [32 (w % 4), +32) of its sub-tile's accumulator (one output
 //                 row per thread), converts to bf16, stores, then seeds the
 //                 buffer with the bias of the tile that will use it next
-// Two TMEM accumulators alternate, so the epilogue of tile i overlaps the
-// MMAs of tile i + 1.  Tiles are numbered with the N index fastest: the CTAs
-// working at the same time share one 128-row block of x through L2.
+// Two TMEM accumulators (each MT sub-tiles) alternate, so the epilogue of tile
+// i overlaps the MMAs of tile i + 1.  Tiles are numbered with the N index
+// fastest: the CTAs working at the same time share one row block of x through
+// L2.  MT = 2 serves skinny outputs (one column tile, N <= 128: the router
+// projection): the layer streams x once while every row block re-reads all of
+// W, so two sub-tiles per W stage halve the W bytes per x byte and leave more
+// of the ring to x.
 //
-// Router form (kRouter): the MoE router projection (N = experts <= 256, one
+// Router form (SLOTS > 0): the MoE router projection (N = experts <= 256, one
 // column tile) whose epilogue takes the page's Top-K-then-softmax router
 // instead of storing logits: the thread that owns a token row rounds each
-// logit to bf16, ranks it in a sorted register list of eight packed keys
-// (bf16 order in the high half, 0xFFFF - expert in the low half, so equal
-// logits keep the lower expert first), and writes the K selected experts,
-// their softmax weights (fp32, stored as bf16) and per-expert counts (shared
-// histogram, added to the global counts once per CTA).  The arithmetic is that
-// of the plain layer followed by the standalone router, bit for bit.
+// logit to bf16, ranks it in a sorted register list of SLOTS packed keys (4
+// for top_k <= 4, else 8; bf16 order in the high half, 0xFFFF - expert in the
+// low half, so equal logits keep the lower expert first), and writes the K
+// selected experts, their softmax weights (fp32, stored as bf16) and
+// per-expert counts (shared histogram, added to the global counts once per
+// CTA).  The arithmetic is that of the plain layer followed by the
+// standalone router, bit for bit.
 #include <cstdint>
 
 #include "linear_args.h"
@@ -38,9 +46,8 @@
 namespace sa {
 namespace {
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;  // rows of one sub-tile (one tcgen05.mma M)
 constexpr int kBK = 64;
-constexpr int kLinThreads = 256;
 constexpr int kEpiWarp0 = 4;
 // Drains (MMAs before TMEM is freed, copies before shared memory is released)
 // always wait up to this long, even when the caller set a shorter wait budget.
@@ -61,14 +68,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_kk(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-template <int BN>
+template <int BN, int MT>
 struct LinCfg {
-  static constexpr int kABytes = kBM * kBK * 2;
+  static_assert(MT == 1 || (MT == 2 && BN <= 128), "two sub-tiles need BN <= 128 (TMEM)");
+  static constexpr int kThreads = 128 + 128 * MT;  // 4 control warps + 4 epilogue warps per sub-tile
+  static constexpr int kSubABytes = kBM * kBK * 2;
+  static constexpr int kABytes = MT * kSubABytes;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 6 ? 6 : (200 * 1024) / kStageBytes;
-  static constexpr int kAccStride = BN <= 128 ? 128 : 256;  // TMEM columns between the two accumulators
-  static constexpr int kTmemCols = 2 * kAccStride;
+  static constexpr int kAccStride = BN <= 128 ? 128 : 256;  // TMEM columns between sub-tile accumulators
+  static constexpr int kTmemCols = 2 * MT * kAccStride;     // two buffers of MT sub-tiles
+  static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
   static constexpr size_t kSmem = 1024 /*alignment slack*/ + static_cast<size_t>(kStages) * kStageBytes + 2048;
 };
 
@@ -107,11 +118,11 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float(bits << 16);
 }
 
-constexpr int kRouterSlots = 8;  // largest supported top_k
-
-__device__ __forceinline__ void offer(uint32_t (&best)[kRouterSlots], uint32_t key) {
+// Router form: S slots hold the S largest keys (S = 4 serves top_k <= 4, 8 up to 8).
+template <int S>
+__device__ __forceinline__ void offer(uint32_t (&best)[S], uint32_t key) {
 #pragma unroll
-  for (int r = 0; r < kRouterSlots; ++r) {  // best[] stays sorted, largest first
+  for (int r = 0; r < S; ++r) {  // best[] stays sorted, largest first
     const uint32_t hi = max(best[r], key);
     key = min(best[r], key);
     best[r] = hi;
@@ -135,11 +146,14 @@ __device__ __forceinline__ void seed_bias(uint32_t taddr, const uint16_t* bias, 
   }
 }
 
-template <int BN, bool kRouter>
-__global__ void __launch_bounds__(kLinThreads, 1)
+// SLOTS = 0: plain layer (bf16 output); SLOTS = 4 or 8: router form keeping that
+// many candidates per token row.
+template <int BN, int MT, int SLOTS>
+__global__ void __launch_bounds__(LinCfg<BN, MT>::kThreads, 1)
 linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                    const LinearArgs a) {
-  using C = LinCfg<BN>;
+  using C = LinCfg<BN, MT>;
+  constexpr bool kRouter = SLOTS > 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   LinBarriers& sb = *reinterpret_cast<LinBarriers*>(tiles + static_cast<size_t>(C::kStages) * C::kStageBytes);
@@ -157,7 +171,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sb.acc_full[b]), 1);
-      mbar_init(smem_u32(&sb.acc_empty[b]), 4);
+      mbar_init(smem_u32(&sb.acc_empty[b]), 4 * MT);  // lane 0 of every epilogue warp
     }
     mbar_init(smem_u32(&sb.drain), 1);
     sb.abort_flag = 0;
@@ -165,7 +179,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
     fence_barrier_init();
   }
   if constexpr (kRouter)
-    for (int e = threadIdx.x; e < 256; e += kLinThreads) sb.hist[e] = 0;
+    for (int e = threadIdx.x; e < 256; e += C::kThreads) sb.hist[e] = 0;
   if (warp == 1) {
     tmem_alloc(smem_u32(&sb.tmem_base), C::kTmemCols);
     tmem_relinquish();
@@ -184,7 +198,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
       int g = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles_total && ok; t += gridDim.x) {
-        const int m0 = (t / a.tiles_n) * kBM;
+        const int m0 = (t / a.tiles_n) * (kBM * MT);
         const int n0 = (t % a.tiles_n) * BN;
         for (int kb = 0; kb < k_steps; ++kb, ++g) {
           const int s = g % C::kStages;
@@ -196,7 +210,9 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
           const uint32_t bar = smem_u32(&sb.full[s]);
           const uint32_t dst = smem_u32(tiles + static_cast<size_t>(s) * C::kStageBytes);
           mbar_arrive_expect_tx(bar, C::kStageBytes);
-          tma_load_2d(dst, &amap, kb * kBK, m0, bar, pol_a);
+#pragma unroll
+          for (int sub = 0; sub < MT; ++sub)  // rows past M are zero-filled
+            tma_load_2d(dst + sub * C::kSubABytes, &amap, kb * kBK, m0 + sub * kBM, bar, pol_a);
           tma_load_2d(dst + C::kABytes, &bmap, kb * kBK, n0, bar, pol_b);
           sb.issued = g + 1;
         }
@@ -212,7 +228,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
         ok = wait_or_abort(smem_u32(&sb.acc_empty[b]), (i >> 1) & 1, a.timeout_ns, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + b * C::kAccStride;
+        const uint32_t d = tmem + b * MT * C::kAccStride;
         for (int kb = 0; kb < k_steps; ++kb, ++g) {
           const int s = g % C::kStages;
           ok = wait_or_abort(smem_u32(&sb.full[s]), (g / C::kStages) & 1, a.timeout_ns, abort_flag);
@@ -222,7 +238,10 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
           const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_ss(d, sw128_kmajor(a_addr + kk * 32), sw128_kmajor(b_addr + kk * 32), kIdesc, 1u);
+#pragma unroll
+            for (int sub = 0; sub < MT; ++sub)
+              tc_mma_ss(d + sub * C::kAccStride, sw128_kmajor(a_addr + sub * C::kSubABytes + kk * 32),
+                        sw128_kmajor(b_addr + kk * 32), kIdesc, 1u);
           tc_commit(smem_u32(&sb.empty[s]));
         }
         if (ok) tc_commit(smem_u32(&sb.acc_full[b]));
@@ -233,12 +252,15 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
       if (!mbar_wait(smem_u32(&sb.drain), 0, kDrainTimeoutNs)) raise_status(a.status, kStatusTimeout);
     }
   } else if (warp >= kEpiWarp0) {
-    const int q = warp - kEpiWarp0;                    // TMEM lane quarter
+    const int sub = (warp - kEpiWarp0) >> 2;           // sub-tile of this warp
+    const int q = warp & 3;                            // TMEM lane quarter (a warp reaches lanes 32 (warp % 4) ..)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // TMEM column of this warp's accumulator in buffer j
+    auto acc_col = [&](int j) { return static_cast<uint32_t>((j * MT + sub) * C::kAccStride); };
     // seed both accumulators for this CTA's first two tiles
     for (int j = 0; j < 2; ++j) {
       const int t = blockIdx.x + j * gridDim.x;
-      if (t < tiles_total) seed_bias<BN>(tmem + lane_base + j * C::kAccStride, a.bias, (t % a.tiles_n) * BN, a.N);
+      if (t < tiles_total) seed_bias<BN>(tmem + lane_base + acc_col(j), a.bias, (t % a.tiles_n) * BN, a.N);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -252,16 +274,16 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const int m0 = (t / a.tiles_n) * kBM;
+      const int m0 = (t / a.tiles_n) * (kBM * MT) + sub * kBM;
       const int n0 = (t % a.tiles_n) * BN;
       const int row = m0 + 32 * q + lane;
       uint16_t* orow = a.out + static_cast<long long>(row) * a.N;
-      const uint32_t acc = tmem + lane_base + b * C::kAccStride;
+      const uint32_t acc = tmem + lane_base + acc_col(b);
       if constexpr (kRouter) {
-        // logits of token `row`: bf16-rounded, ranked into the eight largest keys
-        uint32_t best[kRouterSlots];
+        // logits of token `row`: bf16-rounded, ranked into the SLOTS largest keys
+        uint32_t best[SLOTS];
 #pragma unroll
-        for (int r = 0; r < kRouterSlots; ++r) best[r] = 0;  // below every real key
+        for (int r = 0; r < SLOTS; ++r) best[r] = 0;  // below every real key
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r32[32];
@@ -272,17 +294,17 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
             const int e = c + v;
             if (e < a.N) {
               const uint32_t bits = pack_bf16x2(__uint_as_float(r32[v]), 0.0f) & 0xFFFFu;
-              offer(best, (order16(bits) << 16) | (0xFFFFu - static_cast<uint32_t>(e)));
+              offer<SLOTS>(best, (order16(bits) << 16) | (0xFFFFu - static_cast<uint32_t>(e)));
             }
           }
         }
         if (row < a.M) {
           const int K = a.top_k;
           const float mx = key_value(best[0]);
-          float ex[kRouterSlots];
+          float ex[SLOTS];
           float sum = 0.0f;
 #pragma unroll
-          for (int r = 0; r < kRouterSlots; ++r) {
+          for (int r = 0; r < SLOTS; ++r) {
             ex[r] = 0.0f;
             if (r < K) {
               ex[r] = expf(key_value(best[r]) - mx);
@@ -291,7 +313,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
           }
           const float inv = 1.0f / sum;
 #pragma unroll
-          for (int r = 0; r < kRouterSlots; ++r) {
+          for (int r = 0; r < SLOTS; ++r) {
             if (r < K) {
               const int e = static_cast<int>(0xFFFFu - (best[r] & 0xFFFFu));
               a.topk_idx[static_cast<long long>(row) * K + r] = e;
@@ -329,7 +351,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
       }
       // this buffer's next tile starts from its bias
       const int t2 = t + 2 * gridDim.x;
-      if (t2 < tiles_total) seed_bias<BN>(tmem + lane_base + b * C::kAccStride, a.bias, (t2 % a.tiles_n) * BN, a.N);
+      if (t2 < tiles_total) seed_bias<BN>(tmem + lane_base + acc_col(b), a.bias, (t2 % a.tiles_n) * BN, a.N);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -351,7 +373,7 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
   __syncthreads();
   if constexpr (kRouter) {
     if (a.counts)
-      for (int e = threadIdx.x; e < a.N; e += kLinThreads)
+      for (int e = threadIdx.x; e < a.N; e += C::kThreads)
         if (sb.hist[e]) atomicAdd(a.counts + e, sb.hist[e]);
   }
   if (warp == 1) {
@@ -360,35 +382,50 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
   }
 }
 
-template <int BN, bool kRouter = false>
+template <int BN, int MT, int SLOTS = 0>
 cudaError_t launch_linear_t(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
                             int sms, cudaStream_t stream) {
-  using C = LinCfg<BN>;
+  using C = LinCfg<BN, MT>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_bias_kernel<BN, kRouter>,
+    cudaError_t e = cudaFuncSetAttribute(linear_bias_kernel<BN, MT, SLOTS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int tiles = a.tiles_m * a.tiles_n;
   const int grid = tiles < sms ? tiles : sms;
-  linear_bias_kernel<BN, kRouter><<<grid, kLinThreads, C::kSmem, stream>>>(amap, bmap, a);
+  linear_bias_kernel<BN, MT, SLOTS><<<grid, C::kThreads, C::kSmem, stream>>>(amap, bmap, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+int linear_m_sub(long long m, int n, int block_n, int sms) {
+  return (block_n <= 128 && n <= block_n && (m + kBM - 1) / kBM > sms) ? 2 : 1;
+}
+
+template <int S>
+cudaError_t launch_router_s(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a, int sms,
+                            cudaStream_t stream) {
+  const bool two = a.m_sub == 2;
+  switch (a.block_n) {
+    case 32: return two ? launch_linear_t<32, 2, S>(amap, bmap, a, sms, stream)
+                        : launch_linear_t<32, 1, S>(amap, bmap, a, sms, stream);
+    case 64: return two ? launch_linear_t<64, 2, S>(amap, bmap, a, sms, stream)
+                        : launch_linear_t<64, 1, S>(amap, bmap, a, sms, stream);
+    case 128: return two ? launch_linear_t<128, 2, S>(amap, bmap, a, sms, stream)
+                         : launch_linear_t<128, 1, S>(amap, bmap, a, sms, stream);
+    default: return launch_linear_t<256, 1, S>(amap, bmap, a, sms, stream);
+  }
+}
+
 cudaError_t launch_linear_router(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
                                  int sms, cudaStream_t stream) {
-  switch (a.block_n) {
-    case 32: return launch_linear_t<32, true>(amap, bmap, a, sms, stream);
-    case 64: return launch_linear_t<64, true>(amap, bmap, a, sms, stream);
-    case 128: return launch_linear_t<128, true>(amap, bmap, a, sms, stream);
-    default: return launch_linear_t<256, true>(amap, bmap, a, sms, stream);
-  }
+  return a.top_k <= 4 ? launch_router_s<4>(amap, bmap, a, sms, stream)
+                      : launch_router_s<8>(amap, bmap, a, sms, stream);
 }
 
 int linear_tile_n(int n) {
@@ -408,10 +445,11 @@ int linear_tile_n(int n) {
 cudaError_t launch_linear(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
                           int sms, cudaStream_t stream) {
   switch (a.block_n) {
-    case 128: return launch_linear_t<128>(amap, bmap, a, sms, stream);
-    case 192: return launch_linear_t<192>(amap, bmap, a, sms, stream);
-    case 240: return launch_linear_t<240>(amap, bmap, a, sms, stream);
-    default: return launch_linear_t<256>(amap, bmap, a, sms, stream);
+    case 128: return a.m_sub == 2 ? launch_linear_t<128, 2>(amap, bmap, a, sms, stream)
+                                  : launch_linear_t<128, 1>(amap, bmap, a, sms, stream);
+    case 192: return launch_linear_t<192, 1>(amap, bmap, a, sms, stream);
+    case 240: return launch_linear_t<240, 1>(amap, bmap, a, sms, stream);
+    default: return launch_linear_t<256, 1>(amap, bmap, a, sms, stream);
   }
 }
 

@@ -64,6 +64,27 @@ def test_linear_many_tiles_per_cta_sampled():
     assert sa.sink_attn_device_status(True) == 0
 
 
+@pytest.mark.parametrize("m,n,k", [(24037, 128, 640), (19500, 104, 2880), (20000, 64, 136)])
+def test_linear_skinny_two_subtiles_sampled(m, n, k):
+    """Skinny outputs (one column tile, N <= 128) with more 128-row blocks than SMs take
+    256-row tiles: two 128-row sub-tiles read each W stage.  Rows sampled from both
+    sub-tiles of many tiles and the ragged last tile are checked against the oracle,
+    every row against cuBLAS within the same bound."""
+    sa = require_gpu()
+    d = workloads.make_linear(54, m, n, k)
+    x, w, b = bf16(d["x"]), bf16(d["w"]), bf16(d["bias"])
+    out = sa.linear_bias(x, w, b)
+    rng = np.random.default_rng(8)
+    edge = [0, 127, 128, 255, 256, 383, 384, m - 257, m - 129, m - 128, m - 2, m - 1]
+    rows = np.unique(np.concatenate([rng.choice(m, 80, replace=False), np.array(edge)]))
+    _check(host(out), d["x"], d["w"], d["bias"], rows=rows, what=f"{m}x{n}x{k} two sub-tiles")
+    ref = (x.float() @ w.float().T + b.float()).double()
+    mag = x.float().abs() @ w.float().abs().T
+    bound = 2.0 ** -8 * ref.abs() + 2 * k * 2.0 ** -23 * mag.double()
+    assert bool(((out.double() - ref).abs() <= bound).all())
+    assert sa.sink_attn_device_status(True) == 0
+
+
 def test_linear_bias_is_the_seed():
     """x = 0: every output is exactly the bias (the accumulator starts from it)."""
     sa = require_gpu()

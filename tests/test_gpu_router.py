@@ -138,7 +138,12 @@ def test_router_with_projection_against_the_oracle_router():
 
 
 @pytest.mark.parametrize("t,e,hidden,k", [(2048, 128, 2880, 4), (1000, 32, 2880, 4), (129, 64, 512, 2),
-                                          (300, 256, 256, 8), (1, 128, 2880, 1), (777, 104, 640, 3)])
+                                          (300, 256, 256, 8), (1, 128, 2880, 1), (777, 104, 640, 3),
+                                          # more 128-row blocks than SMs: 256-row tiles (two sub-tiles)
+                                          (24037, 128, 640, 4), (20000, 32, 256, 4), (19500, 64, 512, 2),
+                                          (32768, 128, 2880, 4), (20000, 256, 256, 8),
+                                          # eight slots, six selected
+                                          (1000, 128, 512, 6), (24037, 104, 256, 5)])
 def test_fused_router_is_projection_then_topk(t, e, hidden, k):
     """moe_router (projection with bias seeded in TMEM, bf16 logits, Top-K softmax in the
     epilogue) equals linear_bias followed by moe_router_topk_softmax bit for bit, counts
