@@ -227,6 +227,7 @@ sa_status rope_common(const void* qkv, const void* bias, const int32_t* cu_q, co
   a.max_pages = max_pages;
   a.num_pages = num_pages;
   a.status = status;
+  a.timeout_ns = g_timeout_ns;
   return sa::launch_rope(a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 

@@ -24,6 +24,7 @@ struct RopeArgs {
   float mscale;
   double inv_freq[kMaxRopePairs];
   unsigned* status;
+  unsigned long long timeout_ns;  // bound on the kernel's wait for its input copy
 };
 
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t stream);

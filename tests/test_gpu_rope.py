@@ -58,8 +58,11 @@ def _biased(qkv, bias, hq, hkv):
 
 @pytest.mark.parametrize("plain", [False, True])
 @pytest.mark.parametrize("with_bias", [True, False])
-@pytest.mark.parametrize("hq,hkv", [(64, 8), (4, 1)])
+@pytest.mark.parametrize("hq,hkv", [(64, 8), (4, 1), (120, 4), (48, 8)])
 def test_qkv_bias_rope_contiguous(plain, with_bias, hq, hkv):
+    # A CTA takes the whole tokens that fit 64 KB of qkv rows: 6 at 64/8 heads, 16 (the cap)
+    # at 4/1, 4 at 120/4 (128 head rows, the largest supported), 8 at 48/8; the 323 tokens
+    # leave a partial last CTA in every case.
     sa = require_gpu()
     q_lens = [5, 0, 300, 1, 17]
     kv_lens = np.array([10, 3, 300, 131072, 4000], dtype=np.int32)
