@@ -162,10 +162,15 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
     return;
   }
   for (int tok = lane_tok; tok < ntok; tok += tpar) {
+    // Odd rows read their second half first: the two rows of a quarter-warp then
+    // fall in different banks (bytes [0, 64) and [64, 128) of a row) at each load.
     const uint8_t* src = tile + tok * token_bytes + row * 128 + 16 * j;
+    const int first = (row & 1) * 64;
+    const uint4 u_first = *reinterpret_cast<const uint4*>(src + first);
+    const uint4 u_second = *reinterpret_cast<const uint4*>(src + (64 - first));
     float y1[8], y2[8];
-    widen8(*reinterpret_cast<const uint4*>(src), y1);
-    widen8(*reinterpret_cast<const uint4*>(src + 64), y2);
+    widen8((row & 1) ? u_second : u_first, y1);
+    widen8((row & 1) ? u_first : u_second, y2);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       y1[i] += b1[i];
