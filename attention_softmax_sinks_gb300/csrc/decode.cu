@@ -371,14 +371,46 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 }  // namespace
 
-cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
+// Whether clusters of 16 CTAs of `kern` can be resident on this device (16 is
+// above the portable cluster size of 8); asked once per device and kernel.
+template <typename Kern>
+bool cluster16_schedulable(Kern kern, int nt_index) {
+  static int known[64][2] = {};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  int& k = known[dev][nt_index];
+  if (k == 0) {
+    k = 2;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1, 1);
+      cfg.blockDim = dim3(kWarps * 32, 1, 1);
+      cfg.dynamicSmemBytes = decode_smem_bytes();
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 16;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) k = 1;
+    }
+    cudaGetLastError();  // a refused query leaves no error behind
+  }
+  return k == 1;
+}
+
+cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& args,
                           cudaStream_t stream) {
-  const bool clustered = a.cluster > 1;
-  const dim3 grid(clustered ? a.cluster : a.num_splits, a.hkv, a.batch);
   const size_t smem = decode_smem_bytes();
-  auto kern = a.group <= 8 ? sink_decode_kernel<1> : sink_decode_kernel<2>;
+  auto kern = args.group <= 8 ? sink_decode_kernel<1> : sink_decode_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  DecodeArgs a = args;
+  if (a.cluster > 8 && !cluster16_schedulable(kern, args.group <= 8 ? 0 : 1)) a.cluster = 8;
+  const bool clustered = a.cluster > 1;
+  const dim3 grid(clustered ? a.cluster : a.num_splits, a.hkv, a.batch);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kWarps * 32, 1, 1);

@@ -488,9 +488,10 @@ def bench_long_decode(args, sa, torch, device, pk):
 
 def bench_graph_decode(args, sa, torch, device, pk):
     """Small-batch decode, where launch overhead shows: one sequence of 4096 cached tokens per
-    step (64/8 heads, page 16), decode + merge with the library's split count.  32 steps cycle
-    over 32 different sequences of one permuted page pool (256 MiB of KV, larger than L2), run
-    eagerly and as one captured CUDA graph of the same 32 steps."""
+    step (64/8 heads, page 16) with the library's split count (1 here: one launch whose 16-CTA
+    clusters merge on chip; a count above 1 adds the merge launch).  32 steps cycle over 32
+    different sequences of one permuted page pool (256 MiB of KV, larger than L2), run eagerly
+    and as one captured CUDA graph of the same 32 steps."""
     cfg = DECODE
     nseq, kvl = 32, cfg["kv_len"]
     host = workloads.make_decode(cfg["seed"] + 7, [kvl] * nseq, cfg["hq"], cfg["hkv"], cfg["d"],

@@ -118,7 +118,7 @@ sa_status sink_attn_prefill_paged(const void* q, const void* paged_k, const void
  *  num_splits 1..256.
  *    == 1: out bf16 [batch, num_qo_heads, head_dim], lse fp32
  *          [batch, num_qo_heads] or NULL -- the final result.  The library
- *          may still divide each sequence's KV range among up to 4 CTAs of a
+ *          may still divide each sequence's KV range among up to 16 CTAs of a
  *          thread-block cluster (split 0 carries the sink) and combine their
  *          states on chip through distributed shared memory, in one launch.
  *    >  1: out fp32 [batch, num_splits, num_qo_heads, head_dim] holds each
@@ -183,7 +183,11 @@ sa_status sink_attn_decode_noalloc(const void* q, const void* paged_k, const voi
  * Host-only helper: a split count for sink_attn_decode (fp32 partials, then
  * sink_attn_merge) that fills `num_sms` SMs with about four waves of CTAs
  * while keeping every split at least 16 pages long.  Returns a value in
- * [1, 256].  No CUDA call.
+ * [1, 256].  1 means: call sink_attn_decode with num_splits == 1 (no merge
+ * call); it is returned when batch * num_kv_heads is small enough that
+ * 16-CTA clusters, one per (sequence, KV head), fit one wave of resident CTAs
+ * and the cache has at least 256 pages: the on-chip cluster merge then beats
+ * explicit splits.  No CUDA call.
  */
 int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int page_size,
                             int num_sms);

@@ -142,6 +142,8 @@ def test_decode_split_heuristic(lib):
     assert f(8, 8, 131072, 16, 152) >= 16      # long context spreads over the GPU
     assert f(0, 8, 4096, 16, 152) == 1
     assert f(64, 8, 4096, 16, 152) == 4        # 512 (sequence, KV head) units: four waves
+    assert f(1, 8, 4096, 16, 152) == 1         # 16-CTA clusters fit one wave: on-chip merge
+    assert f(1, 8, 4000, 16, 152) > 1          # fewer than 256 pages: explicit splits
 
 
 def test_router_rejects_before_launch(lib):

@@ -30,14 +30,18 @@ def test_decode_small(hq, hkv, sink_fill):
     assert sa.sink_attn_device_status(True) == 0
 
 
-@pytest.mark.parametrize("batch,kv", [(1, 3000), (2, 777), (16, 2048), (64, 4096), (256, 600)])
-def test_unsplit_decode_with_on_chip_cluster_split(batch, kv):
+@pytest.mark.parametrize("batch,kv,hq,hkv", [(1, 3000, 64, 8), (2, 777, 64, 8), (16, 2048, 64, 8),
+                                             (64, 4096, 64, 8), (256, 600, 64, 8),
+                                             # one wave: clusters of 16 (8 where 16 cannot be resident)
+                                             (1, 4096, 64, 8), (3, 8192, 64, 8), (1, 4096, 64, 4),
+                                             (2, 5000, 32, 8)])
+def test_unsplit_decode_with_on_chip_cluster_split(batch, kv, hq, hkv):
     """num_splits == 1: each sequence's KV range may be split across a CTA cluster
-    (sizes 1..4 depending on the shape) and merged on chip; parity with the oracle
+    (sizes 1..16 depending on the shape) and merged on chip; parity with the oracle
     and with the explicit split + merge path."""
     sa = require_gpu()
     lens = [kv - (7 * b) % 50 for b in range(batch)]
-    d = workloads.make_decode(17, lens, 64, 8, 64)
+    d = workloads.make_decode(17, lens, hq, hkv, 64)
     o, l, args = _run(sa, d, 0.125, 1)
     ro, rl = oracle.decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["kv_lens"],
                            d["sinks"], 0.125, batches=range(min(batch, 16)))
