@@ -558,9 +558,12 @@ def bench_graph_decode(args, sa, torch, device, pk):
 def flush_l2(buf):
     """Evict L2 before a timed launch: write a buffer larger than L2, then read it back.
     The read pushes the written (dirty) lines out to DRAM before the timed region starts
-    and leaves only clean lines, so the timed kernel does not pay for their write-back."""
+    and leaves only clean lines, so the timed kernel does not pay for their write-back.
+    The read sums a float32 view: summing the uint8 buffer itself would first widen it to
+    int64 (a 2 GiB cast copy)."""
+    import torch
     buf.zero_()
-    buf.sum()
+    buf.view(torch.float32).sum()
 
 
 def _timed_flushed(torch, device, stream, fn, reps):
