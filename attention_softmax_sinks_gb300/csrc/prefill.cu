@@ -242,6 +242,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Schedule sc = make_schedule(a);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Launched with programmatic stream serialisation: this CTA may be resident
+  // while the kernel before it on the stream finishes.  The tensor-map
+  // descriptors are kernel parameters, so they are fetched now; every read of an
+  // input comes after the wait.  Dependents may be scheduled at once: they wait
+  // for this whole grid before reading anything, and they can only start when
+  // every CTA of this grid has started.
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&qmap);
+    if (kPersistent) tma_prefetch_desc(&qpmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+  pdl_launch_dependents();
+  pdl_wait_primary();
+
   // ---------------------------------------------------------------- schedule
   const int pairs = a.batch * sc.n_qb;
   int n_items;
@@ -757,7 +772,18 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, co
                       : (persistent ? sink_prefill_kernel<false, true> : sink_prefill_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<blocks, kThreads, smem, stream>>>(qmap, qpmap, kmap, vmap, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, qmap, qpmap, kmap, vmap, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
