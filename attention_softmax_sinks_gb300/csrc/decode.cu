@@ -405,14 +405,18 @@ __global__ void __launch_bounds__(kWarps * 32)
 }  // namespace
 
 // Whether clusters of 16 CTAs of `kern` can be resident on this device (16 is
-// above the portable cluster size of 8); asked once per device and kernel.
+// above the portable cluster size of 8); asked once per device and kernel, never
+// while `stream` is being captured into a graph (the answer is then "no" for that
+// launch, which runs with clusters of 8).
 template <typename Kern>
-bool cluster16_schedulable(Kern kern, int nt_index) {
+bool cluster16_schedulable(Kern kern, int nt_index, cudaStream_t stream) {
   static int known[64][2] = {};  // 0 unknown, 1 yes, 2 no
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   int& k = known[dev][nt_index];
   if (k == 0) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return false;
     k = 2;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
@@ -441,7 +445,7 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   DecodeArgs a = args;
-  if (a.cluster > 8 && !cluster16_schedulable(kern, args.group <= 8 ? 0 : 1)) a.cluster = 8;
+  if (a.cluster > 8 && !cluster16_schedulable(kern, args.group <= 8 ? 0 : 1, stream)) a.cluster = 8;
   const bool clustered = a.cluster > 1;
   const dim3 grid(clustered ? a.cluster : a.num_splits, a.hkv, a.batch);
   cudaLaunchConfig_t cfg = {};
