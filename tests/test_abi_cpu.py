@@ -215,7 +215,7 @@ def test_linear_rejects_before_launch(lib):
 
 def test_library_has_no_unresolved_internal_symbols(lib):
     """Every kernel launcher the C ABI calls is linked in (a missing definition
-    would only show when the library is loaded on the GPU machine)."""
+    would otherwise only show when the library is loaded on a machine with a GPU)."""
     import attention_softmax_sinks_gb300 as sa
     nm = subprocess.run(["nm", "-D", "--undefined-only", sa.library_path()], capture_output=True, text=True)
     if nm.returncode != 0:
