@@ -113,3 +113,70 @@ def test_positive_infinite_sink_everywhere():
                                         dev(m["sinks"]), 20, 0.125)
     assert np.all(host(o2) == 0) and np.all(np.isposinf(host(l2)))
     assert sa.sink_attn_device_status(True) == 0
+
+
+def _sample_rows(cu, hq, seed):
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(len(cu) - 1):
+        if cu[b + 1] == cu[b]:
+            continue
+        for tok in {int(cu[b]), int(cu[b + 1]) - 1, int(rng.integers(cu[b], cu[b + 1]))}:
+            rows.append((tok, int(rng.integers(0, hq))))
+    return rows
+
+
+def test_paged_prefill_beyond_the_on_chip_schedule():
+    """300 sequences of up to 600 new tokens (1500 sequence x query-block pairs, more than
+    the 1024 the persistent schedule sorts on chip): the CTAs fall back to reverse
+    query-block order; decode rows, short chunks and empty sequences mixed, sampled rows
+    of every sequence against the oracle."""
+    sa = require_gpu()
+    rng = np.random.default_rng(47)
+    q_lens = rng.choice([0, 1, 1, 5, 129, 300, 600], 300).tolist()
+    q_lens[7] = 600
+    kv_lens = [q + int(rng.integers(0, 900)) for q in q_lens]
+    kv_lens = [max(k, 1) for k in kv_lens]
+    d = workloads.make_mixed(47, q_lens, kv_lens, 64, 8, 64)
+    o, l = sa.sink_attn_prefill_paged(bf16(d["q"]), bf16(d["k_pages"]), bf16(d["v_pages"]),
+                                      dev(d["page_table"]), dev(d["cu_seqlens_q"]), dev(d["kv_lens"]),
+                                      dev(d["sinks"]), 600, 0.125)
+    rows = _sample_rows(d["cu_seqlens_q"], 64, 48)
+    ro, rl = oracle.prefill_paged(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["cu_seqlens_q"],
+                                  d["kv_lens"], d["sinks"], 0.125, True, rows=rows)
+    go = host(o)[[r[0] for r in rows], [r[1] for r in rows]]
+    gl = host(l)[[r[0] for r in rows], [r[1] for r in rows]]
+    assert_close(go, gl, ro, rl, "paged prefill, 1500 pairs")
+    assert sa.sink_attn_device_status(True) == 0
+
+
+def test_contiguous_prefill_beyond_the_on_chip_schedule():
+    """The same fallback for a ragged contiguous batch: 300 sequences of 1..600 tokens."""
+    sa = require_gpu()
+    rng = np.random.default_rng(49)
+    lens = rng.integers(1, 601, 300).tolist()
+    lens[3] = 600
+    data = workloads.make_prefill(49, lens, 64, 8, 64)
+    o, l = sa.sink_attn_prefill(bf16(data["q"]), bf16(data["k"]), bf16(data["v"]), dev(data["sinks"]),
+                                dev(data["cu_seqlens"]), 600, 0.125)
+    rows = _sample_rows(data["cu_seqlens"], 64, 50)
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"], 0.125, True,
+                            rows=rows)
+    go = host(o)[[r[0] for r in rows], [r[1] for r in rows]]
+    gl = host(l)[[r[0] for r in rows], [r[1] for r in rows]]
+    assert_close(go, gl, ro, rl, "contiguous prefill, 1500 pairs")
+    assert sa.sink_attn_device_status(True) == 0
+
+
+def test_decode_with_the_largest_split_count():
+    """num_splits = 256 (the largest the interface takes) on a 65536-token sequence: 16
+    pages per split, merged; two sequences (one shorter, leaving splits empty) checked."""
+    sa = require_gpu()
+    d = workloads.make_decode(51, [65536, 3000], 64, 8, 64)
+    args = [bf16(d["q"]), bf16(d["k_pages"]), bf16(d["v_pages"]), dev(d["page_table"]),
+            dev(d["kv_lens"]), dev(d["sinks"])]
+    po, pl = sa.sink_attn_decode(*args, 0.125, num_splits=256)
+    o, l = sa.sink_attn_merge(po, pl)
+    ro, rl = oracle.decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["kv_lens"], d["sinks"], 0.125)
+    assert_close(host(o), host(l), ro, rl, "decode, 256 splits")
+    assert sa.sink_attn_device_status(True) == 0
