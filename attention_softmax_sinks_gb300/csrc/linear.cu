@@ -36,8 +36,12 @@
 // low half, so equal logits keep the lower expert first), and writes the K
 // selected experts, their softmax weights (fp32, stored as bf16) and
 // per-expert counts (shared histogram, added to the global counts once per
-// CTA).  The arithmetic is that of the plain layer followed by the
-// standalone router, bit for bit.
+// CTA).  With four slots each group of eight keys is sorted as two quads (five
+// compare-exchanges each), reduced to its top four by a bitonic merge and
+// merged into the list the same way, instead of eight insertions (the epilogue
+// runs after the CTA's last MMA, so its instruction count is exposed).  The
+// arithmetic is that of the plain layer followed by the standalone router, bit
+// for bit.
 #include <cstdint>
 
 #include "linear_args.h"
@@ -116,6 +120,34 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   const uint32_t o = key >> 16;
   const uint32_t bits = (o & 0x8000u) ? (o & 0x7FFFu) : (~o & 0xFFFFu);
   return __uint_as_float(bits << 16);
+}
+
+// Compare-exchange: afterwards a >= b.
+__device__ __forceinline__ void cmpx(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b);
+  b = min(a, b);
+  a = hi;
+}
+
+// Four keys sorted largest first (five compare-exchanges).
+__device__ __forceinline__ void sort4(uint32_t (&x)[4]) {
+  cmpx(x[0], x[1]);
+  cmpx(x[2], x[3]);
+  cmpx(x[0], x[2]);
+  cmpx(x[1], x[3]);
+  cmpx(x[1], x[2]);
+}
+
+// a <- the four largest of a and b, both sorted largest first: max(a[i], b[3 - i]) holds
+// those four as a bitonic sequence, which two rounds of compare-exchanges sort.
+__device__ __forceinline__ void merge4(uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  uint32_t c[4] = {max(a[0], b[3]), max(a[1], b[2]), max(a[2], b[1]), max(a[3], b[0])};
+  cmpx(c[0], c[2]);
+  cmpx(c[1], c[3]);
+  cmpx(c[0], c[1]);
+  cmpx(c[2], c[3]);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) a[r] = c[r];
 }
 
 // Router form: S slots hold the S largest keys (S = 4 serves top_k <= 4, 8 up to 8).
@@ -289,12 +321,36 @@ linear_bias_kernel(const __grid_constant__ CUtensorMap amap, const __grid_consta
           uint32_t r32[32];
           tmem_ld32(acc + c, r32);
           tc_wait_ld();
+          bool whole = c + 32 <= a.N;
+          if constexpr (SLOTS != 4) whole = false;
+          if (whole) {
+            if constexpr (SLOTS == 4) {
+              // 32 keys as four groups of eight: two sorted quads, their top four by a
+              // bitonic merge, merged into the list the same way
 #pragma unroll
-          for (int v = 0; v < 32; ++v) {
-            const int e = c + v;
-            if (e < a.N) {
-              const uint32_t bits = pack_bf16x2(__uint_as_float(r32[v]), 0.0f) & 0xFFFFu;
-              offer<SLOTS>(best, (order16(bits) << 16) | (0xFFFFu - static_cast<uint32_t>(e)));
+              for (int g8 = 0; g8 < 4; ++g8) {
+                uint32_t q[2][4];
+#pragma unroll
+                for (int v = 0; v < 8; v += 2) {
+                  const uint32_t w = pack_bf16x2(__uint_as_float(r32[8 * g8 + v]), __uint_as_float(r32[8 * g8 + v + 1]));
+                  const uint32_t e = static_cast<uint32_t>(c + 8 * g8 + v);
+                  q[v >> 2][v & 3] = (order16(w & 0xFFFFu) << 16) | (0xFFFFu - e);
+                  q[v >> 2][(v & 3) + 1] = (order16(w >> 16) << 16) | (0xFFFFu - e - 1);
+                }
+                sort4(q[0]);
+                sort4(q[1]);
+                merge4(q[0], q[1]);
+                merge4(best, q[0]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) {
+              const int e = c + v;
+              if (e < a.N) {
+                const uint32_t bits = pack_bf16x2(__uint_as_float(r32[v]), 0.0f) & 0xFFFFu;
+                offer<SLOTS>(best, (order16(bits) << 16) | (0xFFFFu - static_cast<uint32_t>(e)));
+              }
             }
           }
         }
