@@ -139,15 +139,18 @@ int sm_count() {
 // one wave (beyond one wave large clusters schedule poorly), every CTA keeping
 // >= 16 pages.  One sequence of 4096 tokens with 8 KV heads: 16-CTA clusters,
 // 7.3 us per captured step against 9.0 us for 16 explicit splits + merge.
-int cluster_split(int units, int max_pages) {
-  const long long slots = 3LL * sm_count();
+// `slots`: resident decode CTAs on the device (3 per SM).
+int cluster_split_for(long long units, long long max_pages, long long slots) {
   int c = 1;
-  while (c < 4 && static_cast<long long>(units) * c < 4 * slots && max_pages / (2 * c) >= 16) c *= 2;
+  while (c < 4 && units * c < 4 * slots && max_pages / (2 * c) >= 16) c *= 2;
   // a grid that fits one wave of resident CTAs even split 8 or 16 ways: larger clusters
-  // (16 is the non-portable size; the launcher falls back to 8 where 16 cannot be resident)
-  while (c < 16 && static_cast<long long>(units) * 2 * c <= slots && max_pages / (2 * c) >= 16) c *= 2;
+  // (16 is the non-portable size; the launcher uses 8 when the clusters of 16 would not
+  // all be resident at once)
+  while (c < 16 && units * 2 * c <= slots && max_pages / (2 * c) >= 16) c *= 2;
   return c;
 }
+
+int cluster_split(int units, int max_pages) { return cluster_split_for(units, max_pages, 3LL * sm_count()); }
 
 // One warp waits on a barrier that nothing will ever complete, with the same
 // bounded wait the attention kernels use, and reports the timeout.
@@ -289,11 +292,17 @@ int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int pag
   const long long units = static_cast<long long>(batch) * num_kv_heads;
   const long long pages = (max_kv_len + page_size - 1) / page_size;
   const long long slots = 3LL * num_sms;  // resident decode CTAs per GPU
-  // few (sequence, KV head) pairs with long caches: num_splits = 1, whose 16-CTA clusters
-  // (one wave) merge on chip, beats explicit splits and a merge launch
-  if (units * 16 <= slots && pages / 16 >= 16) return 1;
+  // num_splits = 1 whenever its clusters (one per (sequence, KV head), merged on chip) fit
+  // one wave of resident CTAs and each CTA keeps at most 256 pages: then the on-chip merge
+  // beats explicit splits and a merge launch (64/8 heads, 4096 tokens: batch 1-8 run
+  // 7.8-15.4 us per step this way against 8.1-20.3 us with the split count below).  Longer
+  // caches want more CTAs than one wave of clusters gives (8 x 131072: 332 us with clusters
+  // of 4 against 312 us with 32 splits).
+  const int c = cluster_split_for(units, pages, slots);
+  if (units * c <= slots && pages <= 256LL * c) return 1;
   long long s = (4 * slots + units - 1) / units;  // about four waves of CTAs
-  const long long max_by_pages = pages / 16 > 0 ? pages / 16 : 1;  // >= 16 pages per split
+  // >= 32 pages per split (batch 16 x 4096 tokens: 8 splits 28.1 us, 16 splits 31.6 us)
+  const long long max_by_pages = pages / 32 > 0 ? pages / 32 : 1;
   if (s > max_by_pages) s = max_by_pages;
   if (s < 1) s = 1;
   if (s > 256) s = 256;

@@ -404,20 +404,20 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 }  // namespace
 
-// Whether clusters of 16 CTAs of `kern` can be resident on this device (16 is
-// above the portable cluster size of 8); asked once per device and kernel, never
-// while `stream` is being captured into a graph (the answer is then "no" for that
-// launch, which runs with clusters of 8).
+// How many clusters of 16 CTAs of `kern` can be resident at once on this device
+// (16 is above the portable cluster size of 8); asked once per device and kernel,
+// never while `stream` is being captured into a graph (the answer is then 0 for
+// that launch, which runs with clusters of 8).
 template <typename Kern>
-bool cluster16_schedulable(Kern kern, int nt_index, cudaStream_t stream) {
-  static int known[64][2] = {};  // 0 unknown, 1 yes, 2 no
+int cluster16_capacity(Kern kern, int nt_index, cudaStream_t stream) {
+  static int known[64][2] = {};  // 0 unknown, else 1 + the number of resident clusters
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   int& k = known[dev][nt_index];
   if (k == 0) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return false;
-    k = 2;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return 0;
+    k = 1;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16, 1, 1);
@@ -431,11 +431,11 @@ bool cluster16_schedulable(Kern kern, int nt_index, cudaStream_t stream) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) k = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) k = 1 + n;
     }
     cudaGetLastError();  // a refused query leaves no error behind
   }
-  return k == 1;
+  return k - 1;
 }
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& args,
@@ -445,7 +445,11 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   DecodeArgs a = args;
-  if (a.cluster > 8 && !cluster16_schedulable(kern, args.group <= 8 ? 0 : 1, stream)) a.cluster = 8;
+  // clusters of 16 only while all of them can be resident at once (one per (sequence,
+  // KV head)); beyond that, waiting clusters cost more than the larger split saves
+  if (a.cluster > 8 &&
+      static_cast<long long>(a.batch) * a.hkv > cluster16_capacity(kern, args.group <= 8 ? 0 : 1, stream))
+    a.cluster = 8;
   const bool clustered = a.cluster > 1;
   const dim3 grid(clustered ? a.cluster : a.num_splits, a.hkv, a.batch);
   cudaLaunchConfig_t cfg = {};

@@ -182,11 +182,11 @@ sa_status sink_attn_decode_noalloc(const void* q, const void* paged_k, const voi
 /*
  * Host-only helper: a split count for sink_attn_decode (fp32 partials, then
  * sink_attn_merge) that fills `num_sms` SMs with about four waves of CTAs
- * while keeping every split at least 16 pages long.  Returns a value in
+ * while keeping every split at least 32 pages long.  Returns a value in
  * [1, 256].  1 means: call sink_attn_decode with num_splits == 1 (no merge
- * call); it is returned when batch * num_kv_heads is small enough that
- * 16-CTA clusters, one per (sequence, KV head), fit one wave of resident CTAs
- * and the cache has at least 256 pages: the on-chip cluster merge then beats
+ * call); it is returned when the clusters that call would use, one per
+ * (sequence, KV head), fit one wave of resident CTAs (3 per SM) and each of
+ * their CTAs keeps at most 256 pages: the on-chip cluster merge then beats
  * explicit splits.  No CUDA call.
  */
 int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int page_size,

@@ -132,18 +132,22 @@ def test_merge_rejects(lib):
 
 def test_decode_split_heuristic(lib):
     f = lib.sink_attn_decode_splits
-    # every result is within [1, 256] and keeps >= 16 pages per split
+    # every result is within [1, 256] and keeps >= 32 pages per split
     for b, hkv, kv in [(1, 8, 131072), (8, 8, 131072), (64, 8, 4096), (256, 8, 512), (1, 1, 1)]:
         s = f(b, hkv, kv, 16, 152)
         assert 1 <= s <= 256
         pages = (kv + 15) // 16
-        assert s == 1 or pages // s >= 16
+        assert s == 1 or pages // s >= 32
     assert f(1, 8, 16, 16, 152) == 1           # a single page cannot be split
     assert f(8, 8, 131072, 16, 152) >= 16      # long context spreads over the GPU
     assert f(0, 8, 4096, 16, 152) == 1
     assert f(64, 8, 4096, 16, 152) == 4        # 512 (sequence, KV head) units: four waves
     assert f(1, 8, 4096, 16, 152) == 1         # 16-CTA clusters fit one wave: on-chip merge
-    assert f(1, 8, 4000, 16, 152) > 1          # fewer than 256 pages: explicit splits
+    assert f(1, 8, 4000, 16, 152) == 1         # 250 pages: clusters of 8, still one wave
+    assert f(8, 8, 4096, 16, 152) == 1         # 64 units x clusters of 4 = 256 CTAs
+    assert f(16, 8, 4096, 16, 152) == 8        # clusters would exceed one wave: 8 splits of 32 pages
+    assert f(8, 8, 131072, 16, 152) >= 16      # long caches: more CTAs than one wave of clusters
+    assert f(1, 8, 131072, 16, 152) > 1
 
 
 def test_router_rejects_before_launch(lib):
