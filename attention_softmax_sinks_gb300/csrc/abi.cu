@@ -400,8 +400,9 @@ static sa_status prefill_common(const void* q, const void* k, const void* v,
   a.scale_log2 = sm_scale * kLog2e;
   a.timeout_ns = g_timeout_ns;
   if (sa_status s = status_ptr(&a.status)) return s;
-  CUtensorMap qm, qpm, km, vm;
+  CUtensorMap qm, qpm, km, vm, om;
   if (sa_status s = map_tokens_heads(&qm, q, total_q, hq, 128)) return s;
+  if (sa_status s = map_tokens_heads(&om, out, total_q, hq, 128)) return s;
   // packed short sequences (G = 4, 8, 16): boxes of 128 / G tokens x the G heads of a group
   const int group = hq / hkv;
   if (group >= 4 && 128 % group == 0) {
@@ -416,7 +417,7 @@ static sa_status prefill_common(const void* q, const void* k, const void* v,
     if (sa_status s = map_tokens_heads(&km, k, total_q, hkv, 128)) return s;
     if (sa_status s = map_tokens_heads(&vm, v, total_q, hkv, 128)) return s;
   }
-  return sa::launch_prefill(qm, qpm, km, vm, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+  return sa::launch_prefill(qm, qpm, km, vm, om, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
 sa_status sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks,

@@ -51,7 +51,10 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
                           cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 // qpmap: Q in boxes of (128 / group tokens, group heads), used for packed short sequences.
+// omap: the output [T, Hq, 64] mapped like qmap (boxes of 128 tokens x 1 head); full query
+// blocks are written through it with TMA stores.
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t stream);
+                           const CUtensorMap& vmap, const CUtensorMap& omap, const PrefillArgs& a,
+                           cudaStream_t stream);
 
 }  // namespace sa

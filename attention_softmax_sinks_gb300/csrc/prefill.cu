@@ -64,7 +64,8 @@ struct __align__(1024) PrefillSmem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint64_t q_full[2];           // Q of the item landed                         (TMA tx)
-  uint64_t q_empty[2];          // every S of the item has read its Q           (1 commit per tile)
+  uint64_t q_empty[2];          // the item's Q buffers are free again: its MMAs are done and the
+                                //   output staged there has been read by the TMA (1 arrival per tile)
   uint64_t kv_full[kStages];    // K_j and V_j landed                           (TMA tx)
   uint64_t kv_empty[kStages];   // every query tile's MMAs on the stage finished (1 commit per tile)
   uint64_t s_full[2];           // S_t(j) is in TMEM                             (tcgen05.commit)
@@ -73,6 +74,7 @@ struct __align__(1024) PrefillSmem {
   uint64_t pv_done[2];          // O_t += P_t(j) V_j completed                   (tcgen05.commit)
   uint64_t o_free[2];           // softmax warpgroup t has read O_t of its item  (128 arrivals)
   uint64_t drain[2];
+  uint64_t stage_full[2];       // every row of tile t's output box is staged   (128 arrivals)
   int n_pairs;                  // pairs with work (a prefix of sortkey)
   int sorted;                   // 0 when the items are in reverse query-block order
   uint32_t tmem_base;
@@ -128,6 +130,16 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t
   }
 }
 
+// TMA store of one box of the 3D tensor map `map` from this CTA's shared memory
+// (128-byte swizzled rows), tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+               "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared memory of every committed store has been read (may be overwritten)
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 struct WorkItem {
   int b, h0, q0, q_start, q_len, kv_len, n_kv;
   int kvh;     // KV head of the item
@@ -235,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sink_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                         const __grid_constant__ CUtensorMap qpmap,
                         const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+                        const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -253,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPersistent) tma_prefetch_desc(&qpmap);
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&omap);
   }
   pdl_launch_dependents();
   pdl_wait_primary();
@@ -390,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.pv_done[t]), 1);
       mbar_init(smem_u32(&sm.o_free[t]), 128);
       mbar_init(smem_u32(&sm.drain[t]), 1);
+      mbar_init(smem_u32(&sm.stage_full[t]), 128);
     }
     sm.abort_flag = 0;
     sm.issued_kv = 0;
@@ -564,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (ok) pv_step(w.n_kv - 1);
-          if (ok && kPersistent) tc_commit(smem_u32(&sm.q_empty[qb]));  // every S of the item issued
+          // Q_t of the item is released by the softmax warpgroup once its epilogue is done
+          // with the buffer (it stages the output there)
           return ok;
         });
         if (!ok) raise_status(a.status, kStatusTimeout);
@@ -586,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t p_col = lane_base + kColP + t * 64;
       const uint64_t scale2 = f2(a.scale_log2, a.scale_log2);
       bool ok = true;
+      int n_staged = 0;  // output boxes this warpgroup has staged (stage_full phase)
       for_items([&](const WorkItem& w, int it, int g) {
         // head and query index (within the sequence) of TMEM lane r
         const int h = w.packed ? w.h0 + r % a.group : w.h0 + t;
@@ -694,31 +711,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool row_ok = i < w.q_len;
         const float inv = d > 0.0f ? 1.0f / d : 0.0f;
-        uint16_t* out = static_cast<uint16_t*>(a.out) +
-                        (static_cast<size_t>(w.q_start + i) * a.hq + h) * kHeadDim;
+        uint32_t ou[2][32];
+        tmem_ld32(o_col, ou[0]);
+        tmem_ld32(o_col + 32, ou[1]);
+        tc_wait_ld();
+        if (kPersistent) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.o_free[t]));  // the next item's first PV may overwrite O_t
+        }
+        auto chunk = [&](int c) {  // output columns [8c, 8c + 8) of this row as bf16
+          const uint32_t* u = ou[c >> 2] + 8 * (c & 3);
+          return make_uint4(pack_bf16x2(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv),
+                            pack_bf16x2(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv),
+                            pack_bf16x2(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv),
+                            pack_bf16x2(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv));
+        };
+        // In the persistent kernel a full query block of one head leaves through a TMA store:
+        // the rows are staged in this item's Q_t buffer (every MMA that read it has completed)
+        // with the 128-byte swizzle of the output map, then one thread stores the 128 x 64 box
+        // while the warpgroup moves on to the next item.  Row by row the output of one head is
+        // 8 KB apart, so direct stores touch 32 lines per warp instruction and hold up the
+        // next item's softmax.  Partial and packed blocks, whose boxes would reach other rows,
+        // store directly, and so does the one-item CTA, whose posted stores retire while the
+        // next CTA starts (staging would keep it resident until the copy has read the tile).
+        const bool staged = kPersistent && !w.packed && w.q0 + kBlockQ <= w.q_len;  // warpgroup-uniform
+        if (staged) {
+          uint8_t* stage = q_tile(sm, it & 1, t) + r * 128;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t u[32];
-          tmem_ld32(o_col + c * 32, u);
-          tc_wait_ld();
-          if (kPersistent && c == 1) {
-            tc_fence_before();
-            mbar_arrive(smem_u32(&sm.o_free[t]));  // the next item's first PV may overwrite O_t
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(stage + ((c ^ (r & 7)) << 4)) = chunk(c);
+          fence_proxy_async_smem();  // visible to the TMA (async proxy)
+          mbar_arrive(smem_u32(&sm.stage_full[t]));
+          if (qw == 0 && lane == 0) {  // bounded wait for the warpgroup's 128 rows
+            if (!wait_bar(smem_u32(&sm.stage_full[t]), n_staged & 1, a.timeout_ns, abort_flag)) return ok = false;
+            tma_store_3d(&omap, smem_u32(q_tile(sm, it & 1, t)), 0, h, w.q_start + w.q0);
+            bulk_commit();
+            bulk_wait_read();  // the buffer may be reused (or released) once the TMA has read it;
+                               // the writes themselves complete by the end of the grid
           }
-          if (row_ok) {
+          ++n_staged;
+        } else if (row_ok) {
+          uint16_t* out = static_cast<uint16_t*>(a.out) +
+                          (static_cast<size_t>(w.q_start + i) * a.hq + h) * kHeadDim;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint4 pk4;
-              pk4.x = pack_bf16x2(__uint_as_float(u[8 * e + 0]) * inv, __uint_as_float(u[8 * e + 1]) * inv);
-              pk4.y = pack_bf16x2(__uint_as_float(u[8 * e + 2]) * inv, __uint_as_float(u[8 * e + 3]) * inv);
-              pk4.z = pack_bf16x2(__uint_as_float(u[8 * e + 4]) * inv, __uint_as_float(u[8 * e + 5]) * inv);
-              pk4.w = pack_bf16x2(__uint_as_float(u[8 * e + 6]) * inv, __uint_as_float(u[8 * e + 7]) * inv);
-              reinterpret_cast<uint4*>(out + c * 32)[e] = pk4;
-            }
-          }
+          for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(out)[c] = chunk(c);
         }
         if (row_ok && a.lse)
           a.lse[static_cast<size_t>(w.q_start + i) * a.hq + h] = d > 0.0f ? (m + lg2(d)) * kLn2 : kNegInf;
+        if (kPersistent && qw == 0 && lane == 0) mbar_arrive(smem_u32(&sm.q_empty[it & 1]));
         return true;
       });
       if (!ok) raise_status(a.status, kStatusTimeout);
@@ -746,7 +785,8 @@ int g_prefill_sms[64] = {};
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t stream) {
+                           const CUtensorMap& vmap, const CUtensorMap& omap, const PrefillArgs& a,
+                           cudaStream_t stream) {
   const int tiles = (a.group % 2 == 0) ? 2 : 1;
   const int n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
   const long long items = static_cast<long long>(n_qb) * (a.hq / tiles) * a.batch;
@@ -782,7 +822,7 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, qmap, qpmap, kmap, vmap, a);
+  e = cudaLaunchKernelEx(&cfg, kern, qmap, qpmap, kmap, vmap, omap, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
