@@ -130,10 +130,23 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
 
+  // Page ids, 32 of this warp's pages at a time: lane l of ids_cur holds the id of the
+  // warp's page 32 w + l (window w holds the page being consumed) and ids_next those of
+  // window w + 1, read a whole window ahead, so no page-table read sits in the loop.
+  auto load_ids = [&](int w) {
+    const int jj = w * 32 + lane;
+    return jj < my_count ? ptab[my_first + jj * kWarps] : -1;
+  };
+  int ids_cur = load_ids(0);
+  int ids_next = load_ids(1);
+  auto id_of = [&](int k, int w) {  // all lanes; page k lies in window w or w + 1
+    const int in_cur = __shfl_sync(0xffffffffu, ids_cur, k & 31);
+    const int in_next = __shfl_sync(0xffffffffu, ids_next, k & 31);
+    return (k >> 5) == w ? in_cur : in_next;
+  };
+
   const uint64_t policy = l2_policy_evict_first();
-  auto issue = [&](int j) {  // lane 0 only
-    const int pg = my_first + j * kWarps;
-    const int phys = ptab[pg];
+  auto issue = [&](int j, int phys) {  // lane 0 only
     const uint32_t bar = full_w + 8 * (j % kStages);
     if (phys < 0 || phys >= a.num_pages) {
       raise_status(a.status, kStatusBadPage);
@@ -147,8 +160,13 @@ __global__ void __launch_bounds__(kWarps * 32)
     tma_load_2d(dst + kPageBytes, &vmap, 0, row, bar, policy);
   };
   int issued = min(kStages, my_count);  // meaningful on lane 0
-  if (lane == 0)
-    for (int j = 0; j < issued; ++j) issue(j);
+  {
+    int first_ids[kStages];
+#pragma unroll
+    for (int jj = 0; jj < kStages; ++jj) first_ids[jj] = id_of(jj, 0);
+    if (lane == 0)
+      for (int jj = 0; jj < issued; ++jj) issue(jj, first_ids[jj]);
+  }
 
   // Q^T fragments (B operand of S^T = K Q^T): lane holds head (lane/4) of each
   // 8-wide tile, dims kk*16 + 2*(lane%4) + {0,1} and +8.
@@ -190,13 +208,18 @@ __global__ void __launch_bounds__(kWarps * 32)
   bool timed_out = false;
   int j = 0;
   for (; j < my_count; ++j) {
+    const int win = j >> 5;
+    if ((j & 31) == 0 && j > 0) {  // entering window win: its ids are loaded, fetch the next
+      ids_cur = ids_next;
+      ids_next = load_ids(win + 1);
+    }
     const int slot = j % kStages;
     if (!mbar_wait(full_w + 8 * slot, (j / kStages) & 1, a.timeout_ns)) {
       timed_out = true;
       break;
     }
     const int pg = my_first + j * kWarps;
-    const int phys = ptab[pg];
+    const int phys = id_of(j, win);
     if (phys >= 0 && phys < a.num_pages) {
       const uint32_t kb = ring_w + slot * kSlotBytes;
       const uint32_t vb = kb + kPageBytes;
@@ -265,8 +288,9 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
     }
     __syncwarp();
+    const int next_phys = id_of(j + kStages, win);
     if (lane == 0 && j + kStages < my_count) {
-      issue(j + kStages);
+      issue(j + kStages, next_phys);
       ++issued;
     }
   }
