@@ -293,14 +293,20 @@ int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int pag
   const long long pages = (max_kv_len + page_size - 1) / page_size;
   const long long slots = 3LL * num_sms;  // resident decode CTAs per GPU
   // num_splits = 1 whenever its clusters (one per (sequence, KV head), merged on chip) fit
-  // one wave of resident CTAs and each CTA keeps at most 256 pages: then the on-chip merge
+  // one wave of resident CTAs and each CTA keeps at most 96 pages: then the on-chip merge
   // beats explicit splits and a merge launch (64/8 heads, 4096 tokens: batch 1-8 run
-  // 7.8-15.4 us per step this way against 8.1-20.3 us with the split count below).  Longer
-  // caches want more CTAs than one wave of clusters gives (8 x 131072: 332 us with clusters
-  // of 4 against 312 us with 32 splits).
+  // 7.8-15.4 us per step this way against 8.1-20.3 us with the split count below; one
+  // sequence of 16384 tokens, 64 pages per CTA: 14.7 against 15.1 us).  With more pages
+  // per CTA a warp's page walk is too long (one sequence of 32768 / 65536 tokens: 24.1 /
+  // 42.6 us with clusters of 16 against 20.0 / 29.9 us with 32 splits).
   const int c = cluster_split_for(units, pages, slots);
-  if (units * c <= slots && pages <= 256LL * c) return 1;
-  long long s = (4 * slots + units - 1) / units;  // about four waves of CTAs
+  if (units * c <= slots && pages <= 96LL * c) return 1;
+  // Few units: about 5/3 CTAs per SM in all (batch 1 / 2 / 4 at 65536-131072 tokens: 32 /
+  // 16 / 8 splits were best or within 3% of it; one 131072-token sequence took 50.5 us so,
+  // 84 us with four waves of CTAs).  Otherwise about four waves of CTAs (8 x 131072:
+  // 312 us with 32 splits against 332 us with clusters of 4).
+  const long long few = 5LL * num_sms / 3;
+  long long s = units < 64 ? (few + units - 1) / units : (4 * slots + units - 1) / units;
   // >= 32 pages per split (batch 16 x 4096 tokens: 8 splits 28.1 us, 16 splits 31.6 us)
   const long long max_by_pages = pages / 32 > 0 ? pages / 32 : 1;
   if (s > max_by_pages) s = max_by_pages;

@@ -181,12 +181,13 @@ sa_status sink_attn_decode_noalloc(const void* q, const void* paged_k, const voi
 
 /*
  * Host-only helper: a split count for sink_attn_decode (fp32 partials, then
- * sink_attn_merge) that fills `num_sms` SMs with about four waves of CTAs
- * while keeping every split at least 32 pages long.  Returns a value in
+ * sink_attn_merge).  With fewer than 64 (sequence, KV head) units it aims at
+ * about 5/3 CTAs per SM in all, otherwise at about four waves of resident
+ * CTAs, keeping every split at least 32 pages long.  Returns a value in
  * [1, 256].  1 means: call sink_attn_decode with num_splits == 1 (no merge
  * call); it is returned when the clusters that call would use, one per
  * (sequence, KV head), fit one wave of resident CTAs (3 per SM) and each of
- * their CTAs keeps at most 256 pages: the on-chip cluster merge then beats
+ * their CTAs keeps at most 96 pages: the on-chip cluster merge then beats
  * explicit splits.  No CUDA call.
  */
 int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int page_size,

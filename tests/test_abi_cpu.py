@@ -148,6 +148,12 @@ def test_decode_split_heuristic(lib):
     assert f(16, 8, 4096, 16, 152) == 8        # clusters would exceed one wave: 8 splits of 32 pages
     assert f(8, 8, 131072, 16, 152) >= 16      # long caches: more CTAs than one wave of clusters
     assert f(1, 8, 131072, 16, 152) > 1
+    assert f(1, 8, 16384, 16, 152) == 1        # 64 pages per CTA of a 16-CTA cluster
+    assert f(1, 8, 32768, 16, 152) == 32       # 128 pages per cluster CTA: ~5/3 CTAs per SM instead
+    assert f(1, 8, 131072, 16, 152) == 32
+    assert f(2, 8, 65536, 16, 152) == 16
+    assert f(4, 8, 131072, 16, 152) == 8
+    assert f(8, 8, 131072, 16, 152) == 29      # 64 units: about four waves
 
 
 def test_router_rejects_before_launch(lib):
