@@ -205,50 +205,78 @@ __global__ void __launch_bounds__(kWarps * 32)
       for (int r = 0; r < 4; ++r) o[nt][mt][r] = 0.0f;
   }
 
+  // S^T = K Q^T of the page in ring slot `slot` (16 tokens x 8 heads per tile)
+  auto scores = [&](int slot, float (&sc)[NT][4]) {
+    const uint32_t kb = ring_w + slot * kSlotBytes;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sc[nt][r] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int chunk = kk * 2 + (lane >> 4);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kb + row * 128 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+    }
+  };
+  // O^T += V^T P^T for the page in ring slot `slot` (64 dims x 8 heads per tile)
+  auto accumulate = [&](int slot, const uint32_t (&pt)[NT][2]) {
+    const uint32_t vb = ring_w + slot * kSlotBytes + kPageBytes;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int tok = (lane & 7) + (lane >> 4) * 8;
+      const int chunk = mt * 2 + ((lane >> 3) & 1);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_trans(vb + tok * 128 + ((chunk ^ (tok & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, pt[nt][0], pt[nt][1]);
+    }
+  };
+
+  // Two pages per step: their score products are independent, and one max reduction and
+  // one rescale serve both, so a warp's serial chain per page is about halved.
   bool timed_out = false;
   int j = 0;
-  for (; j < my_count; ++j) {
-    const int win = j >> 5;
+  for (; j < my_count; j += 2) {
+    const int win = j >> 5;  // j is even: page j + 1 lies in the same window
     if ((j & 31) == 0 && j > 0) {  // entering window win: its ids are loaded, fetch the next
       ids_cur = ids_next;
       ids_next = load_ids(win + 1);
     }
-    const int slot = j % kStages;
-    if (!mbar_wait(full_w + 8 * slot, (j / kStages) & 1, a.timeout_ns)) {
+    const bool two = j + 1 < my_count;
+    if (!mbar_wait(full_w + 8 * (j % kStages), (j / kStages) & 1, a.timeout_ns) ||
+        (two && !mbar_wait(full_w + 8 * ((j + 1) % kStages), ((j + 1) / kStages) & 1, a.timeout_ns))) {
       timed_out = true;
       break;
     }
-    const int pg = my_first + j * kWarps;
-    const int phys = id_of(j, win);
-    if (phys >= 0 && phys < a.num_pages) {
-      const uint32_t kb = ring_w + slot * kSlotBytes;
-      const uint32_t vb = kb + kPageBytes;
-      // ---- S^T = K Q^T (16 tokens x 8 heads per tile)
-      float s[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) s[nt][r] = 0.0f;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int chunk = kk * 2 + (lane >> 4);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(kb + row * 128 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
-      }
-      // ---- scale, mask the ragged tail, online softmax update
-      const int tok0 = pg * kPageSize + (lane >> 2);
-      const bool v0 = tok0 < kv_len, v1 = tok0 + 8 < kv_len;
-      uint32_t pb[NT][2];
+    const int phys_a = id_of(j, win), phys_b = id_of(j + 1, win);
+    const bool use_a = phys_a >= 0 && phys_a < a.num_pages;
+    const bool use_b = two && phys_b >= 0 && phys_b < a.num_pages;
+    if (use_a || use_b) {
+      float sa[NT][4], sb[NT][4];
+      if (use_a) scores(j % kStages, sa);
+      if (use_b) scores((j + 1) % kStages, sb);
+      // ---- scale, mask the ragged tail (and a skipped page), online softmax update
+      const int tok_a = (my_first + j * kWarps) * kPageSize + (lane >> 2);
+      const int tok_b = tok_a + kWarps * kPageSize;
+      const bool a0v = use_a && tok_a < kv_len, a1v = use_a && tok_a + 8 < kv_len;
+      const bool b0v = use_b && tok_b < kv_len, b1v = use_b && tok_b + 8 < kv_len;
+      uint32_t pta[NT][2], ptb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float x0 = v0 ? s[nt][0] * a.scale_log2 : kNegInf;
-        float x1 = v0 ? s[nt][1] * a.scale_log2 : kNegInf;
-        float x2 = v1 ? s[nt][2] * a.scale_log2 : kNegInf;
-        float x3 = v1 ? s[nt][3] * a.scale_log2 : kNegInf;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        const float xa0 = a0v ? sa[nt][0] * a.scale_log2 : kNegInf;
+        const float xa1 = a0v ? sa[nt][1] * a.scale_log2 : kNegInf;
+        const float xa2 = a1v ? sa[nt][2] * a.scale_log2 : kNegInf;
+        const float xa3 = a1v ? sa[nt][3] * a.scale_log2 : kNegInf;
+        const float xb0 = b0v ? sb[nt][0] * a.scale_log2 : kNegInf;
+        const float xb1 = b0v ? sb[nt][1] * a.scale_log2 : kNegInf;
+        const float xb2 = b1v ? sb[nt][2] * a.scale_log2 : kNegInf;
+        const float xb3 = b1v ? sb[nt][3] * a.scale_log2 : kNegInf;
+        float mx0 = fmaxf(fmaxf(xa0, xa2), fmaxf(xb0, xb2));
+        float mx1 = fmaxf(fmaxf(xa1, xa3), fmaxf(xb1, xb3));
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -261,10 +289,12 @@ __global__ void __launch_bounds__(kWarps * 32)
         const float c1 = m[nt][1] == mn1 ? 1.0f : ex2(m[nt][1] - mu1);
         m[nt][0] = mn0;
         m[nt][1] = mn1;
-        const float p0 = ex2(x0 - mu0), p1 = ex2(x1 - mu1);
-        const float p2 = ex2(x2 - mu0), p3 = ex2(x3 - mu1);
-        dsum[nt][0] = dsum[nt][0] * c0 + (p0 + p2);
-        dsum[nt][1] = dsum[nt][1] * c1 + (p1 + p3);
+        const float pa0 = ex2(xa0 - mu0), pa1 = ex2(xa1 - mu1);
+        const float pa2 = ex2(xa2 - mu0), pa3 = ex2(xa3 - mu1);
+        const float pb0 = ex2(xb0 - mu0), pb1 = ex2(xb1 - mu1);
+        const float pb2 = ex2(xb2 - mu0), pb3 = ex2(xb3 - mu1);
+        dsum[nt][0] = dsum[nt][0] * c0 + ((pa0 + pa2) + (pb0 + pb2));
+        dsum[nt][1] = dsum[nt][1] * c1 + ((pa1 + pa3) + (pb1 + pb3));
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           o[nt][mt][0] *= c0;
@@ -273,25 +303,25 @@ __global__ void __launch_bounds__(kWarps * 32)
           o[nt][mt][3] *= c1;
         }
         // P^T as the B operand of O^T += V^T P^T: transpose the two 8x8 blocks
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+        pta[nt][0] = movmatrix_trans(pack_bf16x2(pa0, pa1));
+        pta[nt][1] = movmatrix_trans(pack_bf16x2(pa2, pa3));
+        ptb[nt][0] = movmatrix_trans(pack_bf16x2(pb0, pb1));
+        ptb[nt][1] = movmatrix_trans(pack_bf16x2(pb2, pb3));
       }
-      // ---- O^T += V^T P^T (64 dims x 8 heads per tile)
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int tok = (lane & 7) + (lane >> 4) * 8;
-        const int chunk = mt * 2 + ((lane >> 3) & 1);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(vb + tok * 128 + ((chunk ^ (tok & 7)) << 4), a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-      }
+      if (use_a) accumulate(j % kStages, pta);
+      if (use_b) accumulate((j + 1) % kStages, ptb);
     }
     __syncwarp();
-    const int next_phys = id_of(j + kStages, win);
-    if (lane == 0 && j + kStages < my_count) {
-      issue(j + kStages, next_phys);
-      ++issued;
+    const int next_a = id_of(j + kStages, win), next_b = id_of(j + kStages + 1, win);
+    if (lane == 0) {
+      if (j + kStages < my_count) {
+        issue(j + kStages, next_a);
+        ++issued;
+      }
+      if (j + kStages + 1 < my_count) {
+        issue(j + kStages + 1, next_b);
+        ++issued;
+      }
     }
   }
 
