@@ -9,7 +9,9 @@
 //  * one CTA per (split, kv head, sequence); its 4 warps walk the split's
 //    pages interleaved, each with a private 4-deep ring of TMA page loads
 //    (one 2 KiB K box + one 2 KiB V box per page, 128-byte swizzle, L2
-//    evict-first), so no CTA-wide barrier sits in the streaming loop;
+//    evict-first), so no CTA-wide barrier sits in the streaming loop; a warp
+//    consumes two pages per step (one max reduction and one rescale for both)
+//    and keeps the page ids of its next 32 pages in registers;
 //  * the whole GQA group of a KV head is one 8-wide MMA "N" tile: scores are
 //    computed transposed, S^T[16 tok x 8 heads] = K_page . Q^T, and the PV
 //    product as O^T[64 x 8] += V^T . P^T, so mma.sync m16n8k16 runs with no
