@@ -39,6 +39,35 @@ def test_bad_page_id_decode_is_reported():
     _decode_ok(sa)
 
 
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_skips_a_bad_page_and_keeps_the_rest(splits):
+    """A page id outside the cache is skipped and flagged; every other key still counts.
+    Decode attention does not depend on the order of the keys, so the result must equal
+    the oracle over the same cache with that page removed.  Odd page counts (37, 22) leave
+    a warp's last pair with a single page; the bad page sits inside a pair."""
+    sa = require_gpu()
+    sa.sink_attn_device_status(True)
+    kv = np.array([16 * 37, 16 * 21 + 5], dtype=np.int32)
+    d = workloads.make_decode(8, kv.tolist(), 64, 8, 64)
+    table = d["page_table"].copy()
+    table[0, 10] = d["num_pages"] + 3
+    args = (bf16(d["q"]), bf16(d["k_pages"]), bf16(d["v_pages"]), dev(table), dev(d["kv_lens"]),
+            dev(d["sinks"]), 0.125)
+    if splits > 1:
+        po, pl = sa.sink_attn_decode(*args, num_splits=splits)
+        o, l = sa.sink_attn_merge(po, pl)
+    else:
+        o, l = sa.sink_attn_decode(*args)
+    assert sa.sink_attn_device_status(True) == SA_ERR_BOUNDS
+    ref_table = d["page_table"].copy()
+    kept = np.delete(ref_table[0], 10)
+    ref_table[0, :kept.shape[0]] = kept
+    ref_kv = d["kv_lens"].copy()
+    ref_kv[0] -= 16
+    ro, rl = oracle.decode(d["q"], d["k_pages"], d["v_pages"], ref_table, ref_kv, d["sinks"], 0.125)
+    assert_close(host(o), host(l), ro, rl, f"decode with a skipped page, {splits} split(s)")
+
+
 def test_bad_lengths_are_reported():
     sa = require_gpu()
     sa.sink_attn_device_status(True)
