@@ -63,6 +63,59 @@ constexpr size_t decode_smem_bytes() {
   return 1024 /*alignment slack*/ + kRingBytes + kWarps * kStages * sizeof(uint64_t);
 }
 
+// Merge of a cluster's CTA states, kept out of line so that the streaming loop's code is
+// the same whether or not a launch uses clusters.
+// Every rank merges an equal share of the (head, 4-dim chunk) outputs.  A group of
+// `csz` consecutive lanes takes one output; lane s of the group reads CTA s's state
+// (one round of distributed-shared-memory loads) and the group combines by shuffles.
+template <int NT>
+__device__ __noinline__ void cluster_merge(CtaState<NT>* cs, int csz, void* out_bf16, float* lse_out,
+                                          int hq, int b, int kvh, int G) {
+  {
+    // csz = 2, 4, 8 or 16: a group never straddles a warp
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int n_out = G * 16;
+    const int per_rank = (n_out + csz - 1) / csz;
+    const int first = rank * per_rank, last = min(first + per_rank, n_out);
+    const int src = threadIdx.x % csz, group = threadIdx.x / csz;
+    const int groups = kWarps * 32 / csz;
+    const uint32_t cs_src = dsmem_addr(smem_u32(cs), src);
+    for (int base = first; base < last; base += groups) {  // same trip count in every thread
+      const int i = base + group;
+      const bool live = i < last;
+      const int hh = live ? i >> 4 : 0, d0 = live ? (i & 15) * 4 : 0;
+      const uint32_t off_m = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->m[hh]) - reinterpret_cast<uintptr_t>(cs));
+      const uint32_t off_d = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->d[hh]) - reinterpret_cast<uintptr_t>(cs));
+      const uint32_t off_o = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->o[hh][d0]) - reinterpret_cast<uintptr_t>(cs));
+      const float ms = dsmem_ld(cs_src + off_m);
+      const float ds = dsmem_ld(cs_src + off_d);
+      const float4 os = dsmem_ld4(cs_src + off_o);
+      float M = ms;
+      for (int off = 1; off < csz; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float c = (M == kNegInf || ms == M) ? 1.0f : ex2(ms - M);  // all -inf: d = o = 0 anyway
+      float den = ds * c;
+      float acc[4] = {os.x * c, os.y * c, os.z * c, os.w * c};
+      for (int off = 1; off < csz; off <<= 1) {
+        den += __shfl_xor_sync(0xffffffffu, den, off);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+      }
+      if (live && src == 0) {
+        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+        const int head = kvh * G + hh;
+        uint16_t* out = static_cast<uint16_t*>(out_bf16) +
+                        (static_cast<size_t>(b) * hq + head) * kHeadDim + d0;
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(out) = pk;
+        if (lse_out && d0 == 0)
+          lse_out[static_cast<size_t>(b) * hq + head] = den > 0.0f ? (M + lg2(den)) * kLn2 : kNegInf;
+      }
+    }
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kWarps * 32)
     sink_decode_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -419,43 +472,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   // ---- on-chip merge of the cluster's splits (same log-sum-exp combine as the merge kernel)
   cluster_sync();  // every CTA's state is written
-  if (cluster_ctarank() == 0) {
-    const uint32_t cs_addr = smem_u32(cs);
-    for (int i = threadIdx.x; i < G * 16; i += kWarps * 32) {
-      const int hh = i >> 4, d0 = (i & 15) * 4;
-      const uint32_t off_m = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->m[hh]) - reinterpret_cast<uintptr_t>(cs));
-      const uint32_t off_d = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->d[hh]) - reinterpret_cast<uintptr_t>(cs));
-      const uint32_t off_o = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&cs->o[hh][d0]) - reinterpret_cast<uintptr_t>(cs));
-      float M = kNegInf;
-      for (int r = 0; r < a.cluster; ++r) M = fmaxf(M, dsmem_ld(dsmem_addr(cs_addr + off_m, r)));
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      float den = 0.0f;
-      if (M != kNegInf) {
-        for (int r = 0; r < a.cluster; ++r) {
-          const uint32_t base = dsmem_addr(cs_addr, r);
-          const float mr = dsmem_ld(base + off_m);
-          const float c = mr == M ? 1.0f : ex2(mr - M);
-          den += dsmem_ld(base + off_d) * c;
-          const float4 o4 = dsmem_ld4(base + off_o);
-          acc[0] += o4.x * c;
-          acc[1] += o4.y * c;
-          acc[2] += o4.z * c;
-          acc[3] += o4.w * c;
-        }
-      }
-      const float inv = den > 0.0f ? 1.0f / den : 0.0f;
-      const int head = kvh * G + hh;
-      uint16_t* out = static_cast<uint16_t*>(a.out) +
-                      (static_cast<size_t>(b) * a.hq + head) * kHeadDim + d0;
-      uint2 pk;
-      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<uint2*>(out) = pk;
-      if (a.lse && d0 == 0)
-        a.lse[static_cast<size_t>(b) * a.hq + head] = den > 0.0f ? (M + lg2(den)) * kLn2 : kNegInf;
-    }
-  }
-  cluster_sync();  // rank 0 has read every CTA's shared memory; all may exit
+  cluster_merge<NT>(cs, a.cluster, a.out, a.lse, a.hq, b, kvh, G);
+  cluster_sync();  // every rank has read the others' shared memory; all may exit
 }
 
 }  // namespace
