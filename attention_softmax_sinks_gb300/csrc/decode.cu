@@ -44,7 +44,7 @@ struct MergeArea {  // aliases the ring once streaming is over
   float o[kWarps][NT * 8][kHeadDim];
 };
 
-// One CTA's combined state, read by cluster rank 0 through distributed shared memory.
+// One CTA's combined state, read by every rank of the cluster through distributed shared memory.
 template <int NT>
 struct CtaState {
   float m[NT * 8];
@@ -63,11 +63,10 @@ constexpr size_t decode_smem_bytes() {
   return 1024 /*alignment slack*/ + kRingBytes + kWarps * kStages * sizeof(uint64_t);
 }
 
-// Merge of a cluster's CTA states, kept out of line so that the streaming loop's code is
-// the same whether or not a launch uses clusters.
-// Every rank merges an equal share of the (head, 4-dim chunk) outputs.  A group of
-// `csz` consecutive lanes takes one output; lane s of the group reads CTA s's state
-// (one round of distributed-shared-memory loads) and the group combines by shuffles.
+// Merge of a cluster's CTA states.  Every rank combines an equal share of the (head, 4-dim
+// chunk) outputs: lane s of a group of `csz` lanes reads CTA s's state (one round of
+// distributed-shared-memory loads) and the group reduces by shuffles.  Kept out of line:
+// inlined, it changed the streaming loop's code and slowed unclustered launches.
 template <int NT>
 __device__ __noinline__ void cluster_merge(CtaState<NT>* cs, int csz, void* out_bf16, float* lse_out,
                                           int hq, int b, int kvh, int G) {
@@ -441,7 +440,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         for (int r = 0; r < 4; ++r) acc[r] += mg->o[w][hh][d0 + r] * c;
       }
     }
-    if (clustered) {  // hand the CTA's state to cluster rank 0
+    if (clustered) {  // hand the CTA's state to the cluster merge
       if (d0 == 0) {
         cs->m[hh] = M;
         cs->d[hh] = den;
