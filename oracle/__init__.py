@@ -42,8 +42,9 @@ import math
 import numpy as np
 
 __all__ = [
-    "widen_bf16", "kv_head_of", "visible_keys", "attention_with_sink", "online_sink_attention",
-    "prefill", "gather_pages", "prefill_paged", "split_token_ranges", "decode", "merge",
+    "widen_bf16", "kv_head_of", "visible_keys", "locate_token", "sequence_head",
+    "attention_with_sink", "online_sink_attention", "prefill", "gather_pages", "prefill_paged",
+    "split_token_ranges", "decode", "merge",
 ]
 
 
@@ -67,13 +68,67 @@ def kv_head_of(h: int, num_qo_heads: int, num_kv_heads: int) -> int:
     return h // (num_qo_heads // num_kv_heads)
 
 
-def visible_keys(q_len: int, kv_len: int, causal: bool) -> np.ndarray:
-    """Boolean [q_len, kv_len]: key j visible to query i (reading 4, bottom-right)."""
+def visible_keys(q_len: int, kv_len: int, causal: bool, rows=None) -> np.ndarray:
+    """Boolean [q_len, kv_len]: key j visible to query i (reading 4, bottom-right).
+
+    With ``rows`` (query indices within the sequence) only those rows are built:
+    [len(rows), kv_len].
+    """
+    i = np.arange(q_len) if rows is None else np.asarray(rows, dtype=np.int64)
     j = np.arange(kv_len)[None, :]
     if not causal:
-        return np.ones((q_len, kv_len), dtype=bool)
-    i = np.arange(q_len)[:, None]
-    return j <= i + (kv_len - q_len)
+        return np.ones((len(i), kv_len), dtype=bool)
+    return j <= i[:, None] + (kv_len - q_len)
+
+
+def locate_token(cu_seqlens, tok: int):
+    """(sequence b, index i of the token within b) for a flat token index.
+
+    Sequence b owns tokens [cu[b], cu[b+1]); an empty sequence owns none, so the
+    owner is the last b whose start is <= tok.
+    """
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    b = int(np.searchsorted(cu, tok, side="right") - 1)
+    return b, int(tok - cu[b])
+
+
+def _rows_per_block(kv_len: int) -> int:
+    """Query rows per block, so that a block's score matrix holds about 2^22 entries."""
+    return max(1, (1 << 22) // max(1, kv_len))
+
+
+def sequence_head(q, k, v, sink, sm_scale, q_len: int, kv_len: int, causal: bool, rows=None):
+    """Rows of one (sequence, head): q [n, D] holds the query rows ``rows`` (indices
+    within the sequence, all of them when None); k, v [kv_len, D].
+
+    Rows are independent, so they are taken a block of rows at a time; a block's
+    score matrix stops after the last key any of its rows can see (the keys after
+    it are masked for every row of the block and would add exact zeros).
+    """
+    idx = np.arange(q_len) if rows is None else np.asarray(rows, dtype=np.int64)
+    d = np.asarray(v).shape[-1]
+    out = np.zeros((len(idx), d))
+    lse = np.zeros(len(idx))
+    step = _rows_per_block(kv_len)
+    for r0 in range(0, len(idx), step):
+        sel = idx[r0:r0 + step]
+        last = kv_len
+        if causal and len(sel):
+            last = max(0, min(kv_len, int(sel.max()) + kv_len - q_len + 1))
+        vis = visible_keys(q_len, kv_len, causal, rows=sel)[:, :last]
+        o, l = attention_with_sink(q[r0:r0 + step], k[:last], v[:last], sink, sm_scale, vis)
+        out[r0:r0 + len(sel)], lse[r0:r0 + len(sel)] = o, l
+    return out, lse
+
+
+def _run_units(fn, units, workers: int):
+    """fn over independent units, on ``workers`` threads (numpy releases the GIL)."""
+    units = list(units)
+    if workers <= 1 or len(units) <= 1:
+        return [fn(u) for u in units]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, units))
 
 
 # ---------------------------------------------------------------- the definition
@@ -146,13 +201,14 @@ def online_sink_attention(q, k, v, sink, sm_scale, block: int):
 
 
 # ---------------------------------------------------------------- contiguous prefill
-def prefill(q, k, v, sinks, cu_seqlens, sm_scale, causal=True, rows=None):
+def prefill(q, k, v, sinks, cu_seqlens, sm_scale, causal=True, rows=None, workers=1):
     """Ragged contiguous prefill (q_len == kv_len per sequence).
 
     q [T, Hq, D], k/v [T, Hkv, D] (bf16 bits or floats), sinks [Hq],
     cu_seqlens [B+1].  Returns out [T, Hq, D], lse [T, Hq] in fp64.  With
     ``rows`` (a list of (token, head)), only those rows are computed and the
-    results come back as arrays [len(rows), D] and [len(rows)].
+    results come back as arrays [len(rows), D] and [len(rows)].  ``workers``
+    threads share the (sequence, head) units.
     """
     qf, kf, vf = _as_f64(q), _as_f64(k), _as_f64(v)
     sinks = np.asarray(sinks, dtype=np.float64)
@@ -160,30 +216,34 @@ def prefill(q, k, v, sinks, cu_seqlens, sm_scale, causal=True, rows=None):
     t, hq, d = qf.shape
     hkv = kf.shape[1]
     if rows is not None:
+        groups = {}
+        for r, (tok, h) in enumerate(rows):
+            b, i = locate_token(cu, int(tok))
+            groups.setdefault((b, int(h)), []).append((r, i))
         out = np.zeros((len(rows), d))
         lse = np.zeros(len(rows))
-        for r, (tok, h) in enumerate(rows):
-            b = int(np.searchsorted(cu, tok, side="right") - 1)
-            lo, hi = int(cu[b]), int(cu[b + 1])
-            i = tok - lo
-            g = kv_head_of(h, hq, hkv)
-            vis = visible_keys(hi - lo, hi - lo, causal)[i:i + 1]
-            o, l = attention_with_sink(qf[tok:tok + 1, h], kf[lo:hi, g], vf[lo:hi, g],
-                                       sinks[h], sm_scale, vis)
-            out[r], lse[r] = o[0], l[0]
-        return out, lse
-    out = np.zeros((t, hq, d))
-    lse = np.zeros((t, hq))
-    for b in range(len(cu) - 1):
+    else:
+        groups = {(b, h): None for b in range(len(cu) - 1) if cu[b + 1] > cu[b] for h in range(hq)}
+        out = np.zeros((t, hq, d))
+        lse = np.zeros((t, hq))
+
+    def unit(key):
+        b, h = key
         lo, hi = int(cu[b]), int(cu[b + 1])
-        if hi == lo:
-            continue
-        vis = visible_keys(hi - lo, hi - lo, causal)
-        for h in range(hq):
-            g = kv_head_of(h, hq, hkv)
-            o, l = attention_with_sink(qf[lo:hi, h], kf[lo:hi, g], vf[lo:hi, g], sinks[h],
-                                       sm_scale, vis)
+        g = kv_head_of(h, hq, hkv)
+        sel = None if groups[key] is None else [i for _, i in groups[key]]
+        qrows = qf[lo:hi, h] if sel is None else qf[lo + np.asarray(sel, dtype=np.int64), h]
+        return sequence_head(qrows, kf[lo:hi, g], vf[lo:hi, g], sinks[h], sm_scale,
+                             hi - lo, hi - lo, causal, sel)
+
+    for key, (o, l) in zip(groups, _run_units(unit, groups, workers)):
+        b, h = key
+        if groups[key] is None:
+            lo, hi = int(cu[b]), int(cu[b + 1])
             out[lo:hi, h], lse[lo:hi, h] = o, l
+        else:
+            for n, (r, _) in enumerate(groups[key]):
+                out[r], lse[r] = o[n], l[n]
     return out, lse
 
 
@@ -200,47 +260,57 @@ def gather_pages(pages, page_table_row, kv_len, page_size=None):
 
 
 def prefill_paged(q, k_pages, v_pages, page_table, cu_seqlens_q, kv_lens, sinks, sm_scale,
-                  causal=True, rows=None):
+                  causal=True, rows=None, workers=1):
     """Mixed batch over a paged cache: sequence b has q_len new tokens, the last
-    q_len of its kv_len cached tokens (reading 4).  q [Tq, Hq, D]."""
+    q_len of its kv_len cached tokens (reading 4).  q [Tq, Hq, D].  ``rows`` and
+    ``workers`` as for ``prefill``."""
     qf = _as_f64(q)
     sinks = np.asarray(sinks, dtype=np.float64)
     cu = np.asarray(cu_seqlens_q, dtype=np.int64)
     kv_lens = np.asarray(kv_lens, dtype=np.int64)
     t, hq, d = qf.shape
     hkv = np.asarray(k_pages).shape[1]
-    seqs = range(len(cu) - 1)
     if rows is not None:
-        want = {}
+        groups = {}
         for r, (tok, h) in enumerate(rows):
-            b = int(np.searchsorted(cu, tok, side="right") - 1)
-            want.setdefault(b, []).append((r, tok, h))
-        seqs = sorted(want)
+            b, i = locate_token(cu, int(tok))
+            groups.setdefault((b, int(h)), []).append((r, i))
         out = np.zeros((len(rows), d))
         lse = np.zeros(len(rows))
     else:
+        groups = {(b, h): None for b in range(len(cu) - 1) if cu[b + 1] > cu[b] for h in range(hq)}
         out = np.zeros((t, hq, d))
         lse = np.zeros((t, hq))
-    for b in seqs:
+    cache = {}
+
+    def kv_of(b):
+        if b not in cache:
+            kv_len = int(kv_lens[b])
+            cache[b] = (_as_f64(gather_pages(k_pages, page_table[b], kv_len)),
+                        _as_f64(gather_pages(v_pages, page_table[b], kv_len)))
+        return cache[b]
+
+    for b in sorted({b for b, _ in groups}):
+        kv_of(b)
+
+    def unit(key):
+        b, h = key
         lo, hi = int(cu[b]), int(cu[b + 1])
-        q_len, kv_len = hi - lo, int(kv_lens[b])
-        if q_len == 0:
-            continue
-        kb = _as_f64(gather_pages(k_pages, page_table[b], kv_len))
-        vb = _as_f64(gather_pages(v_pages, page_table[b], kv_len))
-        vis = visible_keys(q_len, kv_len, causal)
-        if rows is not None:
-            for r, tok, h in want[b]:
-                g = kv_head_of(h, hq, hkv)
-                i = tok - lo
-                o, l = attention_with_sink(qf[tok:tok + 1, h], kb[:, g], vb[:, g], sinks[h],
-                                           sm_scale, vis[i:i + 1])
-                out[r], lse[r] = o[0], l[0]
-            continue
-        for h in range(hq):
-            g = kv_head_of(h, hq, hkv)
-            o, l = attention_with_sink(qf[lo:hi, h], kb[:, g], vb[:, g], sinks[h], sm_scale, vis)
+        kb, vb = kv_of(b)
+        g = kv_head_of(h, hq, hkv)
+        sel = None if groups[key] is None else [i for _, i in groups[key]]
+        qrows = qf[lo:hi, h] if sel is None else qf[lo + np.asarray(sel, dtype=np.int64), h]
+        return sequence_head(qrows, kb[:, g], vb[:, g], sinks[h], sm_scale,
+                             hi - lo, int(kv_lens[b]), causal, sel)
+
+    for key, (o, l) in zip(groups, _run_units(unit, groups, workers)):
+        b, h = key
+        if groups[key] is None:
+            lo, hi = int(cu[b]), int(cu[b + 1])
             out[lo:hi, h], lse[lo:hi, h] = o, l
+        else:
+            for n, (r, _) in enumerate(groups[key]):
+                out[r], lse[r] = o[n], l[n]
     return out, lse
 
 
@@ -256,14 +326,16 @@ def split_token_ranges(kv_len: int, page_size: int, num_splits: int):
     return ranges
 
 
-def decode(q, k_pages, v_pages, page_table, kv_lens, sinks, sm_scale, num_splits=1, batches=None):
+def decode(q, k_pages, v_pages, page_table, kv_lens, sinks, sm_scale, num_splits=1, batches=None,
+           workers=1):
     """One new token per sequence over a paged cache.
 
     q [B, Hq, D].  With num_splits == 1 returns out [B, Hq, D], lse [B, Hq].
     With num_splits > 1 returns the partials o [B, S, Hq, D], lse [B, S, Hq]:
     split s attends to its own token range, and only split 0 has the sink
     column (the page's rule that the seeded max belongs to the first block).
-    ``batches`` restricts the work to some sequences (other rows stay 0).
+    ``batches`` restricts the work to some sequences (other rows stay 0);
+    ``workers`` threads share the sequences.
     """
     qf = _as_f64(q)
     sinks = np.asarray(sinks, dtype=np.float64)
@@ -273,7 +345,8 @@ def decode(q, k_pages, v_pages, page_table, kv_lens, sinks, sm_scale, num_splits
     ps = np.asarray(k_pages).shape[2]
     po = np.zeros((bsz, num_splits, hq, d))
     pl = np.zeros((bsz, num_splits, hq))
-    for b in (range(bsz) if batches is None else batches):
+
+    def unit(b):
         kv_len = int(kv_lens[b])
         kb = _as_f64(gather_pages(k_pages, page_table[b], kv_len))
         vb = _as_f64(gather_pages(v_pages, page_table[b], kv_len))
@@ -283,6 +356,8 @@ def decode(q, k_pages, v_pages, page_table, kv_lens, sinks, sm_scale, num_splits
                 o, l = attention_with_sink(qf[b, h][None], kb[t0:t1, g], vb[t0:t1, g], sinks[h],
                                            sm_scale, None, with_sink=(s == 0))
                 po[b, s, h], pl[b, s, h] = o[0], l[0]
+
+    _run_units(unit, range(bsz) if batches is None else batches, workers)
     if num_splits == 1:
         return po[:, 0], pl[:, 0]
     return po, pl

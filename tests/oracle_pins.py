@@ -289,10 +289,63 @@ def pin_causal_counts():
             assert int((p[i] > 0).sum()) == kv_len - q_len + i + 1, (q_len, kv_len, i)
 
 
+def pin_row_sampling_paths():
+    """The sampled paths (``rows=`` of both prefills, ``batches=`` of decode) return
+    exactly the matching entries of the full computation, which the other pins tie
+    to the definition: ragged batches with empty sequences, rows in any order and
+    repeated, tokens at the start of a sequence that follows empty ones, causal and
+    not, several threads or one."""
+    rng = _rng(22)
+    hq, hkv, d = 4, 2, 8
+    lens = [3, 0, 17, 1, 0, 0, 40]
+    cu = workloads.cu_seqlens_from(lens)
+    t = int(cu[-1])
+    q, k, v = (_bf16_floats(rng, (t, h, d)) for h in (hq, hkv, hkv))
+    sinks = _bf16_floats(rng, (hq,))
+    starts = [int(cu[b]) for b in range(len(lens)) if lens[b]]
+    rows = [(int(a), int(h)) for a, h in zip(rng.permutation(t), rng.integers(0, hq, t))]
+    rows += [(s, h) for s in starts for h in range(hq)] + [(t - 1, 0), (t - 1, 0)]
+    for causal in (True, False):
+        ref_o, ref_l = oracle.prefill(q, k, v, sinks, cu, 0.3, causal)
+        for workers in (1, 3):
+            o, l = oracle.prefill(q, k, v, sinks, cu, 0.3, causal, rows=rows, workers=workers)
+            tok = [r[0] for r in rows]
+            hh = [r[1] for r in rows]
+            _close(o, ref_o[tok, hh], 1e-13, f"prefill rows causal={causal} workers={workers}")
+            _close(l, ref_l[tok, hh], 1e-13, f"prefill rows lse causal={causal}")
+    # paged, q_len < kv_len, a sequence with no new token
+    q_lens, kv_lens = [1, 0, 5, 20, 3], [9, 4, 5, 33, 70]
+    data = workloads.make_mixed(7, q_lens, kv_lens, hq, hkv, d, page_size=16)
+    cuq = data["cu_seqlens_q"]
+    tq = int(cuq[-1])
+    prow = [(int(a), int(h)) for a, h in zip(rng.permutation(tq), rng.integers(0, hq, tq))]
+    prow += [(int(cuq[b]), h) for b in (2, 3, 4) for h in range(hq)]
+    for causal in (True, False):
+        args = (data["q"], data["k_pages"], data["v_pages"], data["page_table"], cuq,
+                data["kv_lens"], data["sinks"], 0.125, causal)
+        ref_o, ref_l = oracle.prefill_paged(*args)
+        o, l = oracle.prefill_paged(*args, rows=prow, workers=2)
+        tok = [r[0] for r in prow]
+        hh = [r[1] for r in prow]
+        _close(o, ref_o[tok, hh], 1e-13, f"paged rows causal={causal}")
+        _close(l, ref_l[tok, hh], 1e-13, f"paged rows lse causal={causal}")
+    # decode restricted to some sequences, unsplit and split
+    dd = workloads.make_decode(23, [1, 17, 300, 40, 129], 8, 2, 16, page_size=16)
+    args = (dd["q"], dd["k_pages"], dd["v_pages"], dd["page_table"], dd["kv_lens"], dd["sinks"], 0.25)
+    pick = [3, 0, 2]
+    for s in (1, 3):
+        ref_o, ref_l = oracle.decode(*args, num_splits=s)
+        o, l = oracle.decode(*args, num_splits=s, batches=pick, workers=2)
+        _close(o[pick], ref_o[pick], 1e-13, f"decode batches splits={s}")
+        _close(l[pick], ref_l[pick], 1e-13, f"decode batches lse splits={s}")
+        rest = [b for b in range(5) if b not in pick]
+        assert np.all(o[rest] == 0) and np.all(l[rest] == 0), "unpicked sequences must stay 0"
+
+
 ALL_PINS = [pin_hand_worked, pin_sdpa_reduction, pin_large_sink_saturates, pin_normalisation,
             pin_single_key_closed_form, pin_identical_keys, pin_split_merge_invariance,
             pin_brute_force_decimal, pin_online_algorithm, pin_paging, pin_gqa_mapping,
-            pin_causal_counts]
+            pin_causal_counts, pin_row_sampling_paths]
 
 
 def failing_pins():

@@ -49,11 +49,50 @@ def _lse_log2(orig, q, k, v, sink, sm_scale, visible, with_sink, rp):
     return (res[0], res[1] / math.log(2)) + tuple(res[2:])
 
 
-def _top_left_causal(q_len, kv_len, causal):
-    vis = np.ones((q_len, kv_len), dtype=bool)
+def _top_left_causal(q_len, kv_len, causal, rows=None):
+    i = np.arange(q_len) if rows is None else np.asarray(rows)
+    vis = np.ones((len(i), kv_len), dtype=bool)
     if causal:
-        vis = np.arange(kv_len)[None, :] <= np.arange(q_len)[:, None]
+        vis = np.arange(kv_len)[None, :] <= i[:, None]
     return vis
+
+
+_ORIG_VISIBLE = oracle.visible_keys
+
+
+def _visibility_of_first_row(q_len, kv_len, causal, rows=None):
+    # every row of a block takes the mask of the block's first query
+    vis = _ORIG_VISIBLE(q_len, kv_len, causal, rows)
+    return np.broadcast_to(vis[:1], vis.shape).copy() if len(vis) else vis
+
+
+_ORIG_LOCATE = oracle.locate_token
+
+
+def _locate_left(cu, tok):
+    # searchsorted to the left: a token that starts a sequence goes to the one before
+    cu = np.asarray(cu, dtype=np.int64)
+    b = max(0, int(np.searchsorted(cu, tok, side="left")) - 1)
+    return b, int(tok - cu[b])
+
+
+def _locate_global_index(cu, tok):
+    b, _ = _ORIG_LOCATE(cu, tok)
+    return b, int(tok)
+
+
+_ORIG_DECODE = oracle.decode
+
+
+def _decode_batches_by_position(*args, batches=None, **kw):
+    # the restricted decode writes its n-th picked sequence to row n
+    po, pl = _ORIG_DECODE(*args, batches=batches, **kw)
+    if batches is None:
+        return po, pl
+    po2, pl2 = np.zeros_like(po), np.zeros_like(pl)
+    for n, b in enumerate(batches):
+        po2[n], pl2[n] = po[b], pl[b]
+    return po2, pl2
 
 
 def _gqa_modulo(h, hq, hkv):
@@ -91,6 +130,10 @@ MUTANTS = {
     "gqa_modulo": ("kv_head_of", _gqa_modulo),
     "split_drops_last_token": ("split_token_ranges", _split_drops_last_token),
     "online_d_starts_at_zero": ("online_sink_attention", _online_d_starts_at_zero),
+    "visibility_of_first_row": ("visible_keys", _visibility_of_first_row),
+    "sequence_lookup_left": ("locate_token", _locate_left),
+    "row_index_not_local": ("locate_token", _locate_global_index),
+    "decode_batches_by_position": ("decode", _decode_batches_by_position),
 }
 
 
