@@ -1,6 +1,11 @@
 import os
 import sys
 
+# The oracle runs its independent (sequence, head) units on threads; one BLAS
+# thread per call keeps those threads from oversubscribing the host's cores.
+for _var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_var, "1")
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_common import LSE_TOL, OUT_TOL, assert_close, bf16, dev, host, max_err, require_gpu
+from gpu_common import LSE_TOL, OUT_TOL, assert_close, bf16, dev, host, max_err, oracle_workers, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -108,22 +108,24 @@ def test_paged_decode_config_full():
 
 
 @pytest.mark.parametrize("sink_fill", [None, -np.inf, 20.0])
-def test_long_decode_config_sampled(sink_fill):
-    """Long-context split decode: 8 x 131072 tokens, 32 splits, merged; two sequences checked."""
+def test_long_decode_config_full(sink_fill):
+    """Long-context split decode: 8 x 131072 tokens, 64/8 heads, 32 splits, merged; every
+    sequence and head against the oracle, partials (split 0 alone carries the sink) too."""
     sa = require_gpu()
     cfg = workloads.WORKLOADS["long_decode"]
     d = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * cfg["batch"], cfg["hq"], cfg["hkv"],
                               cfg["d"], cfg["page_size"], cfg["sink_std"], sink_fill=sink_fill)
     po, pl, _ = _run(sa, d, cfg["sm_scale"], cfg["num_splits"])
     o, l = sa.sink_attn_merge(po, pl)
-    pick = [0, cfg["batch"] - 1]
+    assert sa.sink_attn_device_status(True) == 0
     ro, rl = oracle.decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["kv_lens"],
-                           d["sinks"], cfg["sm_scale"], num_splits=cfg["num_splits"], batches=pick)
+                           d["sinks"], cfg["sm_scale"], num_splits=cfg["num_splits"],
+                           workers=min(4, oracle_workers()))
     fo, fl = oracle.merge(ro, rl)
-    assert_close(host(o)[pick], host(l)[pick], fo[pick], fl[pick], f"long decode sink={sink_fill}")
-    # split 0 alone carries the sink: its partial lse is checked directly too
-    assert max_err(host(pl)[pick], rl[pick]) <= LSE_TOL
-    del d
+    assert_close(host(o), host(l), fo, fl, f"long decode 8x131072 sink={sink_fill} (all rows)")
+    assert max_err(host(po), ro) <= OUT_TOL
+    assert max_err(host(pl), rl) <= LSE_TOL
+    del d, po, pl
     torch.cuda.empty_cache()
 
 

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_common import assert_close, bf16, dev, host, require_gpu
+from gpu_common import assert_close, bf16, dev, host, oracle_workers, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -30,25 +30,18 @@ def test_paged_prefill_small(causal):
 
 
 def test_ragged_mixed_config():
-    """32 sequences, KV log-uniform in [1, 32768], decode rows and 128-2048 token chunks."""
+    """32 sequences, KV log-uniform in [1, 32768], decode rows and 128-2048 token chunks:
+    every new token of every sequence, every head, against the oracle."""
     sa = require_gpu()
     cfg = workloads.WORKLOADS["ragged_mixed"]
     q_lens, kv_lens = workloads.ragged_mixed_lengths(cfg["seed"] + 2, cfg["num_seqs"], cfg["max_kv"])
     d = workloads.make_mixed(cfg["seed"], q_lens, kv_lens, cfg["hq"], cfg["hkv"], cfg["d"],
                              cfg["page_size"], cfg["sink_std"])
     o, l = _run(sa, d, int(q_lens.max()), cfg["sm_scale"])
-    cu = d["cu_seqlens_q"]
-    rng = np.random.default_rng(5)
-    rows = []
-    for b in range(len(q_lens)):  # first and last new token of every sequence, plus random ones
-        for tok in {int(cu[b]), int(cu[b + 1]) - 1, int(rng.integers(cu[b], cu[b + 1]))}:
-            rows.append((tok, int(rng.integers(0, cfg["hq"]))))
-    ro, rl = oracle.prefill_paged(d["q"], d["k_pages"], d["v_pages"], d["page_table"], cu,
-                                  d["kv_lens"], d["sinks"], cfg["sm_scale"], True, rows=rows)
-    go = host(o)[[r[0] for r in rows], [r[1] for r in rows]]
-    gl = host(l)[[r[0] for r in rows], [r[1] for r in rows]]
-    assert_close(go, gl, ro, rl, "ragged mixed")
     assert sa.sink_attn_device_status(True) == 0
+    ro, rl = oracle.prefill_paged(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["cu_seqlens_q"],
+                                  d["kv_lens"], d["sinks"], cfg["sm_scale"], True, workers=oracle_workers())
+    assert_close(host(o), host(l), ro, rl, "ragged mixed (all rows)")
 
 
 def test_paged_prefill_matches_contiguous_prefill_bitwise():
