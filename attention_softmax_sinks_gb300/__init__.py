@@ -120,8 +120,30 @@ def _dev(t, name, dtype):
     return t
 
 
-def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _out(t, name, dtype, shape, device):
+    """A caller-supplied output: on ``device``, of ``dtype``, contiguous and ``shape``."""
+    _dev(t, name, dtype)
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _same_device(device, **tensors):
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, expected {device} (the device of the first input)")
+
+
+def _stream(stream, device=None):
+    """Raw handle of ``stream`` (default: the current stream of ``device``)."""
+    if stream is None:
+        s = torch.cuda.current_stream(device)
+    else:
+        s = stream
+        if device is not None and s.device != device:
+            raise ValueError(f"stream is on {s.device}, the tensors on {device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -140,13 +162,17 @@ def sink_attn_prefill(q, k, v, sinks, cu_seqlens, max_seqlen: int, sm_scale: flo
     hkv = k.shape[1]
     if k.shape != (t, hkv, d) or v.shape != k.shape:
         raise ValueError("k and v must be [T, Hkv, D] with q's T and D")
-    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16)
+    _same_device(q.device, k=k, v=v, sinks=sinks, cu_seqlens=cu_seqlens)
+    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, q.device)
     if lse is None and return_lse:
         lse = torch.empty((t, hq), dtype=torch.float32, device=q.device)
-    st = load_library().sink_attn_prefill(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), cu_seqlens.numel() - 1, t,
-        int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
-        _stream(stream))
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, (t, hq), q.device)
+    with torch.cuda.device(q.device):
+        st = load_library().sink_attn_prefill(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), cu_seqlens.numel() - 1, t,
+            int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
+            _stream(stream, q.device))
     _check(st, "sink_attn_prefill")
     return out, lse
 
@@ -166,14 +192,19 @@ def sink_attn_prefill_paged(q, paged_k, paged_v, page_table, cu_seqlens_q, kv_le
         _dev(tns, name, dt)
     t, hq, d = q.shape
     num_pages, hkv, page_size, _ = paged_k.shape
-    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16)
+    _same_device(q.device, paged_k=paged_k, paged_v=paged_v, page_table=page_table,
+                 cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, sinks=sinks)
+    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, q.device)
     if lse is None and return_lse:
         lse = torch.empty((t, hq), dtype=torch.float32, device=q.device)
-    st = load_library().sink_attn_prefill_paged(
-        _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(cu_seqlens_q), _ptr(kv_lens),
-        _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq, hkv, d, page_size,
-        page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
-        _stream(stream))
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, (t, hq), q.device)
+    with torch.cuda.device(q.device):
+        st = load_library().sink_attn_prefill_paged(
+            _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(cu_seqlens_q), _ptr(kv_lens),
+            _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq, hkv, d, page_size,
+            page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
+            _stream(stream, q.device))
     _check(st, "sink_attn_prefill_paged")
     return out, lse
 
@@ -192,17 +223,24 @@ def sink_attn_decode(q, paged_k, paged_v, page_table, kv_lens, sinks, sm_scale: 
         _dev(tns, name, dt)
     b, hq, d = q.shape
     num_pages, hkv, page_size, _ = paged_k.shape
+    _same_device(q.device, paged_k=paged_k, paged_v=paged_v, page_table=page_table, kv_lens=kv_lens,
+                 sinks=sinks)
     s = int(num_splits)
+    out_shape, out_dtype = ((b, hq, d), torch.bfloat16) if s == 1 else ((b, s, hq, d), torch.float32)
+    lse_shape = (b, hq) if s == 1 else (b, s, hq)
     if out is None:
-        out = (torch.empty_like(q) if s == 1 else
-               torch.empty((b, s, hq, d), dtype=torch.float32, device=q.device))
+        out = torch.empty(out_shape, dtype=out_dtype, device=q.device)
+    else:
+        _out(out, "out", out_dtype, out_shape, q.device)
     if lse is None and (return_lse or s > 1):
-        shape = (b, hq) if s == 1 else (b, s, hq)
-        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
-    st = load_library().sink_attn_decode(
-        _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
-        hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), s, _ptr(out), _ptr(lse),
-        _stream(stream))
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, lse_shape, q.device)
+    with torch.cuda.device(q.device):
+        st = load_library().sink_attn_decode(
+            _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
+            hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), s, _ptr(out), _ptr(lse),
+            _stream(stream, q.device))
     _check(st, "sink_attn_decode")
     return out, lse
 
@@ -224,13 +262,18 @@ def sink_attn_decode_noalloc(q, paged_k, paged_v, page_table, kv_lens, sinks, sm
         _dev(tns, name, dt)
     b, hq, d = q.shape
     num_pages, hkv, page_size, _ = paged_k.shape
-    out = torch.empty_like(q) if out is None else _dev(out, "out", torch.bfloat16)
+    _same_device(q.device, paged_k=paged_k, paged_v=paged_v, page_table=page_table, kv_lens=kv_lens,
+                 sinks=sinks)
+    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, q.device)
     if lse is None and return_lse:
         lse = torch.empty((b, hq), dtype=torch.float32, device=q.device)
-    st = load_library().sink_attn_decode_noalloc(
-        _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
-        hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(num_splits), _ptr(out),
-        _ptr(lse), _stream(stream))
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, (b, hq), q.device)
+    with torch.cuda.device(q.device):
+        st = load_library().sink_attn_decode_noalloc(
+            _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
+            hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(num_splits), _ptr(out),
+            _ptr(lse), _stream(stream, q.device))
     _check(st, "sink_attn_decode_noalloc")
     return out, lse
 
@@ -240,12 +283,19 @@ def sink_attn_merge(partial_o, partial_lse, out=None, lse=None, return_lse: bool
     """Merge split partials o [B, S, H, 64] fp32 / lse [B, S, H] fp32 -> (out bf16, lse fp32)."""
     _dev(partial_o, "partial_o", torch.float32), _dev(partial_lse, "partial_lse", torch.float32)
     b, s, h, d = partial_o.shape
-    out = (torch.empty((b, h, d), dtype=torch.bfloat16, device=partial_o.device) if out is None
-           else _dev(out, "out", torch.bfloat16))
+    dv = partial_o.device
+    if tuple(partial_lse.shape) != (b, s, h):
+        raise ValueError(f"partial_lse must be {(b, s, h)}, got {tuple(partial_lse.shape)}")
+    _same_device(dv, partial_lse=partial_lse)
+    out = (torch.empty((b, h, d), dtype=torch.bfloat16, device=dv) if out is None
+           else _out(out, "out", torch.bfloat16, (b, h, d), dv))
     if lse is None and return_lse:
-        lse = torch.empty((b, h), dtype=torch.float32, device=partial_o.device)
-    st = load_library().sink_attn_merge(_ptr(partial_o), _ptr(partial_lse), b, s, h, d, _ptr(out),
-                                        _ptr(lse), _stream(stream))
+        lse = torch.empty((b, h), dtype=torch.float32, device=dv)
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, (b, h), dv)
+    with torch.cuda.device(dv):
+        st = load_library().sink_attn_merge(_ptr(partial_o), _ptr(partial_lse), b, s, h, d, _ptr(out),
+                                            _ptr(lse), _stream(stream, dv))
     _check(st, "sink_attn_merge")
     return out, lse
 
@@ -276,8 +326,10 @@ def sink_attn_abi_version() -> int:
 
 def sink_attn_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) -> None:
     """Launch the bounded-wait diagnostic (records SA_ERR_TIMEOUT in the status word)."""
-    _check(load_library().sink_attn_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
-           "sink_attn_selftest_wait_timeout")
+    dv = torch.device("cuda", torch.cuda.current_device()) if stream is None else stream.device
+    with torch.cuda.device(dv):
+        st = load_library().sink_attn_selftest_wait_timeout(int(timeout_ns), _stream(stream, dv))
+    _check(st, "sink_attn_selftest_wait_timeout")
 
 
 # ----------------------------------------------------------------------------- around attention
@@ -289,16 +341,18 @@ def moe_router_topk_softmax(logits, top_k: int, topk_idx=None, topk_weight=None,
     _dev(logits, "logits", torch.bfloat16)
     t, e = logits.shape
     k = int(top_k)
-    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=logits.device) if topk_idx is None
-                else _dev(topk_idx, "topk_idx", torch.int32))
-    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=logits.device) if topk_weight is None
-                   else _dev(topk_weight, "topk_weight", torch.bfloat16))
+    dv = logits.device
+    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=dv) if topk_idx is None
+                else _out(topk_idx, "topk_idx", torch.int32, (t, k), dv))
+    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=dv) if topk_weight is None
+                   else _out(topk_weight, "topk_weight", torch.bfloat16, (t, k), dv))
     if expert_counts is None and return_counts:
-        expert_counts = torch.empty((e,), dtype=torch.int32, device=logits.device)
+        expert_counts = torch.empty((e,), dtype=torch.int32, device=dv)
     elif expert_counts is not None:
-        _dev(expert_counts, "expert_counts", torch.int32)
-    st = load_library().moe_router_topk_softmax(_ptr(logits), t, e, k, _ptr(topk_idx), _ptr(topk_weight),
-                                                _ptr(expert_counts), _stream(stream))
+        _out(expert_counts, "expert_counts", torch.int32, (e,), dv)
+    with torch.cuda.device(dv):
+        st = load_library().moe_router_topk_softmax(_ptr(logits), t, e, k, _ptr(topk_idx), _ptr(topk_weight),
+                                                    _ptr(expert_counts), _stream(stream, dv))
     _check(st, "moe_router_topk_softmax")
     if expert_counts is not None:
         return topk_idx, topk_weight, expert_counts
@@ -323,15 +377,18 @@ def qkv_bias_rope(qkv, bias, cu_seqlens_q, num_qo_heads: int, num_kv_heads: int,
         _dev(kv_lens, "kv_lens", torch.int32)
     t = qkv.shape[0]
     hq, hkv, d = int(num_qo_heads), int(num_kv_heads), 64
-    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=qkv.device) if q_out is None else q_out
-    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=qkv.device) if k_out is None else k_out
-    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=qkv.device) if v_out is None else v_out
-    for name, x in (("q_out", q_out), ("k_out", k_out), ("v_out", v_out)):
-        _dev(x, name, torch.bfloat16)
-    st = load_library().qkv_bias_rope(_ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens),
-                                      cu_seqlens_q.numel() - 1, t, hq, hkv, qkv.shape[1] // (hq + 2 * hkv),
-                                      *_rope_params(rope), _ptr(q_out), _ptr(k_out), _ptr(v_out),
-                                      _stream(stream))
+    dv = qkv.device
+    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens)
+    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if q_out is None else q_out
+    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if k_out is None else k_out
+    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if v_out is None else v_out
+    for name, x, h in (("q_out", q_out, hq), ("k_out", k_out, hkv), ("v_out", v_out, hkv)):
+        _out(x, name, torch.bfloat16, (t, h, d), dv)
+    with torch.cuda.device(dv):
+        st = load_library().qkv_bias_rope(_ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens),
+                                          cu_seqlens_q.numel() - 1, t, hq, hkv, qkv.shape[1] // (hq + 2 * hkv),
+                                          *_rope_params(rope), _ptr(q_out), _ptr(k_out), _ptr(v_out),
+                                          _stream(stream, dv))
     _check(st, "qkv_bias_rope")
     return q_out, k_out, v_out
 
@@ -349,12 +406,16 @@ def qkv_bias_rope_append_paged(qkv, bias, cu_seqlens_q, kv_lens, paged_k, paged_
     t = qkv.shape[0]
     num_pages, hkv, page_size, d = paged_k.shape
     hq = int(num_qo_heads)
-    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=qkv.device) if q_out is None else q_out
-    _dev(q_out, "q_out", torch.bfloat16)
-    st = load_library().qkv_bias_rope_append_paged(
-        _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
-        qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(q_out), _ptr(paged_k), _ptr(paged_v),
-        _ptr(page_table), page_size, page_table.shape[1], num_pages, _stream(stream))
+    dv = qkv.device
+    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, paged_k=paged_k,
+                 paged_v=paged_v, page_table=page_table)
+    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if q_out is None else q_out
+    _out(q_out, "q_out", torch.bfloat16, (t, hq, d), dv)
+    with torch.cuda.device(dv):
+        st = load_library().qkv_bias_rope_append_paged(
+            _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
+            qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(q_out), _ptr(paged_k), _ptr(paged_v),
+            _ptr(page_table), page_size, page_table.shape[1], num_pages, _stream(stream, dv))
     _check(st, "qkv_bias_rope_append_paged")
     return q_out
 
@@ -371,10 +432,13 @@ def linear_bias(x, w, bias=None, out=None, stream=None):
     n = w.shape[0]
     if w.shape[1] != k:
         raise ValueError(f"w is {tuple(w.shape)}, expected [N, {k}]")
+    _same_device(x.device, w=w, bias=bias)
     out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else out
-    _dev(out, "out", torch.bfloat16)
-    _check(load_library().linear_bias(_ptr(x), _ptr(w), _ptr(bias), m, n, k, _ptr(out), _stream(stream)),
-           "linear_bias")
+    _out(out, "out", torch.bfloat16, (m, n), x.device)
+    with torch.cuda.device(x.device):
+        st = load_library().linear_bias(_ptr(x), _ptr(w), _ptr(bias), m, n, k, _ptr(out),
+                                        _stream(stream, x.device))
+    _check(st, "linear_bias")
     return out
 
 
@@ -392,16 +456,20 @@ def moe_router(x, w_router, bias, top_k: int, topk_idx=None, topk_weight=None, e
     if w_router.shape[1] != hidden:
         raise ValueError(f"w_router is {tuple(w_router.shape)}, expected [E, {hidden}]")
     k = int(top_k)
-    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=x.device) if topk_idx is None
-                else _dev(topk_idx, "topk_idx", torch.int32))
-    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=x.device) if topk_weight is None
-                   else _dev(topk_weight, "topk_weight", torch.bfloat16))
+    dv = x.device
+    _same_device(dv, w_router=w_router, bias=bias)
+    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=dv) if topk_idx is None
+                else _out(topk_idx, "topk_idx", torch.int32, (t, k), dv))
+    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=dv) if topk_weight is None
+                   else _out(topk_weight, "topk_weight", torch.bfloat16, (t, k), dv))
     if expert_counts is None and return_counts:
-        expert_counts = torch.empty((e,), dtype=torch.int32, device=x.device)
+        expert_counts = torch.empty((e,), dtype=torch.int32, device=dv)
     elif expert_counts is not None:
-        _dev(expert_counts, "expert_counts", torch.int32)
-    _check(load_library().moe_router(_ptr(x), _ptr(w_router), _ptr(bias), t, hidden, e, k, _ptr(topk_idx),
-                                     _ptr(topk_weight), _ptr(expert_counts), _stream(stream)), "moe_router")
+        _out(expert_counts, "expert_counts", torch.int32, (e,), dv)
+    with torch.cuda.device(dv):
+        st = load_library().moe_router(_ptr(x), _ptr(w_router), _ptr(bias), t, hidden, e, k, _ptr(topk_idx),
+                                       _ptr(topk_weight), _ptr(expert_counts), _stream(stream, dv))
+    _check(st, "moe_router")
     if expert_counts is not None:
         return topk_idx, topk_weight, expert_counts
     return topk_idx, topk_weight

@@ -22,6 +22,7 @@
 //    the kernel before it (the previous step's merge) still runs: in that time
 //    it asks L2 for the first four pages of each warp's ring, which hides the
 //    page-table -> page latency of its start (headline step 85.8 -> 80.8 us).
+#include <mutex>
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -480,12 +481,15 @@ __global__ void __launch_bounds__(kWarps * 32)
 // How many clusters of 16 CTAs of `kern` can be resident at once on this device
 // (16 is above the portable cluster size of 8); asked once per device and kernel,
 // never while `stream` is being captured into a graph (the answer is then 0 for
-// that launch, which runs with clusters of 8).
+// that launch, which runs with clusters of 8).  Host threads may race on the
+// first call: the cache is filled under a mutex.
 template <typename Kern>
 int cluster16_capacity(Kern kern, int nt_index, cudaStream_t stream) {
   static int known[64][2] = {};  // 0 unknown, else 1 + the number of resident clusters
+  static std::mutex known_mutex;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(known_mutex);
   int& k = known[dev][nt_index];
   if (k == 0) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;

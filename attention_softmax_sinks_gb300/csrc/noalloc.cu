@@ -9,9 +9,14 @@
 // sink_attn_decode + sink_attn_merge exchange, so this entry point keeps them in
 // a fixed, file-scope device array instead.
 //
-// The array (kScratchFloats floats, 8 MiB) is part of the library image: every
-// GPU on which the library is loaded holds it until the process exits.  All
-// calls on a device share it and it keeps the previous call's contents; every
+// The array (kScratchFloats floats, 8 MiB) belongs to the library's device code:
+// under CUDA's lazy module loading (the default) it is created on a device when
+// the library's code is first used there (at the latest by this entry point's
+// first call on that device, which also looks up its address), and the device
+// then holds it until the process exits.  That first call loads code and must
+// not happen while the stream is being captured into a graph, so make it once
+// before any capture.  All calls on a device share the array and it keeps the
+// previous call's contents; every
 // element a call reads is written earlier in the same call (each split writes
 // its whole partial, empty splits included), so nothing needs clearing.  Two
 // calls that overlap on the GPU (different streams, no ordering) race on it.

@@ -156,8 +156,10 @@ sa_status sink_attn_merge(const float* partial_o, const float* partial_lse, int 
  * its hot path because cudaMalloc may synchronise or fail).  Those callers
  * cannot supply the fp32 partials that sink_attn_decode and sink_attn_merge
  * exchange, so this call keeps them in a fixed device array inside the library
- * (8 MiB, 2,097,152 floats, held on every GPU where the library is loaded
- * until the process exits).
+ * (8 MiB, 2,097,152 floats).  Under CUDA's lazy module loading (the default)
+ * the array is created on a device when the library's device code is first
+ * used there, at the latest by this call's first use on that device, and is
+ * then held until the process exits.
  *
  *  Arguments are those of sink_attn_decode, but `out` is always the final
  *  bf16 [batch, num_qo_heads, head_dim] and `lse` the final fp32
@@ -166,8 +168,9 @@ sa_status sink_attn_merge(const float* partial_o, const float* partial_lse, int 
  *  otherwise SA_ERR_CAPACITY and nothing is launched.  num_splits == 1 needs
  *  no scratch and behaves exactly like sink_attn_decode.
  *  No cudaMalloc, cudaFree or other allocation happens in this call.  The first
- *  call on each device looks up the array's device address (a runtime query,
- *  not an allocation); make that first call before any stream capture.
+ *  call on each device may load the library's device code there and looks up
+ *  the array's device address (a runtime query, not an allocation); because of
+ *  that module load, make that first call before any stream capture.
  *  Every call shares the array, which keeps the previous call's contents; a
  *  call writes every element it later reads, so nothing needs clearing, but
  *  two calls that overlap on the GPU race on it: order them on one stream.
