@@ -1,18 +1,20 @@
 """Benchmark of the sink-attention hot path on GB300.
 
-One step = one pass of the decode path over the paged-decode workload
-(64 sequences x 4096 cached tokens, 64 query / 8 KV heads, head_dim 64, page
-size 16, seeded random page permutation): sink_attn_decode (split KV) then
-sink_attn_merge.  Headline metric: algorithmic decode bytes per second
-(KV cache + q + out + lse + page table), reported with the decode kernel's
-fraction of the measured HBM copy bandwidth.  The same JSON line carries the
-causal-prefill measurement (4 x 8192 tokens, 64/8 heads) in TFLOP/s against
-the measured dense bf16 peak.
+One step = one pass of the decode path over the long-context workload (8
+sequences x 131072 cached tokens, 64 query / 8 KV heads, head_dim 64, page size
+16, seeded random page permutation): sink_attn_decode with 32 splits (the sink
+in split 0 only), then sink_attn_merge.  Headline metric: algorithmic decode
+bytes per second (KV cache + q + out + lse + page table), with the decode
+kernel's fraction of the measured HBM copy bandwidth.  The same JSON line
+carries the causal prefill (4 x 8192 tokens, 64/8 heads) in TFLOP/s against the
+measured dense bf16 peak, the ragged mixed batch, the 64 x 4096 paged decode,
+small-batch decode in a CUDA graph, the tiny prefill and the kernels around
+attention.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the fp64 CPU oracle on bounded samples of the same
-workload (host cores only).  For N > 1 (torchrun) every rank runs its own
+workload (every host core).  For N > 1 (torchrun) every rank runs its own
 replica on its own GPU; nothing is exchanged but the timing.
 """
 from __future__ import annotations
@@ -26,7 +28,8 @@ import subprocess
 import sys
 import time
 
-# The CPU baseline runs the oracle single-threaded so that its core count is exact.
+# The CPU baseline runs the oracle on one thread per core, each with one BLAS thread,
+# so that the number of cores it uses is exact.
 os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
 os.environ.setdefault("OMP_NUM_THREADS", "1")
 os.environ.setdefault("MKL_NUM_THREADS", "1")
@@ -41,6 +44,8 @@ import workloads  # noqa: E402
 METRIC = "sink-attn prefill TFLOP/s & decode KV GB/s on 1 GB300, % of roofline"
 DECODE = workloads.WORKLOADS["paged_decode"]
 PREFILL = workloads.WORKLOADS["causal_prefill"]
+LONG = workloads.WORKLOADS["long_decode"]
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context for the measured-copy fraction)
 
 
 def peaks():
@@ -169,41 +174,27 @@ def run_ours(args, rank, world, device):
     sa.load_library()
     torch.cuda.set_device(device)
     pk = peaks()
-    cfg = DECODE
-    kv_lens = [cfg["kv_len"]] * cfg["batch"]
-    host = workloads.make_decode(cfg["seed"], kv_lens, cfg["hq"], cfg["hkv"], cfg["d"],
-                                 cfg["page_size"], cfg["sink_std"])
+    cfg = LONG
+    b, kvl, hq, hkv, d, s = cfg["batch"], cfg["kv_len"], cfg["hq"], cfg["hkv"], cfg["d"], cfg["num_splits"]
+    host = workloads.make_decode(cfg["seed"], [kvl] * b, hq, hkv, d, cfg["page_size"], cfg["sink_std"])
     names = ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")
     dev = {n: to_dev(host[n], torch, device) for n in names}
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    splits = sa.sink_attn_decode_splits(cfg["batch"], cfg["hkv"], cfg["kv_len"], cfg["page_size"], sms)
-    b, hq, d = cfg["batch"], cfg["hq"], cfg["d"]
-    part_o = torch.empty((b, splits, hq, d), dtype=torch.float32, device=device)
-    part_l = torch.empty((b, splits, hq), dtype=torch.float32, device=device)
+    part_o = torch.empty((b, s, hq, d), dtype=torch.float32, device=device)
+    part_l = torch.empty((b, s, hq), dtype=torch.float32, device=device)
     out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=device)
     lse = torch.empty((b, hq), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     max_pages = host["page_table"].shape[1]
-    alg_bytes = decode_bytes(b, cfg["kv_len"], hq, cfg["hkv"], d, max_pages)
+    alg_bytes = decode_bytes(b, kvl, hq, hkv, d, max_pages)
 
     def step(ev=None):
-        if splits > 1:
-            if ev is not None:
-                ev[0].record(stream)
-            sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
-                                dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=splits,
-                                out=part_o, lse=part_l, stream=stream)
-            if ev is not None:
-                ev[1].record(stream)
-            sa.sink_attn_merge(part_o, part_l, out=out, lse=lse, stream=stream)
-        else:
-            if ev is not None:
-                ev[0].record(stream)
-            sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
-                                dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=1,
-                                out=out, lse=lse, stream=stream)
-            if ev is not None:
-                ev[1].record(stream)
+        if ev is not None:
+            ev[0].record(stream)
+        sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"], dev["kv_lens"],
+                            dev["sinks"], cfg["sm_scale"], num_splits=s, out=part_o, lse=part_l, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        sa.sink_attn_merge(part_o, part_l, out=out, lse=lse, stream=stream)
 
     def barrier():
         if world > 1:
@@ -215,42 +206,38 @@ def run_ours(args, rank, world, device):
     barrier()
     clocks = ClockSampler(device.index if device.index is not None else 0)
     clocks.start()
-    # pass 1 (headline): K steps, events only at the ends of the timed region, so the
-    # merge can overlap the decode tail (programmatic dependent launch)
+    # one timed pass: events at both ends of the K steps and around every decode launch,
+    # so the decode kernel's time and the step time come from the same launches
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
     t_start.record(stream)
     for i in range(args.steps):
-        step()
+        step(evs[i])
     t_end.record(stream)
     barrier()
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
-    # pass 2 (roofline): the same K steps with CUDA events around every decode launch
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    barrier()
-    for i in range(args.steps):
-        step(evs[i])
-    barrier()
     clk = clocks.stop()
-    kern_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     ms_per_step = total_ms / args.steps
+    dec_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
     value = job_throughput(alg_bytes, world, ms_per_step)
-    dec_ms = sum(kern_ms) / len(kern_ms)
     achieved = alg_bytes / (dec_ms * 1e-3) / 1e9
-    launches_per_step = 2 if splits > 1 else 1
     status = sa.sink_attn_device_status(True)
 
     # ---- end to end through the public API: pinned host inputs in, result out
-    pinned = {n: (torch.from_numpy(np.ascontiguousarray(host[n]).view(np.int16)).view(torch.bfloat16)
-                  if host[n].dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(host[n]))
-                  ).pin_memory() for n in names}
+    def pin(x):
+        x = np.ascontiguousarray(x)
+        t = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) if x.dtype == np.uint16 else torch.from_numpy(x)
+        return t.pin_memory()
+
+    pinned = {n: pin(host[n]) for n in names}
     h_out = torch.empty((b, hq, d), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty((b, hq), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
-    e2e_steps = max(3, min(20, args.steps))
+    e2e_steps = max(3, min(10, args.steps))
 
     def e2e_step():
         for n in names:
@@ -268,63 +255,106 @@ def run_ours(args, rank, world, device):
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
-
-    # ---- causal prefill measured on its own (tensor-core bound kernel)
-    prefill = mixed = graph = around = long_dec = tiny = None
-    if not args.no_prefill:
-        prefill = bench_prefill(args, sa, torch, device, pk)
-        mixed = bench_mixed(args, sa, torch, device, pk)
-        tiny = bench_tiny_prefill(args, sa, torch, device, pk)
-        long_dec = bench_long_decode(args, sa, torch, device, pk)
-        graph = bench_graph_decode(args, sa, torch, device, pk)
-        around = bench_around_attention(args, sa, torch, device, pk)
-        around["linear_bias"] = bench_linear(args, sa, torch, device, pk)
+    del pinned, dev, part_o, part_l
+    torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks, random page permutation)",
-        "config": {"workload": "paged_decode: 64 seqs x 4096 cached tokens, 1 new token each, "
-                               "64 query / 8 KV heads, head_dim 64, page 16, permuted pages",
-                   "batch": b, "kv_len": cfg["kv_len"], "num_qo_heads": hq, "num_kv_heads": cfg["hkv"],
-                   "head_dim": d, "page_size": cfg["page_size"], "num_splits": splits,
-                   "step": ("sink_attn_decode (split KV, fp32 partials) + sink_attn_merge" if splits > 1 else
-                            "sink_attn_decode: KV of each (sequence, KV head) split across a CTA cluster, "
-                            "sink in split 0, log-sum-exp merge on chip through distributed shared memory"),
-                   "l2": "inputs larger than L2 (512 MiB KV cache per step, 129 MB L2)",
+        "config": {"workload": "long_decode: 8 seqs x 131072 cached tokens, 64/8 heads, head_dim 64, "
+                               "page 16, permuted pages, 32 splits + merge",
+                   "batch": b, "kv_len": kvl, "num_qo_heads": hq, "num_kv_heads": hkv, "head_dim": d,
+                   "page_size": cfg["page_size"], "num_splits": s,
+                   "step": "sink_attn_decode (32 splits, sink in split 0) + sink_attn_merge",
+                   "l2": "inputs larger than L2 (2 GiB KV per step, 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "algorithmic_bytes_per_step": alg_bytes},
         "roofline": {"bound": "hbm", "kernel": "sink_decode_kernel", "achieved": round(achieved, 1),
                      "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
-                     "peak_source": pk["source"] + " (hbm_gbs, copy bandwidth)",
-                     "traffic": recorded_traffic("sink_decode_kernel", ("decode.cu", "ptx.cuh", "internal.h")),
-                     "traffic_source": "profiles/traffic.txt (ncu capture of 32 of the 64 sequences, x2)",
+                     "peak_source": pk["source"] + " hbm_gbs (copy: read + write bytes)",
+                     "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": recorded_traffic("sink_decode_kernel_long", ("decode.cu", "ptx.cuh", "internal.h")),
+                     "traffic_source": "profiles/traffic.txt: ncu, 2 of 8 sequences, x4",
                      "kernel_ms": round(dec_ms, 5),
-                     "kernel_timing": "CUDA events around each decode launch in a second pass of the "
-                                      "same K steps (events between the two kernels would stop the "
-                                      "merge overlapping the decode tail in the headline pass)"},
+                     "kernel_timing": "events around each decode launch, same pass as ms_per_step"},
         "e2e": {"value": round(job_throughput(alg_bytes, world, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "pinned host -> device copies of every input, decode + merge, result -> host"},
-        "gpu_launches": launches_per_step * args.steps,
-        "gpu_launches_note": "headline pass only; the roofline pass launches the same number again",
+                "path": "pinned host inputs -> device, decode + merge, out + lse -> host"},
+        "gpu_launches": 2 * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "device_status": status,
     }
-    if prefill is not None:
-        line["prefill"] = prefill
-    if mixed is not None:
-        line["mixed"] = mixed
-    if tiny is not None:
-        line["tiny_prefill"] = tiny
-    if long_dec is not None:
-        line["long_decode"] = long_dec
-    if graph is not None:
-        line["small_batch_decode"] = graph
-    if around is not None:
+    if not args.no_prefill:
+        line["prefill"] = bench_prefill(args, sa, torch, device, pk)
+        line["mixed"] = bench_mixed(args, sa, torch, device, pk)
+        line["paged_decode"] = bench_paged_decode(args, sa, torch, device, pk)
+        line["small_batch_decode"] = bench_graph_decode(args, sa, torch, device, pk)
+        line["tiny_prefill"] = bench_tiny_prefill(args, sa, torch, device, pk)
+        around = bench_around_attention(args, sa, torch, device, pk)
+        around["linear_bias"] = bench_linear(args, sa, torch, device, pk)
         line["around_attention"] = around
-    return line
+    return line, host
+
+
+def bench_paged_decode(args, sa, torch, device, pk):
+    """Paged decode: 64 sequences x 4096 cached tokens (512 MiB of KV, larger than L2),
+    64/8 heads, the library's split count, decode then merge; events at the ends of the
+    steps and around each decode launch in the same pass."""
+    cfg = DECODE
+    b, kvl, hq, hkv, d = cfg["batch"], cfg["kv_len"], cfg["hq"], cfg["hkv"], cfg["d"]
+    host = workloads.make_decode(cfg["seed"], [kvl] * b, hq, hkv, d, cfg["page_size"], cfg["sink_std"])
+    dv = {n: to_dev(host[n], torch, device) for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    s = sa.sink_attn_decode_splits(b, hkv, kvl, cfg["page_size"], sms)
+    po = torch.empty((b, s, hq, d), dtype=torch.float32, device=device)
+    pl = torch.empty((b, s, hq), dtype=torch.float32, device=device)
+    out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((b, hq), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if s > 1:
+            sa.sink_attn_decode(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"], dv["kv_lens"],
+                                dv["sinks"], cfg["sm_scale"], num_splits=s, out=po, lse=pl, stream=stream)
+        else:
+            sa.sink_attn_decode(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"], dv["kv_lens"],
+                                dv["sinks"], cfg["sm_scale"], num_splits=1, out=out, lse=lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if s > 1:
+            sa.sink_attn_merge(po, pl, out=out, lse=lse, stream=stream)
+
+    for _ in range(5):
+        step()
+    reps = max(10, min(100, args.steps))
+    torch.cuda.synchronize(device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(reps):
+        step()
+    t1.record(stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize(device)
+    step_ms = t0.elapsed_time(t1) / reps
+    dec_ms = sum(a.elapsed_time(c) for a, c in evs) / reps
+    nbytes = decode_bytes(b, kvl, hq, hkv, d, dv["page_table"].shape[1])
+    del dv
+    torch.cuda.empty_cache()
+    ach = nbytes / (dec_ms * 1e-3) / 1e9
+    return {"workload": "paged_decode: 64 seqs x 4096 tokens, 64/8 heads, page 16, permuted pages",
+            "num_splits": s, "step_us": round(step_ms * 1e3, 2), "value": round(nbytes / (step_ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s", "kernel": "sink_decode_kernel", "kernel_us": round(dec_ms * 1e3, 2),
+            "achieved": round(ach, 1), "peak": pk["hbm"], "frac": round(ach / pk["hbm"], 4),
+            "frac_of_nominal_hbm": round(ach / NOMINAL_HBM_GBS, 4),
+            "kernel_timing": "events around each decode launch (separate pass; step_us has none)",
+            "traffic": recorded_traffic("sink_decode_kernel", ("decode.cu", "ptx.cuh", "internal.h")),
+            "gpu_launches": (2 if s > 1 else 1) * (2 * reps + 5)}
 
 
 def bench_mixed(args, sa, torch, device, pk):
@@ -368,13 +398,13 @@ def bench_mixed(args, sa, torch, device, pk):
     bound = "tensor" if t_tc >= t_hbm else "hbm"
     return {"workload": "ragged_mixed: 32 seqs, KV log-uniform in [1, 32768], half decode rows, "
                         "half 128-2048-token chunks, causal, 64/8 heads, page 16",
-            "tflops": round(flops / (ms * 1e-3) / 1e12, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-            "ms": round(ms, 4), "flops": flops, "bytes": nbytes, "decode_rows": int((q == 1).sum()),
-            "roofline": {"bound": bound, "frac": round(max(t_tc, t_hbm) / (ms * 1e-3), 4),
-                         "tensor_frac": round(t_tc / (ms * 1e-3), 4), "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
-                         "note": "frac = max(FLOPs / peak bf16, bytes / peak HBM) / time",
-                         "traffic": recorded_traffic("sink_prefill_kernel_mixed", ("prefill.cu", "ptx.cuh", "internal.h")),
-                         "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"},
+            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 4), "flops": flops, "bytes": nbytes,
+            "decode_rows": int((q == 1).sum()), "kernel": "sink_prefill_kernel", "bound": bound,
+            "frac": round(max(t_tc, t_hbm) / (ms * 1e-3), 4), "tensor_frac": round(t_tc / (ms * 1e-3), 4),
+            "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
+            "frac_rule": "max(FLOPs / peak bf16, bytes / peak HBM) / time",
+            "traffic": recorded_traffic("sink_prefill_kernel_mixed", ("prefill.cu", "ptx.cuh", "internal.h")),
             "gpu_launches": len(times)}
 
 
@@ -422,68 +452,9 @@ def bench_tiny_prefill(args, sa, torch, device, pk):
     tf = flops / (us_graph * 1e-6) / 1e12
     return {"workload": "tiny_prefill: 1 x 128 tokens, causal, 4 query / 1 KV head, head_dim 64",
             "us_per_call": round(us, 2), "us_per_call_graph": round(us_graph, 2), "flops": flops,
-            "roofline": {"bound": "tensor", "achieved": round(tf, 4), "peak": pk["bf16"], "unit": "TFLOP/s",
-                         "frac": round(tf / pk["bf16"], 6),
-                         "note": "latency bound (8.4 MFLOP per call); achieved from the graph replay"},
+            "bound": "tensor", "achieved": round(tf, 4), "peak": pk["bf16"], "unit": "TFLOP/s",
+            "frac": round(tf / pk["bf16"], 6), "note": "latency bound (8.4 MFLOP per call), graph replay",
             "gpu_launches": reps + 10 + 200}
-
-
-def bench_long_decode(args, sa, torch, device, pk):
-    """Long-context split decode: 8 sequences x 131072 cached tokens (2 GiB of KV, far larger
-    than L2), 64/8 heads, 32 splits then the merge; events around each decode launch."""
-    cfg = workloads.WORKLOADS["long_decode"]
-    b, kvl, hq, d = cfg["batch"], cfg["kv_len"], cfg["hq"], cfg["d"]
-    host = workloads.make_decode(cfg["seed"], [kvl] * b, hq, cfg["hkv"], d, cfg["page_size"], cfg["sink_std"])
-    dv = {n: to_dev(host[n], torch, device) for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
-    del host
-    s = cfg["num_splits"]
-    po = torch.empty((b, s, hq, d), dtype=torch.float32, device=device)
-    pl = torch.empty((b, s, hq), dtype=torch.float32, device=device)
-    out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=device)
-    lse = torch.empty((b, hq), dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
-
-    def decode():
-        sa.sink_attn_decode(dv["q"], dv["k_pages"], dv["v_pages"], dv["page_table"], dv["kv_lens"],
-                            dv["sinks"], cfg["sm_scale"], num_splits=s, out=po, lse=pl, stream=stream)
-
-    def step():
-        decode()
-        sa.sink_attn_merge(po, pl, out=out, lse=lse, stream=stream)
-
-    for _ in range(3):
-        step()
-    reps = max(5, min(30, args.steps // 10))
-    torch.cuda.synchronize(device)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(reps):
-        step()
-    t1.record(stream)
-    evs = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        decode()
-        e1.record(stream)
-        sa.sink_attn_merge(po, pl, out=out, lse=lse, stream=stream)
-        evs.append((e0, e1))
-    torch.cuda.synchronize(device)
-    step_ms = t0.elapsed_time(t1) / reps
-    dec_ms = sum(a.elapsed_time(c) for a, c in evs) / reps
-    nbytes = decode_bytes(b, kvl, hq, cfg["hkv"], d, dv["page_table"].shape[1])
-    ach = nbytes / (dec_ms * 1e-3) / 1e9
-    del dv
-    torch.cuda.empty_cache()
-    return {"workload": "long_decode: 8 seqs x 131072 cached tokens, 64/8 heads, page 16, permuted pages, "
-                        "32 splits + merge (2 GiB of KV per step, larger than L2)",
-            "num_splits": s, "step_us": round(step_ms * 1e3, 1), "gbs": round(nbytes / (step_ms * 1e-3) / 1e9, 1),
-            "roofline": {"bound": "hbm", "kernel": "sink_decode_kernel", "achieved": round(ach, 1),
-                         "peak": pk["hbm"], "unit": "GB/s", "frac": round(ach / pk["hbm"], 4),
-                         "kernel_us": round(dec_ms * 1e3, 1),
-                         "traffic": recorded_traffic("sink_decode_kernel_long", ("decode.cu", "ptx.cuh", "internal.h")),
-                         "traffic_source": "profiles/traffic.txt (ncu capture of 2 of the 8 sequences, x4)"},
-            "gpu_launches": 2 * (2 * reps + 3)}
 
 
 def bench_graph_decode(args, sa, torch, device, pk):
@@ -708,54 +679,82 @@ def bench_prefill(args, sa, torch, device, pk):
     ms = [a.elapsed_time(b) for a, b in times]
     avg = sum(ms) / len(ms)
     tflops = flops / (avg * 1e-3) / 1e12
-    return {"workload": "causal_prefill: 4 x 8192 tokens, causal, 64 query / 8 KV heads, head_dim 64, "
-                        "sinks N(0, 2), out + fp32 lse",
-            "value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(avg, 4),
-            "flops": flops, "l2": "flushed (256 MiB write, then read back) before every launch",
-            "roofline": {"bound": "tensor", "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2),
-                         "peak": pk["bf16"], "unit": "TFLOP/s", "frac": round(tflops / pk["bf16"], 4),
-                         "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)",
-                         "traffic": recorded_traffic("sink_prefill_kernel", ("prefill.cu", "ptx.cuh", "internal.h")),
-                         "traffic_unit": "bytes per launch",
-                         "traffic_source": "profiles/traffic.txt (ncu capture of 1 of the 4 sequences, x4)"},
+    return {"workload": "causal_prefill: 4 x 8192 tokens, causal, 64/8 heads, head_dim 64, sinks N(0, 2)",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(avg, 4), "flops": flops,
+            "bound": "tensor", "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2),
+            "peak": pk["bf16"], "frac": round(tflops / pk["bf16"], 4),
+            "peak_source": pk["source"] + " bf16_tflops (burst: kernel timed alone)",
+            "traffic": recorded_traffic("sink_prefill_kernel", ("prefill.cu", "ptx.cuh", "internal.h")),
+            "traffic_source": "profiles/traffic.txt: ncu, 1 of 4 sequences, x4",
+            "l2": "flushed (256 MiB written, read back) before every launch",
             "gpu_launches": steps}
 
 
 # ----------------------------------------------------------------------------- CPU baseline
-def oracle_decode_sample(units, host):
-    """Oracle time for the first `units` (sequence, KV head) groups; returns (seconds, bytes)."""
+def host_description():
+    """Core count and CPU model of this host (for the CPU-baseline records)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    import platform
+    return {"nproc": os.cpu_count() or 1, "cpu_model": model or platform.processor() or platform.machine(),
+            "machine": platform.machine()}
+
+
+def oracle_decode_groups(host, cfg, groups, workers):
+    """The oracle over (sequence, KV head) groups of a decode workload, on ``workers``
+    threads (one BLAS thread each); returns (seconds, algorithmic bytes)."""
     import oracle
-    cfg = DECODE
+    from concurrent.futures import ThreadPoolExecutor
     g = cfg["hq"] // cfg["hkv"]
-    t0 = time.perf_counter()
-    done = 0
-    nbytes = 0
-    for u in range(units):
-        b, kvh = divmod(u % (cfg["batch"] * cfg["hkv"]), cfg["hkv"])
+    nb = len(host["kv_lens"])
+
+    def one(u):
+        b, kvh = divmod(u % (nb * cfg["hkv"]), cfg["hkv"])
         kv = int(host["kv_lens"][b])
-        kb = oracle.widen_bf16(oracle.gather_pages(host["k_pages"], host["page_table"][b], kv)[:, kvh])
-        vb = oracle.widen_bf16(oracle.gather_pages(host["v_pages"], host["page_table"][b], kv)[:, kvh])
+        kb = oracle.widen_bf16(oracle.gather_pages(host["k_pages"][:, kvh:kvh + 1], host["page_table"][b], kv)[:, 0])
+        vb = oracle.widen_bf16(oracle.gather_pages(host["v_pages"][:, kvh:kvh + 1], host["page_table"][b], kv)[:, 0])
         qf = oracle.widen_bf16(host["q"][b, kvh * g:(kvh + 1) * g])
         for hh in range(g):
-            oracle.attention_with_sink(qf[hh][None], kb, vb, float(host["sinks"][kvh * g + hh]),
-                                       cfg["sm_scale"])
-        done += 1
-        nbytes += kv * cfg["d"] * 2 * 2 + g * cfg["d"] * 2 * 2 + g * 4
+            oracle.attention_with_sink(qf[hh][None], kb, vb, float(host["sinks"][kvh * g + hh]), cfg["sm_scale"])
+        return kv * cfg["d"] * 2 * 2 + g * cfg["d"] * 2 * 2 + g * 4
+
+    t0 = time.perf_counter()
+    if workers <= 1:
+        nbytes = sum(one(u) for u in groups)
+    else:
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            nbytes = sum(ex.map(one, groups))
     return time.perf_counter() - t0, nbytes
 
 
-def cpu_baseline(budget_s=12.0):
-    cfg = DECODE
-    host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * cfg["batch"], cfg["hq"], cfg["hkv"],
-                                 cfg["d"], cfg["page_size"], cfg["sink_std"])
-    oracle_decode_sample(1, host)                      # warm the code paths
-    t4, _ = oracle_decode_sample(4, host)
-    units = max(1, int(budget_s / max(t4 / 4, 1e-4)))  # wraps around the 512 groups
-    secs, nbytes = oracle_decode_sample(units, host)
-    groups = cfg["batch"] * cfg["hkv"]
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{units} (sequence, KV head) groups = {units / groups:.2f} passes over the "
-                      f"paged-decode workload, {secs:.1f} s, fp64 numpy, 1 thread"}
+def cpu_baseline(host, budget_s=12.0):
+    """The oracle on the headline workload (8 x 131072-token decode), every host core, on
+    a bounded sample of (sequence, KV head) groups."""
+    cfg = LONG
+    hd = host_description()
+    workers = hd["nproc"]
+    groups_total = len(host["kv_lens"]) * cfg["hkv"]
+    t1, _ = oracle_decode_groups(host, cfg, range(workers), workers)       # warm-up, one group per thread
+    rounds = max(1, int(budget_s / max(t1, 1e-3)))
+    secs, nbytes = oracle_decode_groups(host, cfg, range(rounds * workers), workers)
+    n = rounds * workers
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": workers, "kind": "oracle",
+            "sample": f"{n} (sequence, KV head) groups of the 8 x 131072 decode ({n / groups_total:.2f} passes), "
+                      f"{secs:.1f} s, fp64 numpy, {workers} threads x 1 BLAS thread",
+            "nproc": hd["nproc"], "cpu_model": hd["cpu_model"], "machine": hd["machine"],
+            "threads": workers, "blas_threads_per_thread": 1}
 
 
 def cpu_baselines_per_row(budget_s=3.0):
@@ -820,32 +819,33 @@ def cpu_baselines_per_row(budget_s=3.0):
 
 
 def run_reference(args):
-    cfg = DECODE
+    """The oracle as the reference arm: each step is one (sequence, KV head) group per host
+    core of the headline workload (8 x 131072-token decode), all cores busy."""
+    cfg = LONG
     host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * cfg["batch"], cfg["hq"], cfg["hkv"],
                                  cfg["d"], cfg["page_size"], cfg["sink_std"])
-    oracle_decode_sample(1, host)                      # warm the code paths
-    t4, _ = oracle_decode_sample(4, host)
-    per_step_budget = max(0.002, 150.0 / max(1, args.steps + args.warmup))
-    units = max(1, min(cfg["batch"] * cfg["hkv"], int(per_step_budget / max(t4 / 4, 1e-4))))
-    for _ in range(args.warmup):
-        oracle_decode_sample(units, host)
+    hd = host_description()
+    workers = hd["nproc"]
+    for w in range(args.warmup):
+        oracle_decode_groups(host, cfg, range(w * workers, (w + 1) * workers), workers)
     tot_s = 0.0
     tot_b = 0
-    for _ in range(args.steps):
-        s, nb = oracle_decode_sample(units, host)
-        tot_s += s
+    for k in range(args.steps):
+        secs, nb = oracle_decode_groups(host, cfg, range(k * workers, (k + 1) * workers), workers)
+        tot_s += secs
         tot_b += nb
     value = tot_b / tot_s / 1e9
-    sample = f"{units} (sequence, KV head) group(s) of the paged-decode workload per step, fp64 numpy, 1 thread"
+    sample = (f"{workers} (sequence, KV head) groups of the 8 x 131072 decode per step, fp64 numpy, "
+              f"{workers} threads x 1 BLAS thread")
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": "paged_decode: 64 seqs x 4096 cached tokens, 1 new token each, "
-                               "64 query / 8 KV heads, head_dim 64, page 16, permuted pages"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "config": {"workload": "long_decode: 8 seqs x 131072 cached tokens, 64/8 heads, head_dim 64, "
+                               "page 16, permuted pages, 32 splits + merge"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": workers, "kind": "oracle",
+                         "sample": sample, "nproc": hd["nproc"], "cpu_model": hd["cpu_model"]},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -971,16 +971,18 @@ def main():
     torch.cuda.set_device(device)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
-    line = run_ours(args, rank, world, device)
+    line, host = run_ours(args, rank, world, device)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(host)
             per_row = cpu_baselines_per_row()
             if "prefill" in line:
-                line["prefill"]["cpu_baseline"] = per_row["prefill"]
+                cb = per_row["prefill"]
+                line["prefill"].update({"cpu_baseline_value": cb["value"], "cpu_baseline_unit": cb["unit"],
+                                        "cpu_baseline_cores": cb["cores"], "cpu_baseline_sample": cb["sample"]})
             for key in ("qkv_bias_rope", "moe_router", "linear_bias"):
                 if "around_attention" in line and key in line["around_attention"]:
                     line["around_attention"][key]["cpu_baseline"] = per_row[key]
