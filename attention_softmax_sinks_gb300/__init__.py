@@ -23,7 +23,8 @@ __all__ = [
     "sink_attn_set_wait_timeout_ns", "sink_attn_status_string", "sink_attn_abi_version",
     "sink_attn_selftest_wait_timeout", "sink_attn_decode_noalloc", "moe_router_topk_softmax",
     "qkv_bias_rope", "qkv_bias_rope_append_paged", "linear_bias", "moe_router", "GPT_OSS_YARN",
-    "EXPORTED_SYMBOLS",
+    "EXPORTED_SYMBOLS", "qkv_bias_rope_kv", "qkv_bias_rope_append_paged_kv", "sink_attn_prefill_qkv",
+    "sink_attn_prefill_paged_qkv", "sink_attn_decode_qkv",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -35,7 +36,9 @@ EXPORTED_SYMBOLS = (
     "sink_attn_decode_splits", "sink_attn_device_status", "sink_attn_set_wait_timeout_ns",
     "sink_attn_status_string", "sink_attn_abi_version", "sink_attn_selftest_wait_timeout",
     "sink_attn_decode_noalloc", "moe_router_topk_softmax", "qkv_bias_rope",
-    "qkv_bias_rope_append_paged", "linear_bias", "moe_router",
+    "qkv_bias_rope_append_paged", "linear_bias", "moe_router", "qkv_bias_rope_kv",
+    "qkv_bias_rope_append_paged_kv", "sink_attn_prefill_qkv", "sink_attn_prefill_paged_qkv",
+    "sink_attn_decode_qkv",
 )
 
 _p, _i, _f, _d, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_longlong
@@ -59,6 +62,14 @@ _SIGNATURES = {
     "qkv_bias_rope": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p, _p, _p]),
     "qkv_bias_rope_append_paged": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p,
                                         _p, _p, _i, _i, _i, _p]),
+    "qkv_bias_rope_kv": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p, _p, _p]),
+    "qkv_bias_rope_append_paged_kv": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _d, _i, _d, _d, _p, _p,
+                                           _p, _i, _i, _i, _p, _p]),
+    "sink_attn_prefill_qkv": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p, _p]),
+    "sink_attn_prefill_paged_qkv": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i,
+                                         _i, _f, _i, _p, _p, _p]),
+    "sink_attn_decode_qkv": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _p,
+                                  _p]),
 }
 
 # YaRN constants of the public GPT-OSS model configuration (the pages name YaRN
@@ -473,3 +484,177 @@ def moe_router(x, w_router, bias, top_k: int, topk_idx=None, topk_weight=None, e
     if expert_counts is not None:
         return topk_idx, topk_weight, expert_counts
     return topk_idx, topk_weight
+
+
+# ----------------------------------------------------------------------------- q rotated on chip
+def qkv_bias_rope_kv(qkv, bias, cu_seqlens_q, num_qo_heads: int, num_kv_heads: int, kv_lens=None,
+                     rope=None, k_out=None, v_out=None, rope_table=None, stream=None):
+    """K/V half of qkv_bias_rope for the *_qkv attention calls: k (biased, rotated) and v
+    (biased) written contiguous [T, Hkv, 64] bf16, plus the per-token (cos, sin) table
+    [T, 32, 2] fp32 those calls apply to q.  Returns (k, v, rope_table)."""
+    _dev(qkv, "qkv", torch.bfloat16)
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    if bias is not None:
+        _dev(bias, "bias", torch.bfloat16)
+    if kv_lens is not None:
+        _dev(kv_lens, "kv_lens", torch.int32)
+    t = qkv.shape[0]
+    hq, hkv, d = int(num_qo_heads), int(num_kv_heads), 64
+    dv = qkv.device
+    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens)
+    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if k_out is None else k_out
+    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if v_out is None else v_out
+    rope_table = (torch.empty((t, d // 2, 2), dtype=torch.float32, device=dv) if rope_table is None
+                  else rope_table)
+    _out(k_out, "k_out", torch.bfloat16, (t, hkv, d), dv)
+    _out(v_out, "v_out", torch.bfloat16, (t, hkv, d), dv)
+    _out(rope_table, "rope_table", torch.float32, (t, d // 2, 2), dv)
+    with torch.cuda.device(dv):
+        st = load_library().qkv_bias_rope_kv(_ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens),
+                                             cu_seqlens_q.numel() - 1, t, hq, hkv, qkv.shape[1] // (hq + 2 * hkv),
+                                             *_rope_params(rope), _ptr(k_out), _ptr(v_out), _ptr(rope_table),
+                                             _stream(stream, dv))
+    _check(st, "qkv_bias_rope_kv")
+    return k_out, v_out, rope_table
+
+
+def qkv_bias_rope_append_paged_kv(qkv, bias, cu_seqlens_q, kv_lens, paged_k, paged_v, page_table,
+                                  num_qo_heads: int, rope=None, rope_table=None, stream=None):
+    """K/V half of qkv_bias_rope_append_paged: k and v written in place into the paged
+    cache at each new token's position, and the (cos, sin) table [T, 32, 2] fp32 of the
+    new tokens returned for the *_qkv attention calls."""
+    for name, x, dt in (("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("kv_lens", kv_lens, torch.int32), ("paged_k", paged_k, torch.bfloat16),
+                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32)):
+        _dev(x, name, dt)
+    if bias is not None:
+        _dev(bias, "bias", torch.bfloat16)
+    t = qkv.shape[0]
+    num_pages, hkv, page_size, d = paged_k.shape
+    hq = int(num_qo_heads)
+    dv = qkv.device
+    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, paged_k=paged_k,
+                 paged_v=paged_v, page_table=page_table)
+    rope_table = (torch.empty((t, d // 2, 2), dtype=torch.float32, device=dv) if rope_table is None
+                  else rope_table)
+    _out(rope_table, "rope_table", torch.float32, (t, d // 2, 2), dv)
+    with torch.cuda.device(dv):
+        st = load_library().qkv_bias_rope_append_paged_kv(
+            _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
+            qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(paged_k), _ptr(paged_v),
+            _ptr(page_table), page_size, page_table.shape[1], num_pages, _ptr(rope_table), _stream(stream, dv))
+    _check(st, "qkv_bias_rope_append_paged_kv")
+    return rope_table
+
+
+def sink_attn_prefill_qkv(qkv, qkv_bias, rope_table, k, v, sinks, cu_seqlens, max_seqlen: int,
+                          sm_scale: float, num_qo_heads: int, causal: bool = True, out=None, lse=None,
+                          return_lse: bool = True, stream=None):
+    """sink_attn_prefill with q taken from the projection output qkv [T, (Hq + 2 Hkv) * 64]:
+    the query bias and the rotation by rope_table (from qkv_bias_rope_kv) are applied on
+    chip; k, v as written by qkv_bias_rope_kv."""
+    for name, tns, dt in (("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
+                          ("k", k, torch.bfloat16), ("v", v, torch.bfloat16), ("sinks", sinks, torch.float32),
+                          ("cu_seqlens", cu_seqlens, torch.int32)):
+        _dev(tns, name, dt)
+    if qkv_bias is not None:
+        _dev(qkv_bias, "qkv_bias", torch.bfloat16)
+    t = qkv.shape[0]
+    hq = int(num_qo_heads)
+    _, hkv, d = k.shape
+    if k.shape != (t, hkv, d) or v.shape != k.shape or qkv.shape[1] != (hq + 2 * hkv) * d:
+        raise ValueError("qkv must be [T, (Hq + 2 Hkv) * D] and k, v [T, Hkv, D]")
+    if tuple(rope_table.shape) != (t, d // 2, 2):
+        raise ValueError(f"rope_table must be {(t, d // 2, 2)}")
+    dv = qkv.device
+    _same_device(dv, qkv_bias=qkv_bias, rope_table=rope_table, k=k, v=v, sinks=sinks, cu_seqlens=cu_seqlens)
+    out = (torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if out is None
+           else _out(out, "out", torch.bfloat16, (t, hq, d), dv))
+    if lse is None and return_lse:
+        lse = torch.empty((t, hq), dtype=torch.float32, device=dv)
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, (t, hq), dv)
+    with torch.cuda.device(dv):
+        st = load_library().sink_attn_prefill_qkv(
+            _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens),
+            cu_seqlens.numel() - 1, t, int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)),
+            _ptr(out), _ptr(lse), _stream(stream, dv))
+    _check(st, "sink_attn_prefill_qkv")
+    return out, lse
+
+
+def sink_attn_prefill_paged_qkv(qkv, qkv_bias, rope_table, paged_k, paged_v, page_table, cu_seqlens_q,
+                                kv_lens, sinks, max_q_len: int, sm_scale: float, num_qo_heads: int,
+                                causal: bool = True, out=None, lse=None, return_lse: bool = True,
+                                stream=None):
+    """sink_attn_prefill_paged with q taken from the projection output (see
+    sink_attn_prefill_qkv); the paged cache and rope_table as written by
+    qkv_bias_rope_append_paged_kv."""
+    for name, tns, dt in (("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
+                          ("paged_k", paged_k, torch.bfloat16), ("paged_v", paged_v, torch.bfloat16),
+                          ("page_table", page_table, torch.int32), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                          ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)):
+        _dev(tns, name, dt)
+    if qkv_bias is not None:
+        _dev(qkv_bias, "qkv_bias", torch.bfloat16)
+    t = qkv.shape[0]
+    hq = int(num_qo_heads)
+    num_pages, hkv, page_size, d = paged_k.shape
+    if qkv.shape[1] != (hq + 2 * hkv) * d or tuple(rope_table.shape) != (t, d // 2, 2):
+        raise ValueError("qkv must be [T, (Hq + 2 Hkv) * D] and rope_table [T, D / 2, 2]")
+    dv = qkv.device
+    _same_device(dv, qkv_bias=qkv_bias, rope_table=rope_table, paged_k=paged_k, paged_v=paged_v,
+                 page_table=page_table, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, sinks=sinks)
+    out = (torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if out is None
+           else _out(out, "out", torch.bfloat16, (t, hq, d), dv))
+    if lse is None and return_lse:
+        lse = torch.empty((t, hq), dtype=torch.float32, device=dv)
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, (t, hq), dv)
+    with torch.cuda.device(dv):
+        st = load_library().sink_attn_prefill_paged_qkv(
+            _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(paged_k), _ptr(paged_v), _ptr(page_table),
+            _ptr(cu_seqlens_q), _ptr(kv_lens), _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq,
+            hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out),
+            _ptr(lse), _stream(stream, dv))
+    _check(st, "sink_attn_prefill_paged_qkv")
+    return out, lse
+
+
+def sink_attn_decode_qkv(qkv, qkv_bias, rope_table, paged_k, paged_v, page_table, kv_lens, sinks,
+                         sm_scale: float, num_qo_heads: int, num_splits: int = 1, out=None, lse=None,
+                         return_lse: bool = True, stream=None):
+    """sink_attn_decode with q taken from the projection output qkv [B, (Hq + 2 Hkv) * 64] (one
+    new token per sequence): bias and rotation by row b of rope_table [B, 32, 2] applied in
+    the kernel.  num_splits > 1 returns the fp32 partials, as sink_attn_decode does."""
+    for name, tns, dt in (("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
+                          ("paged_k", paged_k, torch.bfloat16), ("paged_v", paged_v, torch.bfloat16),
+                          ("page_table", page_table, torch.int32), ("kv_lens", kv_lens, torch.int32),
+                          ("sinks", sinks, torch.float32)):
+        _dev(tns, name, dt)
+    if qkv_bias is not None:
+        _dev(qkv_bias, "qkv_bias", torch.bfloat16)
+    b = qkv.shape[0]
+    hq = int(num_qo_heads)
+    num_pages, hkv, page_size, d = paged_k.shape
+    if qkv.shape[1] != (hq + 2 * hkv) * d or tuple(rope_table.shape) != (b, d // 2, 2):
+        raise ValueError("qkv must be [B, (Hq + 2 Hkv) * D] and rope_table [B, D / 2, 2]")
+    dv = qkv.device
+    _same_device(dv, qkv_bias=qkv_bias, rope_table=rope_table, paged_k=paged_k, paged_v=paged_v,
+                 page_table=page_table, kv_lens=kv_lens, sinks=sinks)
+    s = int(num_splits)
+    out_shape, out_dtype = ((b, hq, d), torch.bfloat16) if s == 1 else ((b, s, hq, d), torch.float32)
+    lse_shape = (b, hq) if s == 1 else (b, s, hq)
+    out = (torch.empty(out_shape, dtype=out_dtype, device=dv) if out is None
+           else _out(out, "out", out_dtype, out_shape, dv))
+    if lse is None and (return_lse or s > 1):
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dv)
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, lse_shape, dv)
+    with torch.cuda.device(dv):
+        st = load_library().sink_attn_decode_qkv(
+            _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(paged_k), _ptr(paged_v), _ptr(page_table),
+            _ptr(kv_lens), _ptr(sinks), b, hq, hkv, d, page_size, page_table.shape[1], num_pages,
+            float(sm_scale), s, _ptr(out), _ptr(lse), _stream(stream, dv))
+    _check(st, "sink_attn_decode_qkv")
+    return out, lse

@@ -62,13 +62,16 @@ sa_status encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return SA_OK;
 }
 
-// [rows, heads, 64] bf16 tensor read in boxes of (box_rows tokens, box_heads heads, 64 dims).
+// [rows, heads, 64] bf16 tensor read in boxes of (box_rows tokens, box_heads heads, 64 dims);
+// consecutive tokens are row_heads head rows apart (heads when 0: a dense tensor; more for
+// the query heads inside a [T, (Hq + 2 Hkv) * 64] projection output).
 sa_status map_tokens_heads(CUtensorMap* m, const void* base, long long rows, int heads,
-                           int box_rows, int box_heads = 1) {
+                           int box_rows, int box_heads = 1, int row_heads = 0) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   if (sa_status s = encoder(&enc)) return s;
+  if (row_heads <= 0) row_heads = heads;
   cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(heads) * 64 * 2};
+  cuuint64_t strides[2] = {64 * 2, static_cast<cuuint64_t>(row_heads) * 64 * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
@@ -199,10 +202,12 @@ sa_status rope_common(const void* qkv, const void* bias, const int32_t* cu_q, co
                       int batch, int total_tokens, int hq, int hkv, int head_dim, double base,
                       double factor, int orig_len, double beta_fast, double beta_slow, void* q_out,
                       void* k_out, void* v_out, const int32_t* page_table, int max_pages,
-                      int num_pages, bool paged, cudaStream_t stream) {
+                      int num_pages, bool paged, cudaStream_t stream, bool kv_only = false,
+                      float* table_out = nullptr) {
   if (batch < 0 || total_tokens < 0) return SA_ERR_SHAPE;
   const bool work = batch > 0 && total_tokens > 0;  // empty tensors may carry NULL pointers
-  if (work && (!qkv || !cu_q || !q_out)) return SA_ERR_NULL;
+  if (work && (!qkv || !cu_q || (!kv_only && !q_out))) return SA_ERR_NULL;
+  if (work && kv_only && (!k_out || !v_out || !table_out)) return SA_ERR_NULL;
   if (work && paged && (!kv_lens || !page_table || !k_out || !v_out)) return SA_ERR_NULL;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return SA_ERR_SHAPE;
   if (head_dim != sa::kHeadDim) return SA_ERR_UNSUPPORTED;
@@ -210,7 +215,7 @@ sa_status rope_common(const void* qkv, const void* bias, const int32_t* cu_q, co
   if (paged && (max_pages <= 0 || num_pages <= 0)) return SA_ERR_SHAPE;
   if (static_cast<long long>(total_tokens) * (hq + 2 * hkv) * sa::kHeadDim >= (1LL << 40))
     return SA_ERR_SHAPE;
-  const void* ptrs[] = {qkv, bias, q_out, k_out, v_out};
+  const void* ptrs[] = {qkv, bias, kv_only ? nullptr : q_out, k_out, v_out, table_out};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return SA_ERR_ALIGNMENT;
   sa::RopeArgs a{};
@@ -223,7 +228,9 @@ sa_status rope_common(const void* qkv, const void* bias, const int32_t* cu_q, co
   a.bias = static_cast<const uint16_t*>(bias);
   a.cu_q = cu_q;
   a.kv_lens = kv_lens;
-  a.q_out = static_cast<uint16_t*>(q_out);
+  a.q_out = kv_only ? nullptr : static_cast<uint16_t*>(q_out);
+  a.table_out = table_out;
+  a.kv_only = kv_only ? 1 : 0;
   a.k_out = static_cast<uint16_t*>(k_out);
   a.v_out = static_cast<uint16_t*>(v_out);
   a.page_table = page_table;
@@ -315,12 +322,19 @@ int sink_attn_decode_splits(int batch, int num_kv_heads, int max_kv_len, int pag
   return static_cast<int>(s);
 }
 
-sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged_v,
-                           const int32_t* page_table, const int32_t* kv_lens, const float* sinks,
-                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
-                           int page_size, int max_pages, int num_pages, float sm_scale,
-                           int num_splits, void* out, float* lse, cudaStream_t stream) {
+}  // extern "C"
+
+// rope.table != nullptr: q is the projection output [B, (Hq + 2 Hkv) * 64] and the kernel
+// adds rope.q_bias (nullable) and rotates each sequence's query rows by its table row.
+static sa_status decode_common(const void* q, const void* paged_k, const void* paged_v,
+                               const int32_t* page_table, const int32_t* kv_lens, const float* sinks,
+                               int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                               int page_size, int max_pages, int num_pages, float sm_scale,
+                               int num_splits, void* out, float* lse, cudaStream_t stream,
+                               const sa::DecodeRopeArgs& rope) {
   if (!q || !paged_k || !paged_v || !page_table || !kv_lens || !sinks || !out) return SA_ERR_NULL;
+  if (rope.table && (!aligned16(rope.table) || (rope.q_bias && !aligned16(rope.q_bias))))
+    return SA_ERR_ALIGNMENT;
   if (num_splits > 1 && !lse) return SA_ERR_NULL;
   if (batch < 0 || max_pages <= 0 || num_pages <= 0) return SA_ERR_SHAPE;
   if (num_splits < 1 || num_splits > 256) return SA_ERR_SHAPE;
@@ -353,7 +367,34 @@ sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged
   CUtensorMap km, vm;
   if (sa_status s = map_pages(&km, paged_k, num_pages, num_kv_heads)) return s;
   if (sa_status s = map_pages(&vm, paged_v, num_pages, num_kv_heads)) return s;
-  return sa::launch_decode(km, vm, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+  return sa::launch_decode(km, vm, a, rope, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+}
+
+extern "C" {
+
+sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged_v,
+                           const int32_t* page_table, const int32_t* kv_lens, const float* sinks,
+                           int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                           int page_size, int max_pages, int num_pages, float sm_scale,
+                           int num_splits, void* out, float* lse, cudaStream_t stream) {
+  return decode_common(q, paged_k, paged_v, page_table, kv_lens, sinks, batch, num_qo_heads,
+                       num_kv_heads, head_dim, page_size, max_pages, num_pages, sm_scale, num_splits,
+                       out, lse, stream, sa::DecodeRopeArgs{});
+}
+
+sa_status sink_attn_decode_qkv(const void* qkv, const void* qkv_bias, const float* rope_table,
+                               const void* paged_k, const void* paged_v, const int32_t* page_table,
+                               const int32_t* kv_lens, const float* sinks, int batch,
+                               int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                               int max_pages, int num_pages, float sm_scale, int num_splits,
+                               void* out, float* lse, cudaStream_t stream) {
+  if (!rope_table) return SA_ERR_NULL;
+  if (num_qo_heads > 0 && num_kv_heads > 0 && num_qo_heads + 2 * num_kv_heads > 128)
+    return SA_ERR_UNSUPPORTED;
+  sa::DecodeRopeArgs rope{static_cast<const uint16_t*>(qkv_bias), reinterpret_cast<const float2*>(rope_table)};
+  return decode_common(qkv, paged_k, paged_v, page_table, kv_lens, sinks, batch, num_qo_heads,
+                       num_kv_heads, head_dim, page_size, max_pages, num_pages, sm_scale, num_splits,
+                       out, lse, stream, rope);
 }
 
 sa_status sink_attn_merge(const float* partial_o, const float* partial_lse, int batch,
@@ -369,13 +410,18 @@ sa_status sink_attn_merge(const float* partial_o, const float* partial_lse, int 
   return sa::launch_merge(a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
+// rope_table != nullptr: q is the projection output [T, (Hq + 2 Hkv) * 64] and the kernel
+// adds q_bias (nullable) and rotates the query rows on chip.
 static sa_status prefill_common(const void* q, const void* k, const void* v,
                                 const int32_t* page_table, const int32_t* cu_q,
                                 const int32_t* kv_lens, const float* sinks, int batch,
                                 int total_q, int max_q, int hq, int hkv, int head_dim,
                                 int max_pages, int num_pages, float sm_scale, int causal,
-                                void* out, float* lse, cudaStream_t stream, bool paged) {
+                                void* out, float* lse, cudaStream_t stream, bool paged,
+                                const void* q_bias = nullptr, const float* rope_table = nullptr) {
   if (!q || !k || !v || !cu_q || !sinks || !out) return SA_ERR_NULL;
+  const bool rope = rope_table != nullptr;
+  if (rope && (!aligned16(rope_table) || (q_bias && !aligned16(q_bias)))) return SA_ERR_ALIGNMENT;
   if (paged && (!page_table || !kv_lens)) return SA_ERR_NULL;
   if (batch < 0 || total_q < 0 || max_q < 0) return SA_ERR_SHAPE;
   if (sa_status s = check_heads(hq, hkv, head_dim)) return s;
@@ -405,14 +451,18 @@ static sa_status prefill_common(const void* q, const void* k, const void* v,
   a.paged = paged ? 1 : 0;
   a.scale_log2 = sm_scale * kLog2e;
   a.timeout_ns = g_timeout_ns;
+  sa::PrefillRopeArgs ra{};
+  ra.q_bias = rope ? static_cast<const uint16_t*>(q_bias) : nullptr;
+  ra.table = rope ? reinterpret_cast<const float2*>(rope_table) : nullptr;
   if (sa_status s = status_ptr(&a.status)) return s;
+  const int q_row_heads = rope ? hq + 2 * hkv : hq;  // head rows between consecutive tokens of q
   CUtensorMap qm, qpm, km, vm, om;
-  if (sa_status s = map_tokens_heads(&qm, q, total_q, hq, 128)) return s;
+  if (sa_status s = map_tokens_heads(&qm, q, total_q, hq, 128, 1, q_row_heads)) return s;
   if (sa_status s = map_tokens_heads(&om, out, total_q, hq, 128)) return s;
   // packed short sequences (G = 4, 8, 16): boxes of 128 / G tokens x the G heads of a group
   const int group = hq / hkv;
   if (group >= 4 && 128 % group == 0) {
-    if (sa_status s = map_tokens_heads(&qpm, q, total_q, hq, 128 / group, group)) return s;
+    if (sa_status s = map_tokens_heads(&qpm, q, total_q, hq, 128 / group, group, q_row_heads)) return s;
   } else {
     qpm = qm;
   }
@@ -423,7 +473,7 @@ static sa_status prefill_common(const void* q, const void* k, const void* v,
     if (sa_status s = map_tokens_heads(&km, k, total_q, hkv, 128)) return s;
     if (sa_status s = map_tokens_heads(&vm, v, total_q, hkv, 128)) return s;
   }
-  return sa::launch_prefill(qm, qpm, km, vm, om, a, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
+  return sa::launch_prefill(qm, qpm, km, vm, om, a, ra, stream) == cudaSuccess ? SA_OK : SA_ERR_LAUNCH;
 }
 
 sa_status sink_attn_prefill(const void* q, const void* k, const void* v, const float* sinks,
@@ -448,6 +498,39 @@ sa_status sink_attn_prefill_paged(const void* q, const void* paged_k, const void
   return prefill_common(q, paged_k, paged_v, page_table, cu_seqlens_q, kv_lens, sinks, batch,
                         total_q_tokens, max_q_len, num_qo_heads, num_kv_heads, head_dim,
                         max_pages, num_pages, sm_scale, causal, out, lse, stream, true);
+}
+
+sa_status sink_attn_prefill_qkv(const void* qkv, const void* qkv_bias, const float* rope_table,
+                                const void* k, const void* v, const float* sinks,
+                                const int32_t* cu_seqlens, int batch, int total_tokens,
+                                int max_seqlen, int num_qo_heads, int num_kv_heads, int head_dim,
+                                float sm_scale, int causal, void* out, float* lse,
+                                cudaStream_t stream) {
+  if (!rope_table) return SA_ERR_NULL;
+  if (num_qo_heads > 0 && num_kv_heads > 0 && num_qo_heads + 2 * num_kv_heads > 128)
+    return SA_ERR_UNSUPPORTED;
+  return prefill_common(qkv, k, v, nullptr, cu_seqlens, nullptr, sinks, batch, total_tokens,
+                        max_seqlen, num_qo_heads, num_kv_heads, head_dim, 0, 0, sm_scale, causal,
+                        out, lse, stream, false, qkv_bias, rope_table);
+}
+
+sa_status sink_attn_prefill_paged_qkv(const void* qkv, const void* qkv_bias, const float* rope_table,
+                                      const void* paged_k, const void* paged_v,
+                                      const int32_t* page_table, const int32_t* cu_seqlens_q,
+                                      const int32_t* kv_lens, const float* sinks, int batch,
+                                      int total_q_tokens, int max_q_len, int num_qo_heads,
+                                      int num_kv_heads, int head_dim, int page_size, int max_pages,
+                                      int num_pages, float sm_scale, int causal, void* out,
+                                      float* lse, cudaStream_t stream) {
+  if (!rope_table) return SA_ERR_NULL;
+  if (page_size != sa::kPageSize && page_size > 0) return SA_ERR_UNSUPPORTED;
+  if (page_size <= 0) return SA_ERR_SHAPE;
+  if (num_qo_heads > 0 && num_kv_heads > 0 && num_qo_heads + 2 * num_kv_heads > 128)
+    return SA_ERR_UNSUPPORTED;
+  return prefill_common(qkv, paged_k, paged_v, page_table, cu_seqlens_q, kv_lens, sinks, batch,
+                        total_q_tokens, max_q_len, num_qo_heads, num_kv_heads, head_dim,
+                        max_pages, num_pages, sm_scale, causal, out, lse, stream, true, qkv_bias,
+                        rope_table);
 }
 
 sa_status linear_bias(const void* x, const void* w, const void* bias, int m, int n, int k,
@@ -562,6 +645,32 @@ sa_status qkv_bias_rope_append_paged(const void* qkv, const void* bias,
   return rope_common(qkv, bias, cu_seqlens_q, kv_lens, batch, total_tokens, num_qo_heads,
                      num_kv_heads, head_dim, rope_base, factor, orig_len, beta_fast, beta_slow,
                      q_out, paged_k, paged_v, page_table, max_pages, num_pages, true, stream);
+}
+
+sa_status qkv_bias_rope_kv(const void* qkv, const void* bias, const int32_t* cu_seqlens_q,
+                           const int32_t* kv_lens, int batch, int total_tokens, int num_qo_heads,
+                           int num_kv_heads, int head_dim, double rope_base, double factor,
+                           int orig_len, double beta_fast, double beta_slow, void* k_out,
+                           void* v_out, float* rope_table, cudaStream_t stream) {
+  return rope_common(qkv, bias, cu_seqlens_q, kv_lens, batch, total_tokens, num_qo_heads,
+                     num_kv_heads, head_dim, rope_base, factor, orig_len, beta_fast, beta_slow,
+                     nullptr, k_out, v_out, nullptr, 0, 0, false, stream, true, rope_table);
+}
+
+sa_status qkv_bias_rope_append_paged_kv(const void* qkv, const void* bias,
+                                        const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                        int batch, int total_tokens, int num_qo_heads,
+                                        int num_kv_heads, int head_dim, double rope_base,
+                                        double factor, int orig_len, double beta_fast,
+                                        double beta_slow, void* paged_k, void* paged_v,
+                                        const int32_t* page_table, int page_size, int max_pages,
+                                        int num_pages, float* rope_table, cudaStream_t stream) {
+  if (page_size != sa::kPageSize && page_size > 0) return SA_ERR_UNSUPPORTED;
+  if (page_size <= 0) return SA_ERR_SHAPE;
+  return rope_common(qkv, bias, cu_seqlens_q, kv_lens, batch, total_tokens, num_qo_heads,
+                     num_kv_heads, head_dim, rope_base, factor, orig_len, beta_fast, beta_slow,
+                     nullptr, paged_k, paged_v, page_table, max_pages, num_pages, true, stream, true,
+                     rope_table);
 }
 
 }  // extern "C"

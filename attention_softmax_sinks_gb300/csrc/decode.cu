@@ -25,6 +25,7 @@
 #include <mutex>
 #include "internal.h"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 
 namespace sa {
 namespace {
@@ -116,10 +117,11 @@ __device__ __noinline__ void cluster_merge(CtaState<NT>* cs, int csz, void* out_
   }
 }
 
-template <int NT>
+template <int NT, bool kRope>
 __global__ void __launch_bounds__(kWarps * 32)
     sink_decode_kernel(const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+                       const __grid_constant__ CUtensorMap vmap, const DecodeArgs a,
+                       const DecodeRopeArgs rope) {
   static_assert(sizeof(MergeArea<NT>) <= kCtaStateOffset, "merge area must fit before the CTA state");
   static_assert(kCtaStateOffset + sizeof(CtaState<NT>) <= kRingBytes, "CTA state must fit in the ring");
   extern __shared__ uint8_t smem_raw[];
@@ -225,18 +227,47 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   // Q^T fragments (B operand of S^T = K Q^T): lane holds head (lane/4) of each
   // 8-wide tile, dims kk*16 + 2*(lane%4) + {0,1} and +8.
+  // With q taken from the projection output (kRope), the lane adds the bias and rotates
+  // its pairs in registers (it holds dims d and d + 32 of its heads: fragments kk and
+  // kk + 2), with the arithmetic of the kernel that writes rotated q.
   uint32_t qf[NT][4][2];
+  const int q_row_heads = kRope ? a.hq + 2 * a.hkv : a.hq;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = nt * 8 + (lane >> 2);
     const bool ok = hh < G;
+    const int head = kvh * G + (ok ? hh : 0);
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        static_cast<const uint16_t*>(a.q) +
-        (static_cast<size_t>(b) * a.hq + kvh * G + (ok ? hh : 0)) * kHeadDim);
+        static_cast<const uint16_t*>(a.q) + (static_cast<size_t>(b) * q_row_heads + head) * kHeadDim);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       qf[nt][kk][0] = ok ? qrow[kk * 8 + (lane & 3)] : 0u;
       qf[nt][kk][1] = ok ? qrow[kk * 8 + 4 + (lane & 3)] : 0u;
+    }
+    if (kRope && ok) {
+      const uint32_t* brow = rope.q_bias ? reinterpret_cast<const uint32_t*>(rope.q_bias + head * kHeadDim) : nullptr;
+      const float4* cs = reinterpret_cast<const float4*>(rope.table + static_cast<size_t>(b) * (kHeadDim / 2));
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int w = kk * 8 + 4 * c + (lane & 3);  // 32-bit word: dims 2w, 2w + 1 (pair index)
+          float a0 = bf16_lo(qf[nt][kk][c]), a1 = bf16_hi(qf[nt][kk][c]);
+          float b0 = bf16_lo(qf[nt][kk + 2][c]), b1 = bf16_hi(qf[nt][kk + 2][c]);
+          if (brow) {
+            const uint32_t ba = brow[w], bb = brow[w + 16];
+            a0 += bf16_lo(ba);
+            a1 += bf16_hi(ba);
+            b0 += bf16_lo(bb);
+            b1 += bf16_hi(bb);
+          }
+          const float4 r = cs[w];  // (cos, sin) of pairs 2w and 2w + 1
+          rotate_pair(a0, b0, r.x, r.y);
+          rotate_pair(a1, b1, r.z, r.w);
+          qf[nt][kk][c] = pack_bf16x2(a0, a1);
+          qf[nt][kk + 2][c] = pack_bf16x2(b0, b1);
+        }
+      }
     }
   }
 
@@ -485,7 +516,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 // first call: the cache is filled under a mutex.
 template <typename Kern>
 int cluster16_capacity(Kern kern, int nt_index, cudaStream_t stream) {
-  static int known[64][2] = {};  // 0 unknown, else 1 + the number of resident clusters
+  static int known[64][4] = {};  // 0 unknown, else 1 + the number of resident clusters
   static std::mutex known_mutex;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
@@ -516,16 +547,18 @@ int cluster16_capacity(Kern kern, int nt_index, cudaStream_t stream) {
 }
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& args,
-                          cudaStream_t stream) {
+                          const DecodeRopeArgs& rope, cudaStream_t stream) {
   const size_t smem = decode_smem_bytes();
-  auto kern = args.group <= 8 ? sink_decode_kernel<1> : sink_decode_kernel<2>;
+  auto kern = rope.table ? (args.group <= 8 ? sink_decode_kernel<1, true> : sink_decode_kernel<2, true>)
+                         : (args.group <= 8 ? sink_decode_kernel<1, false> : sink_decode_kernel<2, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   DecodeArgs a = args;
   // clusters of 16 only while all of them can be resident at once (one per (sequence,
   // KV head)); beyond that, waiting clusters cost more than the larger split saves
   if (a.cluster > 8 &&
-      static_cast<long long>(a.batch) * a.hkv > cluster16_capacity(kern, args.group <= 8 ? 0 : 1, stream))
+      static_cast<long long>(a.batch) * a.hkv >
+          cluster16_capacity(kern, (args.group <= 8 ? 0 : 1) + (rope.table ? 2 : 0), stream))
     a.cluster = 8;
   const bool clustered = a.cluster > 1;
   const dim3 grid(clustered ? a.cluster : a.num_splits, a.hkv, a.batch);
@@ -545,7 +578,7 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = clustered ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
+  e = cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a, rope);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

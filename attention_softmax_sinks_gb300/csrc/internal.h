@@ -24,6 +24,14 @@ struct DecodeArgs {
   unsigned long long timeout_ns;
 };
 
+// Decode with q taken from the projection output [B, (Hq + 2 Hkv) * 64] (one new token per
+// sequence): the kernel adds q_bias ([Hq * 64] bf16, or nullptr) and rotates by row b of
+// table ([B, 32] (cos, sin) x temperature).  table == nullptr: q [B, Hq, 64] as given.
+struct DecodeRopeArgs {
+  const uint16_t* q_bias;
+  const float2* table;
+};
+
 struct MergeArgs {
   const float* partial_o;
   const float* partial_lse;
@@ -33,7 +41,7 @@ struct MergeArgs {
 };
 
 struct PrefillArgs {
-  const void* q;           // [T, Hq, 64]
+  const void* q;           // [T, Hq, 64], or the projection output (see PrefillRopeArgs)
   const int32_t* cu_q;     // [B + 1]
   const int32_t* kv_lens;  // [B] (paged) or nullptr (contiguous: kv_len == q_len)
   const int32_t* page_table;
@@ -46,15 +54,23 @@ struct PrefillArgs {
   unsigned long long timeout_ns;
 };
 
+// Prefill with q taken from the projection output [T, (Hq + 2 Hkv) * 64]: the kernel adds
+// q_bias ([Hq * 64] bf16, or nullptr) and rotates the rows by rope_table ([T, 32] (cos, sin)
+// x temperature) on chip.  table == nullptr: q is used as given.
+struct PrefillRopeArgs {
+  const uint16_t* q_bias;
+  const float2* table;
+};
+
 // Tensor maps (TMA descriptors) built on the host by abi.cu.
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
-                          cudaStream_t stream);
+                          const DecodeRopeArgs& rope, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 // qpmap: Q in boxes of (128 / group tokens, group heads), used for packed short sequences.
 // omap: the output [T, Hq, 64] mapped like qmap (boxes of 128 tokens x 1 head); full query
 // blocks are written through it with TMA stores.
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const CUtensorMap& omap, const PrefillArgs& a,
-                           cudaStream_t stream);
+                           const PrefillRopeArgs& rope, cudaStream_t stream);
 
 }  // namespace sa

@@ -43,6 +43,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 
 namespace sa {
 namespace {
@@ -64,6 +65,7 @@ struct __align__(1024) PrefillSmem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint64_t q_full[2];           // Q of the item landed                         (TMA tx)
+  uint64_t q_ready[2][2];       // fused q: [buffer][tile] the tile's Q rows biased and rotated (128 arrivals)
   uint64_t q_empty[2];          // the item's Q buffers are free again: its MMAs are done and the
                                 //   output staged there has been read by the TMA (1 arrival per tile)
   uint64_t kv_full[kStages];    // K_j and V_j landed                           (TMA tx)
@@ -248,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap qpmap,
                         const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
-                        const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
+                        const __grid_constant__ CUtensorMap omap, const PrefillArgs a,
+                        const PrefillRopeArgs rope) {
   extern __shared__ uint8_t smem_raw[];
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -374,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     n_items = pairs * sc.n_hg;
   }
-  // the one item of a non-persistent CTA
-  const WorkItem w0 = kPersistent ? WorkItem{} : item_at(a, sm, sc, blockIdx.x);
-  if (!kPersistent) {
+  // the one item of a non-persistent CTA: leave at once when it has no work
+  if constexpr (!kPersistent) {
+    const WorkItem w0 = item_at(a, sm, sc, blockIdx.x);
     if (w0.n_kv == 0) {
       if (threadIdx.x == 0 && w0.q0 == 0 && w0.h0 == 0) {
         int qs, q_len, kv_len;
@@ -391,6 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.q_full[i]), 1);
+      mbar_init(smem_u32(&sm.q_ready[i][0]), 128);
+      mbar_init(smem_u32(&sm.q_ready[i][1]), 128);
       mbar_init(smem_u32(&sm.q_empty[i]), ntiles);
     }
     for (int s = 0; s < kStages; ++s) {
@@ -425,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // sequence of the persistent schedule.  Stops when body returns false.
   auto for_items = [&](auto&& body) {
     if constexpr (!kPersistent) {
-      body(w0, 0, 0);
+      // recomputed in each role rather than kept live across the register split
+      body(item_at(a, sm, sc, blockIdx.x), 0, 0);
     } else {
       int it = 0, g = 0;
       for (int rr = 0;; ++rr) {
@@ -535,7 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_p = tmem + kColP + t * 64;
         for_items([&](const WorkItem& w, int it, int g) {
           const int qb = it & 1;
-          ok = wait_bar(smem_u32(&sm.q_full[qb]), (it >> 1) & 1, a.timeout_ns, abort_flag);
+          // fused q: the rows are ready once the softmax threads have biased and rotated them
+          ok = wait_bar(smem_u32(rope.table ? &sm.q_ready[qb][t] : &sm.q_full[qb]), (it >> 1) & 1,
+                        a.timeout_ns, abort_flag);
           if (!ok) return false;
           const uint32_t q_addr = smem_u32(q_tile(sm, qb, t));
           auto s_step = [&](int jj) {  // S_t(jj) = Q_t K_jj^T
@@ -608,6 +616,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = w.packed ? w.h0 + r % a.group : w.h0 + t;
         const int i = w.packed ? t * (kBlockQ / a.group) + r / a.group : w.q0 + r;
         const int limit = a.causal ? min(i + w.kv_len - w.q_len, w.kv_len - 1) : w.kv_len - 1;
+        if (rope.table) {
+          // Fused q: this thread's query row is the projection output as loaded; add the
+          // head's bias, rotate each feature pair (i, i + 32) by the token's (cos, sin) row of
+          // the table and round back to bf16 in place, before the tile's first S MMA (the
+          // arithmetic of the kernel that writes rotated q).  The table row and the bias are
+          // requested before the wait for Q, so they arrive while the Q copy lands.
+          const int qb = it & 1;
+          const bool live = i < w.q_len;
+          float4 cs[16];
+          uint4 bias[8];
+          const uint4* brow = reinterpret_cast<const uint4*>(rope.q_bias + h * kHeadDim);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) bias[e] = (live && rope.q_bias) ? __ldg(brow + e) : make_uint4(0, 0, 0, 0);
+          const float4* crow = reinterpret_cast<const float4*>(
+              rope.table + (static_cast<long long>(w.q_start) + (live ? i : 0)) * (kHeadDim / 2));
+#pragma unroll
+          for (int e = 0; e < 16; ++e) cs[e] = live ? __ldg(crow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!wait_bar(smem_u32(&sm.q_full[qb]), (it >> 1) & 1, a.timeout_ns, abort_flag)) return ok = false;
+          // tile 1 waits for tile 0's rows, so tile 0 (whose first S MMA comes first) is not
+          // slowed by tile 1's transform; tile 1 starts a softmax phase later anyway
+          if (t == 1 && !wait_bar(smem_u32(&sm.q_ready[qb][0]), (it >> 1) & 1, a.timeout_ns, abort_flag))
+            return ok = false;
+          if (live) {
+            uint8_t* row = q_tile(sm, qb, t) + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // features [8j, 8j + 8) and their partners [8j + 32, 8j + 40)
+              uint4* p1 = reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4));
+              uint4* p2 = reinterpret_cast<uint4*>(row + (((j + 4) ^ (r & 7)) << 4));
+              float y1[8], y2[8];
+              widen8(*p1, y1);
+              widen8(*p2, y2);
+              if (rope.q_bias) {
+                add_bias8(y1, bias[j]);
+                add_bias8(y2, bias[j + 4]);
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) rotate2(y1, y2, e, cs[4 * j + e]);
+              *p1 = pack8(y1);
+              *p2 = pack8(y2);
+            }
+          }
+          fence_proxy_async_smem();  // the rows are read by the tensor core (async proxy)
+          mbar_arrive(smem_u32(&sm.q_ready[qb][t]));
+        }
         const float sink = a.sinks[h] * kLog2e;
         float m = sink;                                 // running max (log2 units)
         float d = (sink == kNegInf) ? 0.0f : 1.0f;      // running denominator
@@ -786,7 +838,7 @@ int g_prefill_sms[64] = {};
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const CUtensorMap& omap, const PrefillArgs& a,
-                           cudaStream_t stream) {
+                           const PrefillRopeArgs& rope, cudaStream_t stream) {
   const int tiles = (a.group % 2 == 0) ? 2 : 1;
   const int n_qb = (a.max_q + kBlockQ - 1) / kBlockQ;
   const long long items = static_cast<long long>(n_qb) * (a.hq / tiles) * a.batch;
@@ -822,7 +874,7 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, qmap, qpmap, kmap, vmap, omap, a);
+  e = cudaLaunchKernelEx(&cfg, kern, qmap, qpmap, kmap, vmap, omap, a, rope);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -21,10 +21,15 @@
 // head row and one quarter j of its features: features [8j, 8j + 8) and their
 // rotation partners [8j + 32, 8j + 40), read from the tile as two 16-byte
 // vectors, so no lane exchange is needed; its bias values are loaded once.
+//
+// K/V-only mode (for the attention calls that rotate Q themselves): only the
+// K and V rows of each token are copied and written, and the (cos, sin) table
+// of every token goes to `table_out`, where those calls read it.
 #include <cmath>
 #include <cstdint>
 
 #include "rope_args.h"
+#include "rope_math.cuh"
 #include "ptx.cuh"
 
 namespace sa {
@@ -35,23 +40,6 @@ constexpr int kRopeTileBytes = 65536;  // input tile of a CTA: as many whole tok
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 constexpr unsigned long long kDrainTimeoutNs = 2000000000ull;
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ void widen8(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = bf16_lo(w[i]);
-    f[2 * i + 1] = bf16_hi(w[i]);
-  }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
-}
 
 // Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
 // from global memory into this CTA's shared memory, completing on mbarrier `bar`.
@@ -77,17 +65,20 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
   __shared__ float4 cs4[kMaxRopeTokens][kMaxRopePairs / 2];  // (cos, sin) of pairs 2i, 2i + 1
   __shared__ long long dst_row[kMaxRopeTokens];  // paged: page * Hkv * 16 + slot; contiguous: token
   __shared__ uint64_t full;
-  const int rows = a.hq + 2 * a.hkv;
+  const int all_rows = a.hq + 2 * a.hkv;
+  const int first_row = a.kv_only ? a.hq : 0;  // head rows of a token this kernel handles
+  const int rows = all_rows - first_row;
   const int units = rows * 4;
   const int tid = threadIdx.x;
   const int unit = tid % units;
   const int lane_tok = tid / units;  // < tpar
-  const int row = unit >> 2;
+  const int row = first_row + (unit >> 2);  // head row within the token's qkv row
   const int j = unit & 3;
   const int per_cta = rope_tokens_per_cta(rows);
   const int t0 = blockIdx.x * per_cta;
   const int ntok = min(per_cta, a.total_tokens - t0);
-  const uint32_t token_bytes = static_cast<uint32_t>(rows) * 128u;
+  const uint32_t token_bytes = static_cast<uint32_t>(rows) * 128u;      // copied per token
+  const uint32_t src_token_bytes = static_cast<uint32_t>(all_rows) * 128u;
   const uint32_t bar = smem_u32(&full);
 
   // The CTA's tokens are contiguous in qkv: one bulk copy per token into shared
@@ -97,10 +88,11 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
     fence_barrier_init();
     mbar_arrive_expect_tx(bar, token_bytes * ntok);
     const uint64_t policy = l2_policy_evict_first();  // read once
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.qkv) + static_cast<size_t>(t0) * token_bytes;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.qkv) + static_cast<size_t>(t0) * src_token_bytes +
+                         static_cast<size_t>(first_row) * 128u;
     for (int tok = 0; tok < ntok; ++tok)
-      bulk_load(smem_u32(tile + tok * token_bytes), src + static_cast<size_t>(tok) * token_bytes, token_bytes,
-                bar, policy);
+      bulk_load(smem_u32(tile + tok * token_bytes), src + static_cast<size_t>(tok) * src_token_bytes,
+                token_bytes, bar, policy);
   }
   float b1[8], b2[8];
   const long long col = static_cast<long long>(row) * kHeadDim + 8 * j;
@@ -133,6 +125,9 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
     sincosf(static_cast<float>(red), &sn, &cn);
     cs[(tok * kMaxRopePairs + pair) * 2] = cn * a.mscale;
     cs[(tok * kMaxRopePairs + pair) * 2 + 1] = sn * a.mscale;
+    if (a.table_out)
+      reinterpret_cast<float2*>(a.table_out)[static_cast<long long>(t) * kMaxRopePairs + pair] =
+          make_float2(cn * a.mscale, sn * a.mscale);
     if (pair == 0) {
       long long dst = t;
       if (a.paged) {
@@ -164,7 +159,7 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
   for (int tok = lane_tok; tok < ntok; tok += tpar) {
     // Odd rows read their second half first: the two rows of a quarter-warp then
     // fall in different banks (bytes [0, 64) and [64, 128) of a row) at each load.
-    const uint8_t* src = tile + tok * token_bytes + row * 128 + 16 * j;
+    const uint8_t* src = tile + tok * token_bytes + (row - first_row) * 128 + 16 * j;
     const int first = (row & 1) * 64;
     const uint4 u_first = *reinterpret_cast<const uint4*>(src + first);
     const uint4 u_second = *reinterpret_cast<const uint4*>(src + (64 - first));
@@ -176,22 +171,9 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
       y1[i] += b1[i];
       y2[i] += b2[i];
     }
-    float o1[8], o2[8];
     if (rotate) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 r = cs4[tok][4 * j + i];  // pairs 8j + 2i and 8j + 2i + 1
-        o1[2 * i] = fmaf(y1[2 * i], r.x, -y2[2 * i] * r.y);
-        o2[2 * i] = fmaf(y2[2 * i], r.x, y1[2 * i] * r.y);
-        o1[2 * i + 1] = fmaf(y1[2 * i + 1], r.z, -y2[2 * i + 1] * r.w);
-        o2[2 * i + 1] = fmaf(y2[2 * i + 1], r.z, y1[2 * i + 1] * r.w);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o1[i] = y1[i];
-        o2[i] = y2[i];
-      }
+      for (int i = 0; i < 4; ++i) rotate2(y1, y2, i, cs4[tok][4 * j + i]);  // pairs 8j + 2i, 8j + 2i + 1
     }
     const int t = t0 + tok;
     uint16_t* dst = nullptr;
@@ -205,8 +187,8 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
       dst = kv_dst + off + 8 * j;
     }
     if (dst) {
-      *reinterpret_cast<uint4*>(dst) = pack8(o1);
-      *reinterpret_cast<uint4*>(dst + 32) = pack8(o2);
+      *reinterpret_cast<uint4*>(dst) = pack8(y1);
+      *reinterpret_cast<uint4*>(dst + 32) = pack8(y2);
     }
   }
 }
@@ -214,7 +196,7 @@ __global__ void __launch_bounds__(512) qkv_rope_kernel(const RopeArgs a, int tpa
 }  // namespace
 
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t stream) {
-  const int rows = a.hq + 2 * a.hkv;
+  const int rows = a.kv_only ? 2 * a.hkv : a.hq + 2 * a.hkv;
   const int units = 4 * rows;
   const int per_cta = rope_tokens_per_cta(rows);
   int tpar = 256 / units;

@@ -295,6 +295,7 @@ def run_ours(args, rank, world, device):
         around = bench_around_attention(args, sa, torch, device, pk)
         around["linear_bias"] = bench_linear(args, sa, torch, device, pk)
         line["around_attention"] = around
+        line["fused_qkv_prefill"] = bench_fused_qkv(args, sa, torch, device, pk)
     return line, host
 
 
@@ -616,6 +617,44 @@ def bench_around_attention(args, sa, torch, device, pk):
                                                                           ("linear.cu", "linear_args.h", "ptx.cuh")),
                                               "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}},
             "gpu_launches": 2 * (reps + 3) + 3 * (reps + 3)}
+
+
+def bench_fused_qkv(args, sa, torch, device, pk):
+    """q taken from the QKV projection output and rotated inside the prefill, against the
+    separate rotation kernel, on the causal-prefill batch (4 x 8192 tokens, 64/8 heads):
+    unfused = qkv_bias_rope (writes q, k, v) + sink_attn_prefill; fused = qkv_bias_rope_kv
+    (writes k, v and the (cos, sin) table) + sink_attn_prefill_qkv.  L2 flushed before
+    each pair."""
+    stream = torch.cuda.current_stream(device)
+    t, hq, hkv = 32768, PREFILL["hq"], PREFILL["hkv"]
+    cu = to_dev(workloads.cu_seqlens_from([8192] * 4), torch, device)
+    inp = workloads.make_qkv(41, t, hq, hkv)
+    qkv, bias = to_dev(inp["qkv"], torch, device), to_dev(inp["bias"], torch, device)
+    sinks = to_dev(workloads.sinks_f32(0, hq, PREFILL["sink_std"]), torch, device)
+    q = torch.empty((t, hq, 64), dtype=torch.bfloat16, device=device)
+    k = torch.empty((t, hkv, 64), dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    table = torch.empty((t, 32, 2), dtype=torch.float32, device=device)
+    out = torch.empty_like(q)
+    lse = torch.empty((t, hq), dtype=torch.float32, device=device)
+    reps = max(5, min(20, args.steps))
+
+    def unfused():
+        sa.qkv_bias_rope(qkv, bias, cu, hq, hkv, q_out=q, k_out=k, v_out=v, stream=stream)
+        sa.sink_attn_prefill(q, k, v, sinks, cu, 8192, PREFILL["sm_scale"], out=out, lse=lse, stream=stream)
+
+    def fused():
+        sa.qkv_bias_rope_kv(qkv, bias, cu, hq, hkv, k_out=k, v_out=v, rope_table=table, stream=stream)
+        sa.sink_attn_prefill_qkv(qkv, bias, table, k, v, sinks, cu, 8192, PREFILL["sm_scale"], hq, out=out,
+                                 lse=lse, stream=stream)
+
+    un_ms = _timed_flushed(torch, device, stream, unfused, reps)
+    fu_ms = _timed_flushed(torch, device, stream, fused, reps)
+    return {"workload": "4 x 8192 tokens, 64/8 heads: QKV bias + YaRN + causal prefill, L2 flushed before each pair",
+            "unfused_us": round(un_ms * 1e3, 1), "fused_us": round(fu_ms * 1e3, 1),
+            "fused_over_unfused": round(fu_ms / un_ms, 4),
+            "unfused": "qkv_bias_rope + sink_attn_prefill", "fused": "qkv_bias_rope_kv + sink_attn_prefill_qkv",
+            "gpu_launches": 4 * (reps + 3)}
 
 
 def bench_linear(args, sa, torch, device, pk):

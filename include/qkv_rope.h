@@ -66,6 +66,33 @@ sa_status qkv_bias_rope_append_paged(const void* qkv, const void* bias,
                                      const int32_t* page_table, int page_size, int max_pages,
                                      int num_pages, cudaStream_t stream);
 
+/*
+ * K/V half of the step, for the attention calls that take q straight from the
+ * projection output and rotate it on chip (sink_attn_prefill_qkv,
+ * sink_attn_prefill_paged_qkv, sink_attn_decode_qkv in sink_attn.h).  Only
+ * the key and value rows of qkv are read; k and v are biased, k rotated, both
+ * written as by qkv_bias_rope (contiguous k_out, v_out bf16 [T, Hkv, 64]) or
+ * qkv_bias_rope_append_paged (into the paged cache); q is neither read nor
+ * written.  Also writes rope_table, fp32 [T, 32, 2]: for every new token t and
+ * feature pair i the rotation (mscale cos(p theta'_i), mscale sin(p theta'_i))
+ * applied to its k, which the attention call applies to its q.  Every
+ * pointer but bias (and kv_lens for the contiguous form) is required.
+ */
+sa_status qkv_bias_rope_kv(const void* qkv, const void* bias, const int32_t* cu_seqlens_q,
+                           const int32_t* kv_lens, int batch, int total_tokens, int num_qo_heads,
+                           int num_kv_heads, int head_dim, double rope_base, double factor,
+                           int orig_len, double beta_fast, double beta_slow, void* k_out,
+                           void* v_out, float* rope_table, cudaStream_t stream);
+
+sa_status qkv_bias_rope_append_paged_kv(const void* qkv, const void* bias,
+                                        const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                        int batch, int total_tokens, int num_qo_heads,
+                                        int num_kv_heads, int head_dim, double rope_base,
+                                        double factor, int orig_len, double beta_fast,
+                                        double beta_slow, void* paged_k, void* paged_v,
+                                        const int32_t* page_table, int page_size, int max_pages,
+                                        int num_pages, float* rope_table, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -134,6 +134,49 @@ sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged
                            int num_splits, void* out, float* lse, cudaStream_t stream);
 
 /*
+ * The same three calls with q taken straight from the QKV projection output,
+ * the query bias added and the YaRN rotation applied on chip (page "GPT-OSS on
+ * day 0", model overview list: QKV projections with biases, YaRN positions;
+ * the rotation itself is specified in qkv_rope.h).  The keys must already be
+ * biased and rotated in k / the paged cache, and the (cos, sin) table of the
+ * new tokens computed, by qkv_bias_rope_kv or qkv_bias_rope_append_paged_kv
+ * (qkv_rope.h); each query row then goes through the same arithmetic as in
+ * qkv_bias_rope, so the result equals qkv_bias_rope followed by the plain call.
+ *
+ *  qkv        bf16 [tokens, (num_qo_heads + 2 num_kv_heads) * head_dim], the
+ *             projection output without bias (query heads first); only the
+ *             query heads are read.  tokens = total_tokens / total_q_tokens /
+ *             batch (decode: one new token per sequence)
+ *  qkv_bias   bf16 [(num_qo_heads + 2 num_kv_heads) * head_dim] or NULL; only
+ *             the query part is read
+ *  rope_table fp32 [tokens, head_dim / 2, 2], as written by the _kv calls
+ *  other arguments as for the plain call; num_qo_heads + 2 num_kv_heads <= 128
+ *  (SA_ERR_UNSUPPORTED otherwise).  The prefills run their persistent
+ *  schedule, where an idle warp rotates the next item's query rows while the
+ *  current item computes.
+ */
+sa_status sink_attn_prefill_qkv(const void* qkv, const void* qkv_bias, const float* rope_table,
+                                const void* k, const void* v, const float* sinks,
+                                const int32_t* cu_seqlens, int batch, int total_tokens,
+                                int max_seqlen, int num_qo_heads, int num_kv_heads, int head_dim,
+                                float sm_scale, int causal, void* out, float* lse,
+                                cudaStream_t stream);
+sa_status sink_attn_prefill_paged_qkv(const void* qkv, const void* qkv_bias, const float* rope_table,
+                                      const void* paged_k, const void* paged_v,
+                                      const int32_t* page_table, const int32_t* cu_seqlens_q,
+                                      const int32_t* kv_lens, const float* sinks, int batch,
+                                      int total_q_tokens, int max_q_len, int num_qo_heads,
+                                      int num_kv_heads, int head_dim, int page_size, int max_pages,
+                                      int num_pages, float sm_scale, int causal, void* out,
+                                      float* lse, cudaStream_t stream);
+sa_status sink_attn_decode_qkv(const void* qkv, const void* qkv_bias, const float* rope_table,
+                               const void* paged_k, const void* paged_v, const int32_t* page_table,
+                               const int32_t* kv_lens, const float* sinks, int batch,
+                               int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+                               int max_pages, int num_pages, float sm_scale, int num_splits,
+                               void* out, float* lse, cudaStream_t stream);
+
+/*
  * Merge split partials into the final result:
  *   lse = ln sum_s e^(lse_s),  out = sum_s e^(lse_s - lse) o_s  (bf16).
  * Implied by the split rule of section "Kernels for GPT-OSS / Sink Attention";
