@@ -46,6 +46,10 @@ DECODE = workloads.WORKLOADS["paged_decode"]
 PREFILL = workloads.WORKLOADS["causal_prefill"]
 LONG = workloads.WORKLOADS["long_decode"]
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context for the measured-copy fraction)
+# kernel sources whose hash keys the recorded DRAM traffic (profiles/traffic.txt)
+DECODE_SOURCES = ("decode.cu", "ptx.cuh", "internal.h", "rope_math.cuh")
+PREFILL_SOURCES = ("prefill.cu", "ptx.cuh", "internal.h", "rope_math.cuh")
+ROPE_SOURCES = ("rope.cu", "rope_args.h", "internal.h", "ptx.cuh", "rope_math.cuh")
 
 
 def peaks():
@@ -275,7 +279,7 @@ def run_ours(args, rank, world, device):
                      "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
                      "peak_source": pk["source"] + " hbm_gbs (copy: read + write bytes)",
                      "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "traffic": recorded_traffic("sink_decode_kernel_long", ("decode.cu", "ptx.cuh", "internal.h")),
+                     "traffic": recorded_traffic("sink_decode_kernel_long", DECODE_SOURCES),
                      "traffic_source": "profiles/traffic.txt: ncu, 2 of 8 sequences, x4",
                      "kernel_ms": round(dec_ms, 5),
                      "kernel_timing": "events around each decode launch, same pass as ms_per_step"},
@@ -354,7 +358,7 @@ def bench_paged_decode(args, sa, torch, device, pk):
             "achieved": round(ach, 1), "peak": pk["hbm"], "frac": round(ach / pk["hbm"], 4),
             "frac_of_nominal_hbm": round(ach / NOMINAL_HBM_GBS, 4),
             "kernel_timing": "events around each decode launch (separate pass; step_us has none)",
-            "traffic": recorded_traffic("sink_decode_kernel", ("decode.cu", "ptx.cuh", "internal.h")),
+            "traffic": recorded_traffic("sink_decode_kernel", DECODE_SOURCES),
             "gpu_launches": (2 if s > 1 else 1) * (2 * reps + 5)}
 
 
@@ -405,7 +409,7 @@ def bench_mixed(args, sa, torch, device, pk):
             "frac": round(max(t_tc, t_hbm) / (ms * 1e-3), 4), "tensor_frac": round(t_tc / (ms * 1e-3), 4),
             "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
             "frac_rule": "max(FLOPs / peak bf16, bytes / peak HBM) / time",
-            "traffic": recorded_traffic("sink_prefill_kernel_mixed", ("prefill.cu", "ptx.cuh", "internal.h")),
+            "traffic": recorded_traffic("sink_prefill_kernel_mixed", PREFILL_SOURCES),
             "gpu_launches": len(times)}
 
 
@@ -597,7 +601,7 @@ def bench_around_attention(args, sa, torch, device, pk):
                              "frac": round(gbs / pk["hbm"], 4),
                              "traffic": recorded_traffic(kernel, srcs),
                              "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}}
-    return {"qkv_bias_rope": line(("rope.cu", "rope_args.h", "internal.h", "ptx.cuh"), "qkv_rope_kernel", rope_ms,
+    return {"qkv_bias_rope": line(ROPE_SOURCES, "qkv_rope_kernel", rope_ms,
                                   rope_bytes,
                                   "32768 tokens, 64/8 heads: bias + YaRN (GPT-OSS constants) on q, k; "
                                   "q, k, v written contiguous; L2 flushed (written, then read back) before each launch"),
@@ -723,7 +727,7 @@ def bench_prefill(args, sa, torch, device, pk):
             "bound": "tensor", "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2),
             "peak": pk["bf16"], "frac": round(tflops / pk["bf16"], 4),
             "peak_source": pk["source"] + " bf16_tflops (burst: kernel timed alone)",
-            "traffic": recorded_traffic("sink_prefill_kernel", ("prefill.cu", "ptx.cuh", "internal.h")),
+            "traffic": recorded_traffic("sink_prefill_kernel", PREFILL_SOURCES),
             "traffic_source": "profiles/traffic.txt: ncu, 1 of 4 sequences, x4",
             "l2": "flushed (256 MiB written, read back) before every launch",
             "gpu_launches": steps}
