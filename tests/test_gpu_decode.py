@@ -162,3 +162,26 @@ def test_decode_odd_groups(hq, hkv, splits):
                            d["sinks"], 0.125)
     assert_close(host(o), host(l), ro, rl, f"decode group {hq // hkv} splits={splits}")
     assert sa.sink_attn_device_status(True) == 0
+
+
+@pytest.mark.parametrize("batch,kv,splits", [(1, 131072, 32), (2, 65536, 16), (1, 20000, 8), (3, 9999, 3),
+                                             (1, 4096, 2)])
+def test_decode_small_grid_long_walks(batch, kv, splits):
+    """Small grids whose warps walk long page ranges (64 pages per warp for one 131072-token
+    sequence in 32 splits): every sequence against the oracle, partials included, and
+    against the merged result of a different split count."""
+    sa = require_gpu()
+    lens = [kv - 13 * b for b in range(batch)]
+    d = workloads.make_decode(23, lens, 64, 8, 64)
+    po, pl, args = _run(sa, d, 0.125, splits)
+    assert sa.sink_attn_device_status(True) == 0
+    ro, rl = oracle.decode(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["kv_lens"],
+                           d["sinks"], 0.125, num_splits=splits, workers=min(4, oracle_workers()))
+    assert max_err(host(po), ro) <= OUT_TOL
+    assert max_err(host(pl), rl) <= LSE_TOL
+    mo, ml = sa.sink_attn_merge(po, pl)
+    fo, fl = oracle.merge(ro, rl)
+    assert_close(host(mo), host(ml), fo, fl, f"long walks batch={batch} kv={kv} splits={splits}")
+    po2, pl2 = sa.sink_attn_decode(*args, 0.125, num_splits=splits + 1)
+    mo2, ml2 = sa.sink_attn_merge(po2, pl2)
+    assert_close(host(mo), host(ml), host(mo2), host(ml2), "long walks vs another split count")
