@@ -6,7 +6,8 @@
 // (sequence, head): lanes read the split lse values, a shuffle max, each lane
 // turns one split's lse into its weight, and every lane accumulates two of the
 // 64 output dims over the splits with coalesced float2 loads (256 contiguous
-// bytes per split per warp), the weights broadcast by shuffle.
+// bytes per split per warp), the weights broadcast by shuffle.  Up to 32 splits,
+// every split's output is requested at once (one L2 round trip per row).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -24,6 +25,27 @@ __device__ __forceinline__ float split_weight(float lse_s, float M) {
   if (lse_s == M) return 1.0f;
   if (lse_s == kNegInf || M == kPosInf) return 0.0f;
   return ex2((lse_s - M) * kLog2e);
+}
+
+// Up to N splits: every split's weight and partial output is requested at once, so the
+// row costs one round trip to L2 for the lse values and one for the outputs; the sum runs
+// over the splits in order, like the general loop.
+template <int N>
+__device__ __forceinline__ void merge_all_at_once(const float* o_p, const float* lse_p, int heads, int S, float M,
+                                                  int lane, float& z, float2& acc) {
+  const float w_mine = lane < S ? split_weight(lse_p[static_cast<size_t>(lane) * heads], M) : 0.0f;
+  z = w_mine;
+  float2 v[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    v[i] = i < S ? *reinterpret_cast<const float2*>(o_p + static_cast<size_t>(i) * heads * kHeadDim)
+                 : make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float w = __shfl_sync(0xffffffffu, w_mine, i);
+    acc.x = fmaf(w, v[i].x, acc.x);
+    acc.y = fmaf(w, v[i].y, acc.y);
+  }
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32) sink_merge_kernel(const MergeArgs a) {
@@ -54,17 +76,25 @@ __global__ void __launch_bounds__(kMergeWarps * 32) sink_merge_kernel(const Merg
     // -inf, or below a +inf one) holds o = 0 (decode writes empty splits as
     // zeros), so it adds nothing.
     const float* o_p = a.partial_o + (static_cast<size_t>(b) * S * a.heads + h) * kHeadDim + 2 * lane;
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      const int n = min(32, S - s0);
-      const float w_mine = lane < n ? split_weight(lse_p[static_cast<size_t>(s0 + lane) * a.heads], M) : 0.0f;
-      z += w_mine;
+    if (S <= 8) {
+      merge_all_at_once<8>(o_p, lse_p, a.heads, S, M, lane, z, acc);
+    } else if (S <= 16) {
+      merge_all_at_once<16>(o_p, lse_p, a.heads, S, M, lane, z, acc);
+    } else if (S <= 32) {
+      merge_all_at_once<32>(o_p, lse_p, a.heads, S, M, lane, z, acc);
+    } else {
+      for (int s0 = 0; s0 < S; s0 += 32) {
+        const int n = min(32, S - s0);
+        const float w_mine = lane < n ? split_weight(lse_p[static_cast<size_t>(s0 + lane) * a.heads], M) : 0.0f;
+        z += w_mine;
 #pragma unroll 8
-      for (int i = 0; i < n; ++i) {
-        const float w = __shfl_sync(0xffffffffu, w_mine, i);
-        const float2 v =
-            *reinterpret_cast<const float2*>(o_p + static_cast<size_t>(s0 + i) * a.heads * kHeadDim);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
+        for (int i = 0; i < n; ++i) {
+          const float w = __shfl_sync(0xffffffffu, w_mine, i);
+          const float2 v =
+              *reinterpret_cast<const float2*>(o_p + static_cast<size_t>(s0 + i) * a.heads * kHeadDim);
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+        }
       }
     }
 #pragma unroll
