@@ -118,7 +118,8 @@ def _check(status: int, where: str):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Raw device address (ctypes passes Python ints as void*), or None."""
+    return None if t is None else t.data_ptr()
 
 
 def _dev(t, name, dtype):
@@ -131,34 +132,47 @@ def _dev(t, name, dtype):
     return t
 
 
-def _out(t, name, dtype, shape, device):
-    """A caller-supplied output: on ``device``, of ``dtype``, contiguous and ``shape``."""
+def _out(t, name, dtype, shape, dev):
+    """A caller-supplied output: on device index ``dev``, of ``dtype``, contiguous and ``shape``."""
     _dev(t, name, dtype)
-    if t.device != device:
-        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+    if t.get_device() != dev:
+        raise ValueError(f"{name} is on cuda:{t.get_device()}, the inputs on cuda:{dev}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must be {tuple(shape)}, got {tuple(t.shape)}")
     return t
 
 
-def _same_device(device, **tensors):
-    for name, t in tensors.items():
-        if t is not None and t.device != device:
-            raise ValueError(f"{name} is on {t.device}, expected {device} (the device of the first input)")
+def _same_device(dev, *named):
+    """Every (name, tensor) pair with a tensor lies on device index ``dev``."""
+    for name, t in named:
+        if t is not None and t.get_device() != dev:
+            raise ValueError(f"{name} is on cuda:{t.get_device()}, expected cuda:{dev} "
+                             "(the device of the first input)")
 
 
-def _stream(stream, device=None):
-    """Raw handle of ``stream`` (default: the current stream of ``device``)."""
-    if stream is None:
-        s = torch.cuda.current_stream(device)
-    else:
-        s = stream
-        if device is not None and s.device != device:
-            raise ValueError(f"stream is on {s.device}, the tensors on {device}")
-    return ctypes.c_void_p(s.cuda_stream)
+def _call(fn, dev, stream, *args):
+    """fn(*args, stream) with device ``dev`` current for the call and ``stream`` (default: that
+    device's current stream) as the last argument; the previous current device is restored."""
+    if stream is not None and stream.device_index != dev:
+        raise ValueError(f"stream is on cuda:{stream.device_index}, the tensors on cuda:{dev}")
+    if torch.cuda.current_device() == dev:
+        s = torch.cuda.current_stream() if stream is None else stream
+        return fn(*args, s.cuda_stream)
+    with torch.cuda.device(dev):
+        s = torch.cuda.current_stream() if stream is None else stream
+        return fn(*args, s.cuda_stream)
 
 
 # ----------------------------------------------------------------------------- entry points
+def _checked(named):
+    """Validate (name, tensor, dtype) triples: CUDA, dtype, contiguous.  Returns the first
+    tensor's device and device index."""
+    for name, t, dt in named:
+        _dev(t, name, dt)
+    first = named[0][1]
+    return first.device, first.get_device()
+
+
 def sink_attn_prefill(q, k, v, sinks, cu_seqlens, max_seqlen: int, sm_scale: float,
                       causal: bool = True, out=None, lse=None, return_lse: bool = True,
                       stream=None):
@@ -167,23 +181,21 @@ def sink_attn_prefill(q, k, v, sinks, cu_seqlens, max_seqlen: int, sm_scale: flo
     q [T, Hq, 64] bf16, k/v [T, Hkv, 64] bf16, sinks [Hq] fp32, cu_seqlens [B+1] int32.
     Returns (out [T, Hq, 64] bf16, lse [T, Hq] fp32 or None).
     """
-    _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16)
-    _dev(sinks, "sinks", torch.float32), _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    dev, di = _checked((("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("sinks", sinks, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)))
     t, hq, d = q.shape
     hkv = k.shape[1]
     if k.shape != (t, hkv, d) or v.shape != k.shape:
         raise ValueError("k and v must be [T, Hkv, D] with q's T and D")
-    _same_device(q.device, k=k, v=v, sinks=sinks, cu_seqlens=cu_seqlens)
-    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, q.device)
+    _same_device(di, ("k", k), ("v", v), ("sinks", sinks), ("cu_seqlens", cu_seqlens))
+    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, di)
     if lse is None and return_lse:
-        lse = torch.empty((t, hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((t, hq), dtype=torch.float32, device=dev)
     elif lse is not None:
-        _out(lse, "lse", torch.float32, (t, hq), q.device)
-    with torch.cuda.device(q.device):
-        st = load_library().sink_attn_prefill(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), cu_seqlens.numel() - 1, t,
-            int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
-            _stream(stream, q.device))
+        _out(lse, "lse", torch.float32, (t, hq), di)
+    st = _call(load_library().sink_attn_prefill, di, stream,
+               _ptr(q), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens), cu_seqlens.numel() - 1, t,
+               int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse))
     _check(st, "sink_attn_prefill")
     return out, lse
 
@@ -196,27 +208,38 @@ def sink_attn_prefill_paged(q, paged_k, paged_v, page_table, cu_seqlens_q, kv_le
     q [Tq, Hq, 64] bf16, paged_k/v [P, Hkv, 16, 64] bf16, page_table [B, max_pages] int32,
     cu_seqlens_q [B+1] int32, kv_lens [B] int32, sinks [Hq] fp32.
     """
-    for name, tns, dt in (("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
-                          ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
-                          ("cu_seqlens_q", cu_seqlens_q, torch.int32), ("kv_lens", kv_lens, torch.int32),
-                          ("sinks", sinks, torch.float32)):
-        _dev(tns, name, dt)
+    dev, di = _checked((("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
+                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
+                        ("cu_seqlens_q", cu_seqlens_q, torch.int32), ("kv_lens", kv_lens, torch.int32),
+                        ("sinks", sinks, torch.float32)))
     t, hq, d = q.shape
     num_pages, hkv, page_size, _ = paged_k.shape
-    _same_device(q.device, paged_k=paged_k, paged_v=paged_v, page_table=page_table,
-                 cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, sinks=sinks)
-    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, q.device)
+    _same_device(di, ("paged_k", paged_k), ("paged_v", paged_v), ("page_table", page_table),
+                 ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens), ("sinks", sinks))
+    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, di)
     if lse is None and return_lse:
-        lse = torch.empty((t, hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((t, hq), dtype=torch.float32, device=dev)
     elif lse is not None:
-        _out(lse, "lse", torch.float32, (t, hq), q.device)
-    with torch.cuda.device(q.device):
-        st = load_library().sink_attn_prefill_paged(
-            _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(cu_seqlens_q), _ptr(kv_lens),
-            _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq, hkv, d, page_size,
-            page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse),
-            _stream(stream, q.device))
+        _out(lse, "lse", torch.float32, (t, hq), di)
+    st = _call(load_library().sink_attn_prefill_paged, di, stream,
+               _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(cu_seqlens_q), _ptr(kv_lens),
+               _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq, hkv, d, page_size,
+               page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out), _ptr(lse))
     _check(st, "sink_attn_prefill_paged")
+    return out, lse
+
+
+def _decode_outputs(out, lse, return_lse, b, s, hq, d, dev, di):
+    out_shape, out_dtype = ((b, hq, d), torch.bfloat16) if s == 1 else ((b, s, hq, d), torch.float32)
+    lse_shape = (b, hq) if s == 1 else (b, s, hq)
+    if out is None:
+        out = torch.empty(out_shape, dtype=out_dtype, device=dev)
+    else:
+        _out(out, "out", out_dtype, out_shape, di)
+    if lse is None and (return_lse or s > 1):
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    elif lse is not None:
+        _out(lse, "lse", torch.float32, lse_shape, di)
     return out, lse
 
 
@@ -228,30 +251,18 @@ def sink_attn_decode(q, paged_k, paged_v, page_table, kv_lens, sinks, sm_scale: 
     num_splits > 1: returns the partials (o [B, S, Hq, 64] fp32, lse [B, S, Hq] fp32)
     for sink_attn_merge.
     """
-    for name, tns, dt in (("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
-                          ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
-                          ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)):
-        _dev(tns, name, dt)
+    dev, di = _checked((("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
+                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
+                        ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)))
     b, hq, d = q.shape
     num_pages, hkv, page_size, _ = paged_k.shape
-    _same_device(q.device, paged_k=paged_k, paged_v=paged_v, page_table=page_table, kv_lens=kv_lens,
-                 sinks=sinks)
+    _same_device(di, ("paged_k", paged_k), ("paged_v", paged_v), ("page_table", page_table),
+                 ("kv_lens", kv_lens), ("sinks", sinks))
     s = int(num_splits)
-    out_shape, out_dtype = ((b, hq, d), torch.bfloat16) if s == 1 else ((b, s, hq, d), torch.float32)
-    lse_shape = (b, hq) if s == 1 else (b, s, hq)
-    if out is None:
-        out = torch.empty(out_shape, dtype=out_dtype, device=q.device)
-    else:
-        _out(out, "out", out_dtype, out_shape, q.device)
-    if lse is None and (return_lse or s > 1):
-        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
-    elif lse is not None:
-        _out(lse, "lse", torch.float32, lse_shape, q.device)
-    with torch.cuda.device(q.device):
-        st = load_library().sink_attn_decode(
-            _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
-            hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), s, _ptr(out), _ptr(lse),
-            _stream(stream, q.device))
+    out, lse = _decode_outputs(out, lse, return_lse, b, s, hq, d, dev, di)
+    st = _call(load_library().sink_attn_decode, di, stream,
+               _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
+               hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), s, _ptr(out), _ptr(lse))
     _check(st, "sink_attn_decode")
     return out, lse
 
@@ -267,24 +278,18 @@ def sink_attn_decode_noalloc(q, paged_k, paged_v, page_table, kv_lens, sinks, sm
     [B, Hq] fp32 to keep this wrapper allocation-free as well.  Calls that
     overlap on the GPU race on the shared array.
     """
-    for name, tns, dt in (("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
-                          ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
-                          ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)):
-        _dev(tns, name, dt)
+    dev, di = _checked((("q", q, torch.bfloat16), ("paged_k", paged_k, torch.bfloat16),
+                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32),
+                        ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)))
     b, hq, d = q.shape
     num_pages, hkv, page_size, _ = paged_k.shape
-    _same_device(q.device, paged_k=paged_k, paged_v=paged_v, page_table=page_table, kv_lens=kv_lens,
-                 sinks=sinks)
-    out = torch.empty_like(q) if out is None else _out(out, "out", torch.bfloat16, q.shape, q.device)
-    if lse is None and return_lse:
-        lse = torch.empty((b, hq), dtype=torch.float32, device=q.device)
-    elif lse is not None:
-        _out(lse, "lse", torch.float32, (b, hq), q.device)
-    with torch.cuda.device(q.device):
-        st = load_library().sink_attn_decode_noalloc(
-            _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
-            hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(num_splits), _ptr(out),
-            _ptr(lse), _stream(stream, q.device))
+    _same_device(di, ("paged_k", paged_k), ("paged_v", paged_v), ("page_table", page_table),
+                 ("kv_lens", kv_lens), ("sinks", sinks))
+    out, lse = _decode_outputs(out, lse, return_lse, b, 1, hq, d, dev, di)
+    st = _call(load_library().sink_attn_decode_noalloc, di, stream,
+               _ptr(q), _ptr(paged_k), _ptr(paged_v), _ptr(page_table), _ptr(kv_lens), _ptr(sinks), b, hq,
+               hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(num_splits),
+               _ptr(out), _ptr(lse))
     _check(st, "sink_attn_decode_noalloc")
     return out, lse
 
@@ -292,21 +297,19 @@ def sink_attn_decode_noalloc(q, paged_k, paged_v, page_table, kv_lens, sinks, sm
 def sink_attn_merge(partial_o, partial_lse, out=None, lse=None, return_lse: bool = True,
                     stream=None):
     """Merge split partials o [B, S, H, 64] fp32 / lse [B, S, H] fp32 -> (out bf16, lse fp32)."""
-    _dev(partial_o, "partial_o", torch.float32), _dev(partial_lse, "partial_lse", torch.float32)
+    dev, di = _checked((("partial_o", partial_o, torch.float32), ("partial_lse", partial_lse, torch.float32)))
     b, s, h, d = partial_o.shape
-    dv = partial_o.device
     if tuple(partial_lse.shape) != (b, s, h):
         raise ValueError(f"partial_lse must be {(b, s, h)}, got {tuple(partial_lse.shape)}")
-    _same_device(dv, partial_lse=partial_lse)
-    out = (torch.empty((b, h, d), dtype=torch.bfloat16, device=dv) if out is None
-           else _out(out, "out", torch.bfloat16, (b, h, d), dv))
+    _same_device(di, ("partial_lse", partial_lse))
+    out = (torch.empty((b, h, d), dtype=torch.bfloat16, device=dev) if out is None
+           else _out(out, "out", torch.bfloat16, (b, h, d), di))
     if lse is None and return_lse:
-        lse = torch.empty((b, h), dtype=torch.float32, device=dv)
+        lse = torch.empty((b, h), dtype=torch.float32, device=dev)
     elif lse is not None:
-        _out(lse, "lse", torch.float32, (b, h), dv)
-    with torch.cuda.device(dv):
-        st = load_library().sink_attn_merge(_ptr(partial_o), _ptr(partial_lse), b, s, h, d, _ptr(out),
-                                            _ptr(lse), _stream(stream, dv))
+        _out(lse, "lse", torch.float32, (b, h), di)
+    st = _call(load_library().sink_attn_merge, di, stream,
+               _ptr(partial_o), _ptr(partial_lse), b, s, h, d, _ptr(out), _ptr(lse))
     _check(st, "sink_attn_merge")
     return out, lse
 
@@ -337,10 +340,9 @@ def sink_attn_abi_version() -> int:
 
 def sink_attn_selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) -> None:
     """Launch the bounded-wait diagnostic (records SA_ERR_TIMEOUT in the status word)."""
-    dv = torch.device("cuda", torch.cuda.current_device()) if stream is None else stream.device
-    with torch.cuda.device(dv):
-        st = load_library().sink_attn_selftest_wait_timeout(int(timeout_ns), _stream(stream, dv))
-    _check(st, "sink_attn_selftest_wait_timeout")
+    di = torch.cuda.current_device() if stream is None else stream.device_index
+    _check(_call(load_library().sink_attn_selftest_wait_timeout, di, stream, int(timeout_ns)),
+           "sink_attn_selftest_wait_timeout")
 
 
 # ----------------------------------------------------------------------------- around attention
@@ -349,21 +351,19 @@ def moe_router_topk_softmax(logits, top_k: int, topk_idx=None, topk_weight=None,
     """Top-K-then-softmax router over bf16 logits [T, E] (page "GPT-OSS on day 0",
     section "Kernels for GPT-OSS / MoE").  Returns (idx int32 [T, k], weight bf16
     [T, k]) and, with return_counts or a given expert_counts, the int32 [E] counts."""
-    _dev(logits, "logits", torch.bfloat16)
+    dev, di = _checked((("logits", logits, torch.bfloat16),))
     t, e = logits.shape
     k = int(top_k)
-    dv = logits.device
-    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=dv) if topk_idx is None
-                else _out(topk_idx, "topk_idx", torch.int32, (t, k), dv))
-    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=dv) if topk_weight is None
-                   else _out(topk_weight, "topk_weight", torch.bfloat16, (t, k), dv))
+    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=dev) if topk_idx is None
+                else _out(topk_idx, "topk_idx", torch.int32, (t, k), di))
+    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=dev) if topk_weight is None
+                   else _out(topk_weight, "topk_weight", torch.bfloat16, (t, k), di))
     if expert_counts is None and return_counts:
-        expert_counts = torch.empty((e,), dtype=torch.int32, device=dv)
+        expert_counts = torch.empty((e,), dtype=torch.int32, device=dev)
     elif expert_counts is not None:
-        _out(expert_counts, "expert_counts", torch.int32, (e,), dv)
-    with torch.cuda.device(dv):
-        st = load_library().moe_router_topk_softmax(_ptr(logits), t, e, k, _ptr(topk_idx), _ptr(topk_weight),
-                                                    _ptr(expert_counts), _stream(stream, dv))
+        _out(expert_counts, "expert_counts", torch.int32, (e,), di)
+    st = _call(load_library().moe_router_topk_softmax, di, stream,
+               _ptr(logits), t, e, k, _ptr(topk_idx), _ptr(topk_weight), _ptr(expert_counts))
     _check(st, "moe_router_topk_softmax")
     if expert_counts is not None:
         return topk_idx, topk_weight, expert_counts
@@ -376,30 +376,30 @@ def _rope_params(rope):
             float(r["beta_slow"]))
 
 
+def _opt(named):
+    """Validate the optional (name, tensor, dtype) triples that are not None."""
+    for name, t, dt in named:
+        if t is not None:
+            _dev(t, name, dt)
+
+
 def qkv_bias_rope(qkv, bias, cu_seqlens_q, num_qo_heads: int, num_kv_heads: int, kv_lens=None,
                   rope=None, q_out=None, k_out=None, v_out=None, stream=None):
     """QKV bias + YaRN rotation of q and k.  qkv bf16 [T, (Hq + 2 Hkv) * 64] -> (q [T, Hq, 64],
     k [T, Hkv, 64], v [T, Hkv, 64]) bf16.  rope: dict like GPT_OSS_YARN (default)."""
-    _dev(qkv, "qkv", torch.bfloat16)
-    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
-    if bias is not None:
-        _dev(bias, "bias", torch.bfloat16)
-    if kv_lens is not None:
-        _dev(kv_lens, "kv_lens", torch.int32)
+    dev, di = _checked((("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32)))
+    _opt((("bias", bias, torch.bfloat16), ("kv_lens", kv_lens, torch.int32)))
     t = qkv.shape[0]
     hq, hkv, d = int(num_qo_heads), int(num_kv_heads), 64
-    dv = qkv.device
-    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens)
-    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if q_out is None else q_out
-    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if k_out is None else k_out
-    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if v_out is None else v_out
+    _same_device(di, ("bias", bias), ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens))
+    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=dev) if q_out is None else q_out
+    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dev) if k_out is None else k_out
+    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dev) if v_out is None else v_out
     for name, x, h in (("q_out", q_out, hq), ("k_out", k_out, hkv), ("v_out", v_out, hkv)):
-        _out(x, name, torch.bfloat16, (t, h, d), dv)
-    with torch.cuda.device(dv):
-        st = load_library().qkv_bias_rope(_ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens),
-                                          cu_seqlens_q.numel() - 1, t, hq, hkv, qkv.shape[1] // (hq + 2 * hkv),
-                                          *_rope_params(rope), _ptr(q_out), _ptr(k_out), _ptr(v_out),
-                                          _stream(stream, dv))
+        _out(x, name, torch.bfloat16, (t, h, d), di)
+    st = _call(load_library().qkv_bias_rope, di, stream,
+               _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
+               qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(q_out), _ptr(k_out), _ptr(v_out))
     _check(st, "qkv_bias_rope")
     return q_out, k_out, v_out
 
@@ -408,25 +408,21 @@ def qkv_bias_rope_append_paged(qkv, bias, cu_seqlens_q, kv_lens, paged_k, paged_
                                num_qo_heads: int, rope=None, q_out=None, stream=None):
     """QKV bias + YaRN rotation; q returned [T, Hq, 64], k and v written in place into the
     paged cache [num_pages, Hkv, 16, 64] at each new token's position."""
-    for name, x, dt in (("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+    dev, di = _checked((("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
                         ("kv_lens", kv_lens, torch.int32), ("paged_k", paged_k, torch.bfloat16),
-                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32)):
-        _dev(x, name, dt)
-    if bias is not None:
-        _dev(bias, "bias", torch.bfloat16)
+                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32)))
+    _opt((("bias", bias, torch.bfloat16),))
     t = qkv.shape[0]
     num_pages, hkv, page_size, d = paged_k.shape
     hq = int(num_qo_heads)
-    dv = qkv.device
-    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, paged_k=paged_k,
-                 paged_v=paged_v, page_table=page_table)
-    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if q_out is None else q_out
-    _out(q_out, "q_out", torch.bfloat16, (t, hq, d), dv)
-    with torch.cuda.device(dv):
-        st = load_library().qkv_bias_rope_append_paged(
-            _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
-            qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(q_out), _ptr(paged_k), _ptr(paged_v),
-            _ptr(page_table), page_size, page_table.shape[1], num_pages, _stream(stream, dv))
+    _same_device(di, ("bias", bias), ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens),
+                 ("paged_k", paged_k), ("paged_v", paged_v), ("page_table", page_table))
+    q_out = torch.empty((t, hq, d), dtype=torch.bfloat16, device=dev) if q_out is None else q_out
+    _out(q_out, "q_out", torch.bfloat16, (t, hq, d), di)
+    st = _call(load_library().qkv_bias_rope_append_paged, di, stream,
+               _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
+               qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(q_out), _ptr(paged_k), _ptr(paged_v),
+               _ptr(page_table), page_size, page_table.shape[1], num_pages)
     _check(st, "qkv_bias_rope_append_paged")
     return q_out
 
@@ -435,20 +431,16 @@ def linear_bias(x, w, bias=None, out=None, stream=None):
     """out [M, N] = x [M, K] @ w[N, K]^T + bias[N] on the tcgen05 tensor cores, bf16 in and out,
     the fp32 accumulator seeded with the bias (page "GPT-OSS on day 0", section "Kernels for
     GPT-OSS / MoE")."""
-    _dev(x, "x", torch.bfloat16)
-    _dev(w, "w", torch.bfloat16)
-    if bias is not None:
-        _dev(bias, "bias", torch.bfloat16)
+    dev, di = _checked((("x", x, torch.bfloat16), ("w", w, torch.bfloat16)))
+    _opt((("bias", bias, torch.bfloat16),))
     m, k = x.shape
     n = w.shape[0]
     if w.shape[1] != k:
         raise ValueError(f"w is {tuple(w.shape)}, expected [N, {k}]")
-    _same_device(x.device, w=w, bias=bias)
-    out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device) if out is None else out
-    _out(out, "out", torch.bfloat16, (m, n), x.device)
-    with torch.cuda.device(x.device):
-        st = load_library().linear_bias(_ptr(x), _ptr(w), _ptr(bias), m, n, k, _ptr(out),
-                                        _stream(stream, x.device))
+    _same_device(di, ("w", w), ("bias", bias))
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=dev) if out is None else out
+    _out(out, "out", torch.bfloat16, (m, n), di)
+    st = _call(load_library().linear_bias, di, stream, _ptr(x), _ptr(w), _ptr(bias), m, n, k, _ptr(out))
     _check(st, "linear_bias")
     return out
 
@@ -458,28 +450,24 @@ def moe_router(x, w_router, bias, top_k: int, topk_idx=None, topk_weight=None, e
     """Router projection + bias + bf16 logits + Top-K softmax in one tcgen05 kernel:
     x [T, hidden] bf16, w_router [E, hidden] bf16, bias [E] bf16 or None.  Returns
     (idx int32 [T, k], weight bf16 [T, k]) and the int32 [E] counts when asked."""
-    _dev(x, "x", torch.bfloat16)
-    _dev(w_router, "w_router", torch.bfloat16)
-    if bias is not None:
-        _dev(bias, "bias", torch.bfloat16)
+    dev, di = _checked((("x", x, torch.bfloat16), ("w_router", w_router, torch.bfloat16)))
+    _opt((("bias", bias, torch.bfloat16),))
     t, hidden = x.shape
     e = w_router.shape[0]
     if w_router.shape[1] != hidden:
         raise ValueError(f"w_router is {tuple(w_router.shape)}, expected [E, {hidden}]")
     k = int(top_k)
-    dv = x.device
-    _same_device(dv, w_router=w_router, bias=bias)
-    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=dv) if topk_idx is None
-                else _out(topk_idx, "topk_idx", torch.int32, (t, k), dv))
-    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=dv) if topk_weight is None
-                   else _out(topk_weight, "topk_weight", torch.bfloat16, (t, k), dv))
+    _same_device(di, ("w_router", w_router), ("bias", bias))
+    topk_idx = (torch.empty((t, k), dtype=torch.int32, device=dev) if topk_idx is None
+                else _out(topk_idx, "topk_idx", torch.int32, (t, k), di))
+    topk_weight = (torch.empty((t, k), dtype=torch.bfloat16, device=dev) if topk_weight is None
+                   else _out(topk_weight, "topk_weight", torch.bfloat16, (t, k), di))
     if expert_counts is None and return_counts:
-        expert_counts = torch.empty((e,), dtype=torch.int32, device=dv)
+        expert_counts = torch.empty((e,), dtype=torch.int32, device=dev)
     elif expert_counts is not None:
-        _out(expert_counts, "expert_counts", torch.int32, (e,), dv)
-    with torch.cuda.device(dv):
-        st = load_library().moe_router(_ptr(x), _ptr(w_router), _ptr(bias), t, hidden, e, k, _ptr(topk_idx),
-                                       _ptr(topk_weight), _ptr(expert_counts), _stream(stream, dv))
+        _out(expert_counts, "expert_counts", torch.int32, (e,), di)
+    st = _call(load_library().moe_router, di, stream, _ptr(x), _ptr(w_router), _ptr(bias), t, hidden, e, k,
+               _ptr(topk_idx), _ptr(topk_weight), _ptr(expert_counts))
     _check(st, "moe_router")
     if expert_counts is not None:
         return topk_idx, topk_weight, expert_counts
@@ -492,28 +480,21 @@ def qkv_bias_rope_kv(qkv, bias, cu_seqlens_q, num_qo_heads: int, num_kv_heads: i
     """K/V half of qkv_bias_rope for the *_qkv attention calls: k (biased, rotated) and v
     (biased) written contiguous [T, Hkv, 64] bf16, plus the per-token (cos, sin) table
     [T, 32, 2] fp32 those calls apply to q.  Returns (k, v, rope_table)."""
-    _dev(qkv, "qkv", torch.bfloat16)
-    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
-    if bias is not None:
-        _dev(bias, "bias", torch.bfloat16)
-    if kv_lens is not None:
-        _dev(kv_lens, "kv_lens", torch.int32)
+    dev, di = _checked((("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32)))
+    _opt((("bias", bias, torch.bfloat16), ("kv_lens", kv_lens, torch.int32)))
     t = qkv.shape[0]
     hq, hkv, d = int(num_qo_heads), int(num_kv_heads), 64
-    dv = qkv.device
-    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens)
-    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if k_out is None else k_out
-    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dv) if v_out is None else v_out
-    rope_table = (torch.empty((t, d // 2, 2), dtype=torch.float32, device=dv) if rope_table is None
+    _same_device(di, ("bias", bias), ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens))
+    k_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dev) if k_out is None else k_out
+    v_out = torch.empty((t, hkv, d), dtype=torch.bfloat16, device=dev) if v_out is None else v_out
+    rope_table = (torch.empty((t, d // 2, 2), dtype=torch.float32, device=dev) if rope_table is None
                   else rope_table)
-    _out(k_out, "k_out", torch.bfloat16, (t, hkv, d), dv)
-    _out(v_out, "v_out", torch.bfloat16, (t, hkv, d), dv)
-    _out(rope_table, "rope_table", torch.float32, (t, d // 2, 2), dv)
-    with torch.cuda.device(dv):
-        st = load_library().qkv_bias_rope_kv(_ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens),
-                                             cu_seqlens_q.numel() - 1, t, hq, hkv, qkv.shape[1] // (hq + 2 * hkv),
-                                             *_rope_params(rope), _ptr(k_out), _ptr(v_out), _ptr(rope_table),
-                                             _stream(stream, dv))
+    _out(k_out, "k_out", torch.bfloat16, (t, hkv, d), di)
+    _out(v_out, "v_out", torch.bfloat16, (t, hkv, d), di)
+    _out(rope_table, "rope_table", torch.float32, (t, d // 2, 2), di)
+    st = _call(load_library().qkv_bias_rope_kv, di, stream,
+               _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
+               qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(k_out), _ptr(v_out), _ptr(rope_table))
     _check(st, "qkv_bias_rope_kv")
     return k_out, v_out, rope_table
 
@@ -523,26 +504,22 @@ def qkv_bias_rope_append_paged_kv(qkv, bias, cu_seqlens_q, kv_lens, paged_k, pag
     """K/V half of qkv_bias_rope_append_paged: k and v written in place into the paged
     cache at each new token's position, and the (cos, sin) table [T, 32, 2] fp32 of the
     new tokens returned for the *_qkv attention calls."""
-    for name, x, dt in (("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+    dev, di = _checked((("qkv", qkv, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
                         ("kv_lens", kv_lens, torch.int32), ("paged_k", paged_k, torch.bfloat16),
-                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32)):
-        _dev(x, name, dt)
-    if bias is not None:
-        _dev(bias, "bias", torch.bfloat16)
+                        ("paged_v", paged_v, torch.bfloat16), ("page_table", page_table, torch.int32)))
+    _opt((("bias", bias, torch.bfloat16),))
     t = qkv.shape[0]
     num_pages, hkv, page_size, d = paged_k.shape
     hq = int(num_qo_heads)
-    dv = qkv.device
-    _same_device(dv, bias=bias, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, paged_k=paged_k,
-                 paged_v=paged_v, page_table=page_table)
-    rope_table = (torch.empty((t, d // 2, 2), dtype=torch.float32, device=dv) if rope_table is None
+    _same_device(di, ("bias", bias), ("cu_seqlens_q", cu_seqlens_q), ("kv_lens", kv_lens),
+                 ("paged_k", paged_k), ("paged_v", paged_v), ("page_table", page_table))
+    rope_table = (torch.empty((t, d // 2, 2), dtype=torch.float32, device=dev) if rope_table is None
                   else rope_table)
-    _out(rope_table, "rope_table", torch.float32, (t, d // 2, 2), dv)
-    with torch.cuda.device(dv):
-        st = load_library().qkv_bias_rope_append_paged_kv(
-            _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
-            qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(paged_k), _ptr(paged_v),
-            _ptr(page_table), page_size, page_table.shape[1], num_pages, _ptr(rope_table), _stream(stream, dv))
+    _out(rope_table, "rope_table", torch.float32, (t, d // 2, 2), di)
+    st = _call(load_library().qkv_bias_rope_append_paged_kv, di, stream,
+               _ptr(qkv), _ptr(bias), _ptr(cu_seqlens_q), _ptr(kv_lens), cu_seqlens_q.numel() - 1, t, hq, hkv,
+               qkv.shape[1] // (hq + 2 * hkv), *_rope_params(rope), _ptr(paged_k), _ptr(paged_v),
+               _ptr(page_table), page_size, page_table.shape[1], num_pages, _ptr(rope_table))
     _check(st, "qkv_bias_rope_append_paged_kv")
     return rope_table
 
@@ -553,12 +530,10 @@ def sink_attn_prefill_qkv(qkv, qkv_bias, rope_table, k, v, sinks, cu_seqlens, ma
     """sink_attn_prefill with q taken from the projection output qkv [T, (Hq + 2 Hkv) * 64]:
     the query bias and the rotation by rope_table (from qkv_bias_rope_kv) are applied on
     chip; k, v as written by qkv_bias_rope_kv."""
-    for name, tns, dt in (("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
-                          ("k", k, torch.bfloat16), ("v", v, torch.bfloat16), ("sinks", sinks, torch.float32),
-                          ("cu_seqlens", cu_seqlens, torch.int32)):
-        _dev(tns, name, dt)
-    if qkv_bias is not None:
-        _dev(qkv_bias, "qkv_bias", torch.bfloat16)
+    dev, di = _checked((("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
+                        ("k", k, torch.bfloat16), ("v", v, torch.bfloat16), ("sinks", sinks, torch.float32),
+                        ("cu_seqlens", cu_seqlens, torch.int32)))
+    _opt((("qkv_bias", qkv_bias, torch.bfloat16),))
     t = qkv.shape[0]
     hq = int(num_qo_heads)
     _, hkv, d = k.shape
@@ -566,19 +541,18 @@ def sink_attn_prefill_qkv(qkv, qkv_bias, rope_table, k, v, sinks, cu_seqlens, ma
         raise ValueError("qkv must be [T, (Hq + 2 Hkv) * D] and k, v [T, Hkv, D]")
     if tuple(rope_table.shape) != (t, d // 2, 2):
         raise ValueError(f"rope_table must be {(t, d // 2, 2)}")
-    dv = qkv.device
-    _same_device(dv, qkv_bias=qkv_bias, rope_table=rope_table, k=k, v=v, sinks=sinks, cu_seqlens=cu_seqlens)
-    out = (torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if out is None
-           else _out(out, "out", torch.bfloat16, (t, hq, d), dv))
+    _same_device(di, ("qkv_bias", qkv_bias), ("rope_table", rope_table), ("k", k), ("v", v), ("sinks", sinks),
+                 ("cu_seqlens", cu_seqlens))
+    out = (torch.empty((t, hq, d), dtype=torch.bfloat16, device=dev) if out is None
+           else _out(out, "out", torch.bfloat16, (t, hq, d), di))
     if lse is None and return_lse:
-        lse = torch.empty((t, hq), dtype=torch.float32, device=dv)
+        lse = torch.empty((t, hq), dtype=torch.float32, device=dev)
     elif lse is not None:
-        _out(lse, "lse", torch.float32, (t, hq), dv)
-    with torch.cuda.device(dv):
-        st = load_library().sink_attn_prefill_qkv(
-            _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens),
-            cu_seqlens.numel() - 1, t, int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)),
-            _ptr(out), _ptr(lse), _stream(stream, dv))
+        _out(lse, "lse", torch.float32, (t, hq), di)
+    st = _call(load_library().sink_attn_prefill_qkv, di, stream,
+               _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(k), _ptr(v), _ptr(sinks), _ptr(cu_seqlens),
+               cu_seqlens.numel() - 1, t, int(max_seqlen), hq, hkv, d, float(sm_scale), int(bool(causal)),
+               _ptr(out), _ptr(lse))
     _check(st, "sink_attn_prefill_qkv")
     return out, lse
 
@@ -590,33 +564,30 @@ def sink_attn_prefill_paged_qkv(qkv, qkv_bias, rope_table, paged_k, paged_v, pag
     """sink_attn_prefill_paged with q taken from the projection output (see
     sink_attn_prefill_qkv); the paged cache and rope_table as written by
     qkv_bias_rope_append_paged_kv."""
-    for name, tns, dt in (("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
-                          ("paged_k", paged_k, torch.bfloat16), ("paged_v", paged_v, torch.bfloat16),
-                          ("page_table", page_table, torch.int32), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
-                          ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)):
-        _dev(tns, name, dt)
-    if qkv_bias is not None:
-        _dev(qkv_bias, "qkv_bias", torch.bfloat16)
+    dev, di = _checked((("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
+                        ("paged_k", paged_k, torch.bfloat16), ("paged_v", paged_v, torch.bfloat16),
+                        ("page_table", page_table, torch.int32), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                        ("kv_lens", kv_lens, torch.int32), ("sinks", sinks, torch.float32)))
+    _opt((("qkv_bias", qkv_bias, torch.bfloat16),))
     t = qkv.shape[0]
     hq = int(num_qo_heads)
     num_pages, hkv, page_size, d = paged_k.shape
     if qkv.shape[1] != (hq + 2 * hkv) * d or tuple(rope_table.shape) != (t, d // 2, 2):
         raise ValueError("qkv must be [T, (Hq + 2 Hkv) * D] and rope_table [T, D / 2, 2]")
-    dv = qkv.device
-    _same_device(dv, qkv_bias=qkv_bias, rope_table=rope_table, paged_k=paged_k, paged_v=paged_v,
-                 page_table=page_table, cu_seqlens_q=cu_seqlens_q, kv_lens=kv_lens, sinks=sinks)
-    out = (torch.empty((t, hq, d), dtype=torch.bfloat16, device=dv) if out is None
-           else _out(out, "out", torch.bfloat16, (t, hq, d), dv))
+    _same_device(di, ("qkv_bias", qkv_bias), ("rope_table", rope_table), ("paged_k", paged_k),
+                 ("paged_v", paged_v), ("page_table", page_table), ("cu_seqlens_q", cu_seqlens_q),
+                 ("kv_lens", kv_lens), ("sinks", sinks))
+    out = (torch.empty((t, hq, d), dtype=torch.bfloat16, device=dev) if out is None
+           else _out(out, "out", torch.bfloat16, (t, hq, d), di))
     if lse is None and return_lse:
-        lse = torch.empty((t, hq), dtype=torch.float32, device=dv)
+        lse = torch.empty((t, hq), dtype=torch.float32, device=dev)
     elif lse is not None:
-        _out(lse, "lse", torch.float32, (t, hq), dv)
-    with torch.cuda.device(dv):
-        st = load_library().sink_attn_prefill_paged_qkv(
-            _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(paged_k), _ptr(paged_v), _ptr(page_table),
-            _ptr(cu_seqlens_q), _ptr(kv_lens), _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq,
-            hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out),
-            _ptr(lse), _stream(stream, dv))
+        _out(lse, "lse", torch.float32, (t, hq), di)
+    st = _call(load_library().sink_attn_prefill_paged_qkv, di, stream,
+               _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(paged_k), _ptr(paged_v), _ptr(page_table),
+               _ptr(cu_seqlens_q), _ptr(kv_lens), _ptr(sinks), cu_seqlens_q.numel() - 1, t, int(max_q_len), hq,
+               hkv, d, page_size, page_table.shape[1], num_pages, float(sm_scale), int(bool(causal)), _ptr(out),
+               _ptr(lse))
     _check(st, "sink_attn_prefill_paged_qkv")
     return out, lse
 
@@ -627,34 +598,23 @@ def sink_attn_decode_qkv(qkv, qkv_bias, rope_table, paged_k, paged_v, page_table
     """sink_attn_decode with q taken from the projection output qkv [B, (Hq + 2 Hkv) * 64] (one
     new token per sequence): bias and rotation by row b of rope_table [B, 32, 2] applied in
     the kernel.  num_splits > 1 returns the fp32 partials, as sink_attn_decode does."""
-    for name, tns, dt in (("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
-                          ("paged_k", paged_k, torch.bfloat16), ("paged_v", paged_v, torch.bfloat16),
-                          ("page_table", page_table, torch.int32), ("kv_lens", kv_lens, torch.int32),
-                          ("sinks", sinks, torch.float32)):
-        _dev(tns, name, dt)
-    if qkv_bias is not None:
-        _dev(qkv_bias, "qkv_bias", torch.bfloat16)
+    dev, di = _checked((("qkv", qkv, torch.bfloat16), ("rope_table", rope_table, torch.float32),
+                        ("paged_k", paged_k, torch.bfloat16), ("paged_v", paged_v, torch.bfloat16),
+                        ("page_table", page_table, torch.int32), ("kv_lens", kv_lens, torch.int32),
+                        ("sinks", sinks, torch.float32)))
+    _opt((("qkv_bias", qkv_bias, torch.bfloat16),))
     b = qkv.shape[0]
     hq = int(num_qo_heads)
     num_pages, hkv, page_size, d = paged_k.shape
     if qkv.shape[1] != (hq + 2 * hkv) * d or tuple(rope_table.shape) != (b, d // 2, 2):
         raise ValueError("qkv must be [B, (Hq + 2 Hkv) * D] and rope_table [B, D / 2, 2]")
-    dv = qkv.device
-    _same_device(dv, qkv_bias=qkv_bias, rope_table=rope_table, paged_k=paged_k, paged_v=paged_v,
-                 page_table=page_table, kv_lens=kv_lens, sinks=sinks)
+    _same_device(di, ("qkv_bias", qkv_bias), ("rope_table", rope_table), ("paged_k", paged_k),
+                 ("paged_v", paged_v), ("page_table", page_table), ("kv_lens", kv_lens), ("sinks", sinks))
     s = int(num_splits)
-    out_shape, out_dtype = ((b, hq, d), torch.bfloat16) if s == 1 else ((b, s, hq, d), torch.float32)
-    lse_shape = (b, hq) if s == 1 else (b, s, hq)
-    out = (torch.empty(out_shape, dtype=out_dtype, device=dv) if out is None
-           else _out(out, "out", out_dtype, out_shape, dv))
-    if lse is None and (return_lse or s > 1):
-        lse = torch.empty(lse_shape, dtype=torch.float32, device=dv)
-    elif lse is not None:
-        _out(lse, "lse", torch.float32, lse_shape, dv)
-    with torch.cuda.device(dv):
-        st = load_library().sink_attn_decode_qkv(
-            _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(paged_k), _ptr(paged_v), _ptr(page_table),
-            _ptr(kv_lens), _ptr(sinks), b, hq, hkv, d, page_size, page_table.shape[1], num_pages,
-            float(sm_scale), s, _ptr(out), _ptr(lse), _stream(stream, dv))
+    out, lse = _decode_outputs(out, lse, return_lse, b, s, hq, d, dev, di)
+    st = _call(load_library().sink_attn_decode_qkv, di, stream,
+               _ptr(qkv), _ptr(qkv_bias), _ptr(rope_table), _ptr(paged_k), _ptr(paged_v), _ptr(page_table),
+               _ptr(kv_lens), _ptr(sinks), b, hq, hkv, d, page_size, page_table.shape[1], num_pages,
+               float(sm_scale), s, _ptr(out), _ptr(lse))
     _check(st, "sink_attn_decode_qkv")
     return out, lse
