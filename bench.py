@@ -266,47 +266,44 @@ def run_ours(args, rank, world, device):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks, random page permutation)",
-        "config": {"workload": "long_decode: 8 seqs x 131072 cached tokens, 64/8 heads, head_dim 64, "
-                               "page 16, permuted pages, 32 splits + merge",
-                   "batch": b, "kv_len": kvl, "num_qo_heads": hq, "num_kv_heads": hkv, "head_dim": d,
-                   "page_size": cfg["page_size"], "num_splits": s,
-                   "step": "sink_attn_decode (32 splits, sink in split 0) + sink_attn_merge",
-                   "l2": "inputs larger than L2 (2 GiB KV per step, 129 MB L2)",
+        "data": "synthetic: seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks, permuted pages",
+        "config": {"workload": "long_decode: 8 x 131072 cached tokens, 64/8 heads, d 64, page 16, "
+                               "32 splits + merge",
+                   "batch": b, "kv_len": kvl, "num_splits": s,
+                   "l2": "inputs > L2 (2 GiB KV per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "algorithmic_bytes_per_step": alg_bytes},
-        "roofline": {"bound": "hbm", "kernel": "sink_decode_kernel", "achieved": round(achieved, 1),
-                     "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
-                     "peak_source": pk["source"] + " hbm_gbs (copy: read + write bytes)",
-                     "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "traffic": recorded_traffic("sink_decode_kernel_long", DECODE_SOURCES),
-                     "traffic_source": "profiles/traffic.txt: ncu, 2 of 8 sequences, x4",
-                     "kernel_ms": round(dec_ms, 5),
-                     "kernel_timing": "events around each decode launch, same pass as ms_per_step"},
         "e2e": {"value": round(job_throughput(alg_bytes, world, e2e_ms), 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "pinned host inputs -> device, decode + merge, out + lse -> host"},
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "device_status": status,
     }
+    roofline = {"bound": "hbm", "kernel": "sink_decode_kernel", "achieved": round(achieved, 1),
+                "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
+                "peak_source": pk["source"] + " copy",
+                "frac_of_nominal_hbm": round(achieved / NOMINAL_HBM_GBS, 4),
+                "traffic": recorded_traffic("sink_decode_kernel_long", DECODE_SOURCES),
+                "kernel_ms": round(dec_ms, 5)}
     if not args.no_prefill:
-        line["prefill"] = bench_prefill(args, sa, torch, device, pk)
-        line["mixed"] = bench_mixed(args, sa, torch, device, pk)
-        line["paged_decode"] = bench_paged_decode(args, sa, torch, device, pk)
-        line["small_batch_decode"] = bench_graph_decode(args, sa, torch, device, pk)
-        line["tiny_prefill"] = bench_tiny_prefill(args, sa, torch, device, pk)
         around = bench_around_attention(args, sa, torch, device, pk)
-        around["linear_bias"] = bench_linear(args, sa, torch, device, pk)
-        line["around_attention"] = around
+        around["linear"] = bench_linear(args, sa, torch, device, pk)
+        line["around"] = around
         line["fused_qkv_prefill"] = bench_fused_qkv(args, sa, torch, device, pk)
+        line["tiny_prefill"] = bench_tiny_prefill(args, sa, torch, device, pk)
+        line["small_batch_decode"] = bench_graph_decode(args, sa, torch, device, pk, 32, DECODE["kv_len"], 7)
+        line["long_single_decode"] = bench_graph_decode(args, sa, torch, device, pk, 8, LONG["kv_len"], 3)
+        line["paged_decode"] = bench_paged_decode(args, sa, torch, device, pk)
+        line["mixed"] = bench_mixed(args, sa, torch, device, pk)
+        line["prefill"] = bench_prefill(args, sa, torch, device, pk)
+    line["roofline"] = roofline
     return line, host
 
 
 def bench_paged_decode(args, sa, torch, device, pk):
     """Paged decode: 64 sequences x 4096 cached tokens (512 MiB of KV, larger than L2),
-    64/8 heads, the library's split count, decode then merge; events at the ends of the
-    steps and around each decode launch in the same pass."""
+    64/8 heads, the library's split count, decode then merge; one pass timed at its ends,
+    one with events around each decode launch."""
     cfg = DECODE
     b, kvl, hq, hkv, d = cfg["batch"], cfg["kv_len"], cfg["hq"], cfg["hkv"], cfg["d"]
     host = workloads.make_decode(cfg["seed"], [kvl] * b, hq, hkv, d, cfg["page_size"], cfg["sink_std"])
@@ -352,12 +349,10 @@ def bench_paged_decode(args, sa, torch, device, pk):
     del dv
     torch.cuda.empty_cache()
     ach = nbytes / (dec_ms * 1e-3) / 1e9
-    return {"workload": "paged_decode: 64 seqs x 4096 tokens, 64/8 heads, page 16, permuted pages",
-            "num_splits": s, "step_us": round(step_ms * 1e3, 2), "value": round(nbytes / (step_ms * 1e-3) / 1e9, 1),
-            "unit": "GB/s", "kernel": "sink_decode_kernel", "kernel_us": round(dec_ms * 1e3, 2),
-            "achieved": round(ach, 1), "peak": pk["hbm"], "frac": round(ach / pk["hbm"], 4),
-            "frac_of_nominal_hbm": round(ach / NOMINAL_HBM_GBS, 4),
-            "kernel_timing": "events around each decode launch (separate pass; step_us has none)",
+    return {"workload": "64 x 4096 tokens", "num_splits": s, "step_us": round(step_ms * 1e3, 2),
+            "value": round(nbytes / (step_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "kernel": "sink_decode_kernel",
+            "kernel_us": round(dec_ms * 1e3, 2), "achieved": round(ach, 1), "peak": pk["hbm"],
+            "frac": round(ach / pk["hbm"], 4), "frac_of_nominal_hbm": round(ach / NOMINAL_HBM_GBS, 4),
             "traffic": recorded_traffic("sink_decode_kernel", DECODE_SOURCES),
             "gpu_launches": (2 if s > 1 else 1) * (2 * reps + 5)}
 
@@ -401,14 +396,11 @@ def bench_mixed(args, sa, torch, device, pk):
     t_tc = flops / (pk["bf16"] * 1e12)
     t_hbm = nbytes / (pk["hbm"] * 1e9)
     bound = "tensor" if t_tc >= t_hbm else "hbm"
-    return {"workload": "ragged_mixed: 32 seqs, KV log-uniform in [1, 32768], half decode rows, "
-                        "half 128-2048-token chunks, causal, 64/8 heads, page 16",
-            "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 4), "flops": flops, "bytes": nbytes,
-            "decode_rows": int((q == 1).sum()), "kernel": "sink_prefill_kernel", "bound": bound,
+    return {"workload": "ragged_mixed: 32 paged seqs, half decode rows", "value": round(flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 4), "flops": flops,
+            "bytes": nbytes, "kernel": "sink_prefill_kernel", "bound": bound,
             "frac": round(max(t_tc, t_hbm) / (ms * 1e-3), 4), "tensor_frac": round(t_tc / (ms * 1e-3), 4),
             "hbm_frac": round(t_hbm / (ms * 1e-3), 4),
-            "frac_rule": "max(FLOPs / peak bf16, bytes / peak HBM) / time",
             "traffic": recorded_traffic("sink_prefill_kernel_mixed", PREFILL_SOURCES),
             "gpu_launches": len(times)}
 
@@ -455,30 +447,27 @@ def bench_tiny_prefill(args, sa, torch, device, pk):
     us_graph = timed(graph.replay, 10) / 200
     flops = prefill_flops(1, cfg["seqlen"], cfg["hq"], cfg["d"])
     tf = flops / (us_graph * 1e-6) / 1e12
-    return {"workload": "tiny_prefill: 1 x 128 tokens, causal, 4 query / 1 KV head, head_dim 64",
-            "us_per_call": round(us, 2), "us_per_call_graph": round(us_graph, 2), "flops": flops,
-            "bound": "tensor", "achieved": round(tf, 4), "peak": pk["bf16"], "unit": "TFLOP/s",
-            "frac": round(tf / pk["bf16"], 6), "note": "latency bound (8.4 MFLOP per call), graph replay",
-            "gpu_launches": reps + 10 + 200}
+    return {"workload": "1 x 128 tokens, 4/1 heads", "us_per_call": round(us, 2),
+            "us_per_call_graph": round(us_graph, 2), "achieved": round(tf, 4), "unit": "TFLOP/s",
+            "frac": round(tf / pk["bf16"], 6), "gpu_launches": reps + 10 + 200}
 
 
-def bench_graph_decode(args, sa, torch, device, pk):
-    """Small-batch decode, where launch overhead shows: one sequence of 4096 cached tokens per
-    step (64/8 heads, page 16) with the library's split count (1 here: one launch whose 16-CTA
-    clusters merge on chip; a count above 1 adds the merge launch).  32 steps cycle over 32
-    different sequences of one permuted page pool (256 MiB of KV, larger than L2), run eagerly
-    and as one captured CUDA graph of the same 32 steps."""
+def bench_graph_decode(args, sa, torch, device, pk, nseq, kvl, seed_offset):
+    """Decode at batch 1: one sequence of ``kvl`` cached tokens per step (64/8 heads, page 16)
+    with the library's split count (1: one launch whose 16-CTA clusters merge on chip; a
+    count above 1 adds the merge launch).  ``nseq`` steps cycle over ``nseq`` different
+    sequences of one permuted page pool (32 x 4096 tokens = 256 MiB, 8 x 131072 = 2 GiB of KV,
+    both larger than L2), run eagerly and as one captured CUDA graph of the same steps."""
     cfg = DECODE
-    nseq, kvl = 32, cfg["kv_len"]
-    host = workloads.make_decode(cfg["seed"] + 7, [kvl] * nseq, cfg["hq"], cfg["hkv"], cfg["d"],
+    host = workloads.make_decode(cfg["seed"] + seed_offset, [kvl] * nseq, cfg["hq"], cfg["hkv"], cfg["d"],
                                  cfg["page_size"], cfg["sink_std"])
     dv = {n: to_dev(host[n], torch, device)
           for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
     hq, d = cfg["hq"], cfg["d"]
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     splits = sa.sink_attn_decode_splits(1, cfg["hkv"], kvl, cfg["page_size"], sms)
-    part_o = torch.empty((nseq, splits, hq, d), dtype=torch.float32, device=device)
-    part_l = torch.empty((nseq, splits, hq), dtype=torch.float32, device=device)
+    part_o = torch.empty((1, splits, hq, d), dtype=torch.float32, device=device)
+    part_l = torch.empty((1, splits, hq), dtype=torch.float32, device=device)
     out = torch.empty((nseq, hq, d), dtype=torch.bfloat16, device=device)
     lse = torch.empty((nseq, hq), dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
@@ -489,8 +478,8 @@ def bench_graph_decode(args, sa, torch, device, pk):
             if splits > 1:
                 sa.sink_attn_decode(dv["q"][sl], dv["k_pages"], dv["v_pages"], dv["page_table"][sl],
                                     dv["kv_lens"][sl], dv["sinks"], cfg["sm_scale"], num_splits=splits,
-                                    out=part_o[sl], lse=part_l[sl], stream=stream)
-                sa.sink_attn_merge(part_o[sl], part_l[sl], out=out[sl], lse=lse[sl], stream=stream)
+                                    out=part_o, lse=part_l, stream=stream)
+                sa.sink_attn_merge(part_o, part_l, out=out[sl], lse=lse[sl], stream=stream)
             else:
                 sa.sink_attn_decode(dv["q"][sl], dv["k_pages"], dv["v_pages"], dv["page_table"][sl],
                                     dv["kv_lens"][sl], dv["sinks"], cfg["sm_scale"], num_splits=1,
@@ -522,12 +511,11 @@ def bench_graph_decode(args, sa, torch, device, pk):
     graph_us = timed(graph.replay)
     step_bytes = decode_bytes(1, kvl, hq, cfg["hkv"], d, host["page_table"].shape[1])
     per_step = 2 if splits > 1 else 1
-    return {"workload": "small-batch decode: 1 seq x 4096 cached tokens per step, 64/8 heads, page 16; "
-                        "32 steps over 32 sequences of a 256 MiB page pool (larger than L2)",
-            "num_splits": splits, "launches_per_step": per_step,
-            "eager_us_per_step": round(eager_us, 2), "graph_us_per_step": round(graph_us, 2),
-            "graph_gbs": round(step_bytes / (graph_us * 1e-6) / 1e9, 1),
-            "eager_gbs": round(step_bytes / (eager_us * 1e-6) / 1e9, 1),
+    del dv
+    torch.cuda.empty_cache()
+    return {"workload": f"1 x {kvl} tokens per step, {nseq} sequences", "num_splits": splits,
+            "launches_per_step": per_step, "eager_us_per_step": round(eager_us, 2),
+            "graph_us_per_step": round(graph_us, 2), "graph_gbs": round(step_bytes / (graph_us * 1e-6) / 1e9, 1),
             "gpu_launches": per_step * nseq * (2 * reps + 2)}
 
 
@@ -594,32 +582,19 @@ def bench_around_attention(args, sa, torch, device, pk):
         sa.moe_router_topk_softmax(rlog, k, topk_idx=idx, topk_weight=w, expert_counts=counts, stream=stream)),
         reps)
 
-    def line(srcs, kernel, ms, nbytes, note):
+    def hbm(kernel, srcs, ms, nbytes):
         gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"workload": note, "kernel": kernel, "us": round(ms * 1e3, 2), "bytes": nbytes,
-                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                             "frac": round(gbs / pk["hbm"], 4),
-                             "traffic": recorded_traffic(kernel, srcs),
-                             "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}}
-    return {"qkv_bias_rope": line(ROPE_SOURCES, "qkv_rope_kernel", rope_ms,
-                                  rope_bytes,
-                                  "32768 tokens, 64/8 heads: bias + YaRN (GPT-OSS constants) on q, k; "
-                                  "q, k, v written contiguous; L2 flushed (written, then read back) before each launch"),
-            "moe_router": line(("router.cu", "router_args.h", "ptx.cuh"), "router_topk_kernel", router_ms,
-                               router_bytes,
-                               "32768 tokens x 128 bf16 logits, top 4, softmax over the selected, "
-                               "expert counts; L2 flushed (written, then read back) before each launch"),
-            "moe_router_fused": {"workload": "router of 32768 tokens: [32768, 2880] x [128, 2880]^T + bias, "
-                                             "bf16 logits, top 4 softmax, counts; L2 flushed before each call",
-                                 "fused_us": round(fused_ms * 1e3, 2), "two_kernels_us": round(two_ms * 1e3, 2),
-                                 "kernel": "linear_bias_kernel (router epilogue)",
-                                 "roofline": {"bound": "hbm", "achieved": round(t * 2880 * 2 / (fused_ms * 1e-3) / 1e9, 1),
-                                              "peak": pk["hbm"], "unit": "GB/s",
-                                              "frac": round(t * 2880 * 2 / (fused_ms * 1e-3) / 1e9 / pk["hbm"], 4),
-                                              "note": "bytes = the hidden states read once (189 MB)",
-                                              "traffic": recorded_traffic("linear_bias_kernel_router",
-                                                                          ("linear.cu", "linear_args.h", "ptx.cuh")),
-                                              "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"}},
+        return {"kernel": kernel, "us": round(ms * 1e3, 2), "bytes": nbytes, "achieved": round(gbs, 1),
+                "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4), "traffic": recorded_traffic(kernel, srcs)}
+    fused_gbs = t * 2880 * 2 / (fused_ms * 1e-3) / 1e9  # the hidden states read once
+    return {"qkv_bias_rope": hbm("qkv_rope_kernel", ROPE_SOURCES, rope_ms, rope_bytes),
+            "moe_router": hbm("router_topk_kernel", ("router.cu", "router_args.h", "ptx.cuh"), router_ms,
+                              router_bytes),
+            "moe_router_fused": {"kernel": "linear_bias_kernel", "us": round(fused_ms * 1e3, 2),
+                                 "two_kernels_us": round(two_ms * 1e3, 2), "achieved": round(fused_gbs, 1),
+                                 "unit": "GB/s", "frac": round(fused_gbs / pk["hbm"], 4),
+                                 "traffic": recorded_traffic("linear_bias_kernel_router",
+                                                             ("linear.cu", "linear_args.h", "ptx.cuh"))},
             "gpu_launches": 2 * (reps + 3) + 3 * (reps + 3)}
 
 
@@ -654,11 +629,8 @@ def bench_fused_qkv(args, sa, torch, device, pk):
 
     un_ms = _timed_flushed(torch, device, stream, unfused, reps)
     fu_ms = _timed_flushed(torch, device, stream, fused, reps)
-    return {"workload": "4 x 8192 tokens, 64/8 heads: QKV bias + YaRN + causal prefill, L2 flushed before each pair",
-            "unfused_us": round(un_ms * 1e3, 1), "fused_us": round(fu_ms * 1e3, 1),
-            "fused_over_unfused": round(fu_ms / un_ms, 4),
-            "unfused": "qkv_bias_rope + sink_attn_prefill", "fused": "qkv_bias_rope_kv + sink_attn_prefill_qkv",
-            "gpu_launches": 4 * (reps + 3)}
+    return {"workload": "4 x 8192 tokens", "unfused_us": round(un_ms * 1e3, 1), "fused_us": round(fu_ms * 1e3, 1),
+            "fused_over_unfused": round(fu_ms / un_ms, 4), "gpu_launches": 4 * (reps + 3)}
 
 
 def bench_linear(args, sa, torch, device, pk):
@@ -676,18 +648,10 @@ def bench_linear(args, sa, torch, device, pk):
     ref_ms = _timed_flushed(torch, device, stream, lambda: torch.nn.functional.linear(x, w, b), reps)
     flops = 2.0 * m * n * k
     tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": "output projection of 32768 tokens: [32768, 4096] x [2880, 4096]^T + bias, bf16, "
-                        "fp32 accumulator seeded with the bias; L2 flushed (written, then read back) before each launch",
-            "kernel": "linear_bias_kernel", "ms": round(ms, 4), "flops": flops,
-            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
-                         "frac": round(tf / pk["bf16"], 4),
-                         "peak_source": pk["source"] + " (bf16_tflops, burst: kernel timed alone)",
-                         "traffic": recorded_traffic("linear_bias_kernel", ("linear.cu", "linear_args.h", "ptx.cuh")),
-                         "traffic_unit": "bytes per launch",
-                         "traffic_source": "profiles/traffic.txt (ncu capture of this workload)"},
-            "cublas_context": {"ms": round(ref_ms, 4), "tflops": round(flops / (ref_ms * 1e-3) / 1e12, 2),
-                               "note": "torch.nn.functional.linear (cuBLAS), not on this library's path"},
-            "gpu_launches": reps + 3}
+    return {"kernel": "linear_bias_kernel", "ms": round(ms, 4), "achieved": round(tf, 2), "unit": "TFLOP/s",
+            "frac": round(tf / pk["bf16"], 4),
+            "traffic": recorded_traffic("linear_bias_kernel", ("linear.cu", "linear_args.h", "ptx.cuh")),
+            "cublas_tflops": round(flops / (ref_ms * 1e-3) / 1e12, 2), "gpu_launches": reps + 3}
 
 
 def bench_prefill(args, sa, torch, device, pk):
@@ -722,14 +686,11 @@ def bench_prefill(args, sa, torch, device, pk):
     ms = [a.elapsed_time(b) for a, b in times]
     avg = sum(ms) / len(ms)
     tflops = flops / (avg * 1e-3) / 1e12
-    return {"workload": "causal_prefill: 4 x 8192 tokens, causal, 64/8 heads, head_dim 64, sinks N(0, 2)",
-            "value": round(tflops, 2), "unit": "TFLOP/s", "ms": round(avg, 4), "flops": flops,
-            "bound": "tensor", "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2),
-            "peak": pk["bf16"], "frac": round(tflops / pk["bf16"], 4),
-            "peak_source": pk["source"] + " bf16_tflops (burst: kernel timed alone)",
-            "traffic": recorded_traffic("sink_prefill_kernel", PREFILL_SOURCES),
-            "traffic_source": "profiles/traffic.txt: ncu, 1 of 4 sequences, x4",
-            "l2": "flushed (256 MiB written, read back) before every launch",
+    return {"workload": "causal_prefill: 4 x 8192 tokens, 64/8 heads", "value": round(tflops, 2),
+            "unit": "TFLOP/s", "ms": round(avg, 4), "flops": flops, "bound": "tensor",
+            "kernel": "sink_prefill_kernel", "achieved": round(tflops, 2), "peak": pk["bf16"],
+            "frac": round(tflops / pk["bf16"], 4), "peak_source": pk["source"] + " bf16 burst",
+            "traffic": recorded_traffic("sink_prefill_kernel", PREFILL_SOURCES), "l2": "flushed before each launch",
             "gpu_launches": steps}
 
 
@@ -1022,13 +983,13 @@ def main():
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(host)
             per_row = cpu_baselines_per_row()
+            # the oracle beside the other rows: value in the row's unit, one thread
             if "prefill" in line:
-                cb = per_row["prefill"]
-                line["prefill"].update({"cpu_baseline_value": cb["value"], "cpu_baseline_unit": cb["unit"],
-                                        "cpu_baseline_cores": cb["cores"], "cpu_baseline_sample": cb["sample"]})
-            for key in ("qkv_bias_rope", "moe_router", "linear_bias"):
-                if "around_attention" in line and key in line["around_attention"]:
-                    line["around_attention"][key]["cpu_baseline"] = per_row[key]
+                line["prefill"]["cpu_baseline"] = {k: per_row["prefill"][k] for k in ("value", "cores", "sample")}
+            for key, row in (("qkv_bias_rope", "qkv_bias_rope"), ("moe_router", "moe_router"),
+                             ("linear_bias", "linear")):
+                if "around" in line and row in line["around"]:
+                    line["around"][row]["cpu_baseline"] = per_row[key]["value"]
         print(json.dumps(line), flush=True)
 
 
