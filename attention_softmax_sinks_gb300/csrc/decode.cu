@@ -21,7 +21,10 @@
 //  * launched with programmatic dependent launch, so a CTA is resident while
 //    the kernel before it (the previous step's merge) still runs: in that time
 //    it asks L2 for the first four pages of each warp's ring, which hides the
-//    page-table -> page latency of its start (headline step 85.8 -> 80.8 us).
+//    page-table -> page latency of its start (headline step 85.8 -> 80.8 us);
+//    after the wait, the warp's first page ids are read in the same round trip
+//    as the sequence length, for the length seen before the wait, and read
+//    again only if the length changed (64 x 4096 step 78.3 -> 78.0 us).
 #include <mutex>
 #include "internal.h"
 #include "ptx.cuh"
@@ -135,16 +138,16 @@ __global__ void __launch_bounds__(kWarps * 32)
   const uint32_t ring_w = smem_u32(ring + warp * kStages * kSlotBytes);
   const uint32_t full_w = smem_u32(full + warp * kStages);
 
+  // kv_lens and the page table may still be being written by the kernel before this one:
+  // what is read before the wait below only chooses what to prefetch and which page-table
+  // entries to read early (both are read again after the wait and checked).
+  const int kvl = a.kv_lens[blockIdx.z];
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(full_w + 8 * s, 1);
     fence_barrier_init();
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
     // While the kernel before this one finishes, ask L2 for this warp's first pages.
-    // kv_lens and the page table may still be being written by that kernel: what is
-    // read here only chooses what to prefetch (L2 stays coherent, nothing read here
-    // is used for the attention itself, which re-reads both after the wait below).
-    const int kvl = a.kv_lens[blockIdx.z];
     if (kvl > 0 && kvl <= a.max_pages * kPageSize) {
       const int np = (kvl + kPageSize - 1) / kPageSize;
       const int ns = a.cluster > 1 ? a.cluster : a.num_splits;
@@ -169,32 +172,41 @@ __global__ void __launch_bounds__(kWarps * 32)
   // an input comes after this wait.
   pdl_wait_primary();
 
-  int kv_len = a.kv_lens[b];
   const int cap = a.max_pages * kPageSize;
-  if (kv_len < 0 || kv_len > cap) {
-    if (threadIdx.x == 0) raise_status(a.status, kStatusBadLen);
-    kv_len = kv_len < 0 ? 0 : cap;
-  }
-  const int n_pages = (kv_len + kPageSize - 1) / kPageSize;
   const bool clustered = a.cluster > 1;  // splits of one (sequence, KV head) form a cluster
   const int n_split = clustered ? a.cluster : a.num_splits;
-  const int per_split = (n_pages + n_split - 1) / n_split;
-  const int p_begin = min(split * per_split, n_pages);
-  const int p_end = min(p_begin + per_split, n_pages);
-  // this warp's pages: p_begin + warp + j * kWarps, j = 0 .. my_count-1
-  const int my_first = p_begin + warp;
-  const int my_count = my_first < p_end ? (p_end - my_first + kWarps - 1) / kWarps : 0;
-
   const int32_t* ptab = a.page_table + static_cast<size_t>(b) * a.max_pages;
-
+  // this warp's pages for a sequence of kv tokens: p_begin + warp + j * kWarps, j < count
+  auto warp_pages = [&](int kv, int& first, int& count) {
+    const int np = (kv + kPageSize - 1) / kPageSize;
+    const int per = (np + n_split - 1) / n_split;
+    const int pb = min(split * per, np);
+    const int pe = min(pb + per, np);
+    first = pb + warp;
+    count = first < pe ? (pe - first + kWarps - 1) / kWarps : 0;
+  };
   // Page ids, 32 of this warp's pages at a time: lane l of ids_cur holds the id of the
   // warp's page 32 w + l (window w holds the page being consumed) and ids_next those of
   // window w + 1, read a whole window ahead, so no page-table read sits in the loop.
+  int my_first, my_count;
   auto load_ids = [&](int w) {
     const int jj = w * 32 + lane;
     return jj < my_count ? ptab[my_first + jj * kWarps] : -1;
   };
+  // The first window is read together with kv_lens, for the length read before the wait;
+  // if the length read now differs, it is read again.
+  const int kv_early = (kvl < 0 || kvl > cap) ? 0 : kvl;
+  warp_pages(kv_early, my_first, my_count);
   int ids_cur = load_ids(0);
+  int kv_len = a.kv_lens[b];
+  if (kv_len < 0 || kv_len > cap) {
+    if (threadIdx.x == 0) raise_status(a.status, kStatusBadLen);
+    kv_len = kv_len < 0 ? 0 : cap;
+  }
+  if (kv_len != kv_early) {
+    warp_pages(kv_len, my_first, my_count);
+    ids_cur = load_ids(0);
+  }
   int ids_next = load_ids(1);
   auto id_of = [&](int k, int w) {  // all lanes; page k lies in window w or w + 1
     const int in_cur = __shfl_sync(0xffffffffu, ids_cur, k & 31);
