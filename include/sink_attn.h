@@ -151,9 +151,10 @@ sa_status sink_attn_decode(const void* q, const void* paged_k, const void* paged
  *             the query part is read
  *  rope_table fp32 [tokens, head_dim / 2, 2], as written by the _kv calls
  *  other arguments as for the plain call; num_qo_heads + 2 num_kv_heads <= 128
- *  (SA_ERR_UNSUPPORTED otherwise).  The prefills run their persistent
- *  schedule, where an idle warp rotates the next item's query rows while the
- *  current item computes.
+ *  (SA_ERR_UNSUPPORTED otherwise).  The prefills use the same schedules as
+ *  the plain calls; once a query tile has landed in shared memory, each
+ *  softmax thread biases and rotates its own row there before the tile's
+ *  first score product.
  */
 sa_status sink_attn_prefill_qkv(const void* qkv, const void* qkv_bias, const float* rope_table,
                                 const void* k, const void* v, const float* sinks,
