@@ -860,6 +860,8 @@ def run_profile_case(case):
 
     decode:  32 sequences x 4096 tokens (256 MiB of KV, larger than L2), 64/8 heads, 4 splits.
     decode_long: 2 sequences x 131072 tokens (512 MiB of KV), 64/8 heads, 32 splits.
+    decode_one: one sequence of 4096 tokens per launch (16-CTA clusters merged on chip),
+             launches cycling over 32 sequences of a 256 MiB pool.
     prefill: 1 x 8192 tokens causal, 64/8 heads.
     prefill_persistent: 8192 + 8191 tokens causal (the persistent schedule), 64/8 heads.
     mixed:   the ragged mixed batch (32 sequences, paged, GQA-packed decode rows).
@@ -894,6 +896,16 @@ def run_profile_case(case):
             po, pl = sa.sink_attn_decode(dev["q"], dev["k_pages"], dev["v_pages"], dev["page_table"],
                                          dev["kv_lens"], dev["sinks"], cfg["sm_scale"], num_splits=cfg["num_splits"])
             sa.sink_attn_merge(po, pl)
+    elif case == "decode_one":
+        cfg = DECODE
+        host = workloads.make_decode(cfg["seed"] + 7, [cfg["kv_len"]] * 32, cfg["hq"], cfg["hkv"], cfg["d"],
+                                     cfg["page_size"], cfg["sink_std"])
+        dev = {n: to_dev(host[n], torch, device)
+               for n in ("q", "k_pages", "v_pages", "page_table", "kv_lens", "sinks")}
+        for i in range(5):
+            sl = slice(i, i + 1)
+            sa.sink_attn_decode(dev["q"][sl], dev["k_pages"], dev["v_pages"], dev["page_table"][sl],
+                                dev["kv_lens"][sl], dev["sinks"], cfg["sm_scale"], num_splits=1)
     elif case == "prefill_persistent":
         cfg = PREFILL
         lens = [cfg["seqlen"], cfg["seqlen"] - 1]  # not uniform: the persistent schedule
@@ -952,7 +964,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
-    ap.add_argument("--profile", choices=["decode", "decode_long", "prefill", "prefill_persistent", "mixed", "linear",
+    ap.add_argument("--profile", choices=["decode", "decode_long", "decode_one", "prefill", "prefill_persistent", "mixed", "linear",
                                           "rope", "router", "router_fused"], default=None,
                     help="run a small case of one kernel for an ncu capture, then exit")
     args = ap.parse_args()
