@@ -2,6 +2,7 @@
 // argument validation, the per-device status word, TMA descriptor encoding
 // and the launches.  No allocation, no synchronisation (except the explicit
 // status read-back).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -123,17 +124,17 @@ sa_status check_heads(int hq, int hkv, int head_dim) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-int g_sm_count[kMaxDevices] = {};
+std::atomic<int> g_sm_count[kMaxDevices];  // 0 until asked (host threads may race)
 
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
-  if (!g_sm_count[dev]) {
+  if (!g_sm_count[dev].load(std::memory_order_relaxed)) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    g_sm_count[dev] = n;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return g_sm_count[dev].load(std::memory_order_relaxed);
 }
 
 // Cluster size for an unsplit decode: CTAs of one (sequence, KV head) share its

@@ -42,6 +42,7 @@
 // runs after the CTA's last MMA, so its instruction count is exposed).  The
 // arithmetic is that of the plain layer followed by the standalone router, bit
 // for bit.
+#include <atomic>
 #include <cstdint>
 
 #include "linear_args.h"
@@ -442,14 +443,17 @@ template <int BN, int MT, int SLOTS = 0>
 cudaError_t launch_linear_t(const CUtensorMap& amap, const CUtensorMap& bmap, const LinearArgs& a,
                             int sms, cudaStream_t stream) {
   using C = LinCfg<BN, MT>;
-  static bool attr_set[64] = {};
+  // the shared-memory opt-in, once per device (host threads may race here: atomic flags,
+  // and setting the attribute twice is harmless)
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_bias_kernel<BN, MT, SLOTS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(linear_bias_kernel<BN, MT, SLOTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmem));
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   const int tiles = a.tiles_m * a.tiles_n;
   const int grid = tiles < sms ? tiles : sms;

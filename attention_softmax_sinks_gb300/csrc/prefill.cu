@@ -39,6 +39,7 @@
 //    into TMEM and finally stores out = O/d and lse = m + ln d.
 //  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 //                P0 [384,448) P1 [448,512).
+#include <atomic>
 #include <cstddef>
 
 #include "internal.h"
@@ -832,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-int g_prefill_sms[64] = {};
+std::atomic<int> g_prefill_sms[64];  // SM count per device, 0 until asked (host threads may race)
 
 }  // namespace
 
@@ -847,18 +848,19 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& qpmap, co
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!g_prefill_sms[dev]) {
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  int sms = g_prefill_sms[dev].load(std::memory_order_relaxed);
+  if (!sms) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    g_prefill_sms[dev] = n > 0 ? n : 1;
+    if (sms <= 0) sms = 1;
+    g_prefill_sms[dev].store(sms, std::memory_order_relaxed);
   }
   // Contiguous KV with every sequence at max_q tokens (their sum is then
   // batch * max_q): items are uniform per query block, so one CTA per item in
   // heaviest-first order.  Otherwise a persistent grid with the sorted schedule.
   const bool uniform = !a.paged && static_cast<long long>(a.total_q) == static_cast<long long>(a.batch) * a.max_q;
   const bool persistent = !uniform || items > 0x7fffffffLL;
-  const int blocks = static_cast<int>(persistent ? (items < g_prefill_sms[dev] ? items : g_prefill_sms[dev]) : items);
+  const int blocks = static_cast<int>(persistent ? (items < sms ? items : sms) : items);
   const size_t smem = (persistent ? sizeof(PrefillSmem) : kSmemOnePerCta) + 1024;
   auto kern = a.paged ? (persistent ? sink_prefill_kernel<true, true> : sink_prefill_kernel<true, false>)
                       : (persistent ? sink_prefill_kernel<false, true> : sink_prefill_kernel<false, false>);
