@@ -45,6 +45,7 @@ METRIC = "sink-attn prefill TFLOP/s & decode KV GB/s on 1 GB300, % of roofline"
 DECODE = workloads.WORKLOADS["paged_decode"]
 PREFILL = workloads.WORKLOADS["causal_prefill"]
 LONG = workloads.WORKLOADS["long_decode"]
+LONG_WORKLOAD = "long_decode: 8 x 131072 cached tokens, 64/8 heads, d 64, page 16, 32 splits + merge"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context for the measured-copy fraction)
 # kernel sources whose hash keys the recorded DRAM traffic (profiles/traffic.txt)
 DECODE_SOURCES = ("decode.cu", "ptx.cuh", "internal.h", "rope_math.cuh")
@@ -267,8 +268,7 @@ def run_ours(args, rank, world, device):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks, permuted pages",
-        "config": {"workload": "long_decode: 8 x 131072 cached tokens, 64/8 heads, d 64, page 16, "
-                               "32 splits + merge",
+        "config": {"workload": LONG_WORKLOAD,
                    "batch": b, "kv_len": kvl, "num_splits": s,
                    "l2": "inputs > L2 (2 GiB KV per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -716,9 +716,10 @@ def host_description():
             "machine": platform.machine()}
 
 
-def oracle_decode_groups(host, cfg, groups, workers):
+def oracle_decode_groups(host, cfg, groups, workers, max_tokens=None):
     """The oracle over (sequence, KV head) groups of a decode workload, on ``workers``
-    threads (one BLAS thread each); returns (seconds, algorithmic bytes)."""
+    threads (one BLAS thread each); returns (seconds, algorithmic bytes).  ``max_tokens``
+    limits each group to its sequence's first tokens (a shorter sample of the same work)."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     g = cfg["hq"] // cfg["hkv"]
@@ -727,6 +728,8 @@ def oracle_decode_groups(host, cfg, groups, workers):
     def one(u):
         b, kvh = divmod(u % (nb * cfg["hkv"]), cfg["hkv"])
         kv = int(host["kv_lens"][b])
+        if max_tokens is not None:
+            kv = min(kv, int(max_tokens))
         kb = oracle.widen_bf16(oracle.gather_pages(host["k_pages"][:, kvh:kvh + 1], host["page_table"][b], kv)[:, 0])
         vb = oracle.widen_bf16(oracle.gather_pages(host["v_pages"][:, kvh:kvh + 1], host["page_table"][b], kv)[:, 0])
         qf = oracle.widen_bf16(host["q"][b, kvh * g:(kvh + 1) * g])
@@ -822,32 +825,42 @@ def cpu_baselines_per_row(budget_s=3.0):
     return res
 
 
-def run_reference(args):
+def run_reference(args, budget_s=150.0):
     """The oracle as the reference arm: each step is one (sequence, KV head) group per host
-    core of the headline workload (8 x 131072-token decode), all cores busy."""
+    core of the headline workload (8 x 131072-token decode), all cores busy.  The first
+    warm-up step times a full step; when the requested warm-up + timed steps would take
+    longer than ``budget_s``, every group is cut to its sequence's first tokens so that the
+    run stays within about that long (the line says so in its sample)."""
     cfg = LONG
     host = workloads.make_decode(cfg["seed"], [cfg["kv_len"]] * cfg["batch"], cfg["hq"], cfg["hkv"],
                                  cfg["d"], cfg["page_size"], cfg["sink_std"])
     hd = host_description()
     workers = hd["nproc"]
-    for w in range(args.warmup):
-        oracle_decode_groups(host, cfg, range(w * workers, (w + 1) * workers), workers)
+    t_full, _ = oracle_decode_groups(host, cfg, range(workers), workers)
+    max_tokens = None
+    if (args.warmup + args.steps) * t_full > budget_s:
+        frac = budget_s / ((args.warmup + args.steps) * t_full)
+        ps = cfg["page_size"]
+        max_tokens = max(ps, int(cfg["kv_len"] * frac) // ps * ps)
+    for w in range(1, args.warmup):
+        oracle_decode_groups(host, cfg, range(w * workers, (w + 1) * workers), workers, max_tokens)
     tot_s = 0.0
     tot_b = 0
     for k in range(args.steps):
-        secs, nb = oracle_decode_groups(host, cfg, range(k * workers, (k + 1) * workers), workers)
+        secs, nb = oracle_decode_groups(host, cfg, range(k * workers, (k + 1) * workers), workers, max_tokens)
         tot_s += secs
         tot_b += nb
     value = tot_b / tot_s / 1e9
-    sample = (f"{workers} (sequence, KV head) groups of the 8 x 131072 decode per step, fp64 numpy, "
+    span = (f"the first {max_tokens} of each sequence's {cfg['kv_len']} tokens" if max_tokens
+            else f"all {cfg['kv_len']} tokens")
+    sample = (f"{workers} (sequence, KV head) groups of the 8 x 131072 decode per step ({span}), fp64 numpy, "
               f"{workers} threads x 1 BLAS thread")
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": "long_decode: 8 seqs x 131072 cached tokens, 64/8 heads, head_dim 64, "
-                               "page 16, permuted pages, 32 splits + merge"},
+        "config": {"workload": LONG_WORKLOAD},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": workers, "kind": "oracle",
                          "sample": sample, "nproc": hd["nproc"], "cpu_model": hd["cpu_model"]},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

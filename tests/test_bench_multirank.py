@@ -60,3 +60,21 @@ def test_reference_arm_prints_from_rank0_only():
                           "--steps", "1", "--warmup", "3"], capture_output=True, text=True, env=env,
                          timeout=600)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_reference_arm_stays_within_its_budget():
+    """The reference arm (the fp64 oracle on the host cores) cuts each group to a sequence
+    prefix when the requested steps would take longer than its budget, and says so."""
+    import argparse
+    import time
+    sys.path.insert(0, ROOT)
+    import bench
+    args = argparse.Namespace(steps=40, warmup=3)
+    t0 = time.perf_counter()
+    line = bench.run_reference(args, budget_s=4.0)
+    oracle_s = time.perf_counter() - t0
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 40
+    assert line["config"]["workload"] == bench.LONG_WORKLOAD
+    assert "the first" in line["cpu_baseline"]["sample"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert oracle_s < 120  # data generation plus about the budget
