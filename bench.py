@@ -825,7 +825,7 @@ def cpu_baselines_per_row(budget_s=3.0):
     return res
 
 
-def run_reference(args, budget_s=150.0):
+def run_reference(args, budget_s=90.0):
     """The oracle as the reference arm: each step is one (sequence, KV head) group per host
     core of the headline workload (8 x 131072-token decode), all cores busy.  The first
     warm-up step times a full step; when the requested warm-up + timed steps would take
