@@ -342,10 +342,33 @@ def pin_row_sampling_paths():
         assert np.all(o[rest] == 0) and np.all(l[rest] == 0), "unpicked sequences must stay 0"
 
 
+def pin_merge_limits():
+    """The merge at the limits of its inputs, against what the definition fixes: a row whose
+    splits are all empty (lse -inf) is out = 0, lse = -inf; a split with lse +inf (a +inf
+    sink) takes all the weight, shared equally among such splits, and lse = +inf; an empty
+    split next to finite ones changes nothing."""
+    rng = _rng(23)
+    o = rng.standard_normal((1, 4, 3, 5))
+    l = np.array([[[-np.inf, 0.5, -np.inf], [-np.inf, np.inf, -np.inf],
+                   [-np.inf, 1.5, 2.0], [-np.inf, np.inf, -1.0]]])   # [1, S=4, H=3]
+    o[0, :, 0] = 0.0                       # empty splits hold o = 0
+    o[0, 0, 2] = 0.0
+    out, lse = oracle.merge(o, l)
+    _close(out[0, 0], np.zeros(5), 0.0, "all-empty row out")
+    assert lse[0, 0] == -np.inf, "all-empty row lse"
+    _close(out[0, 1], 0.5 * (o[0, 1, 1] + o[0, 3, 1]), 1e-15, "+inf splits share the weight")
+    assert lse[0, 1] == np.inf, "+inf split lse"
+    # head 2: splits 2 and 3 finite, split 0 empty: the empty one changes nothing
+    ref_o, ref_l = oracle.merge(o[:, 2:, 2:3], l[:, 2:, 2:3])
+    _close(out[0, 2], ref_o[0, 0], 1e-15, "empty split ignored (out)")
+    _close(lse[0, 2], ref_l[0, 0], 1e-15, "empty split ignored (lse)")
+    _close(lse[0, 2], np.logaddexp(2.0, -1.0), 1e-15, "two finite splits lse")
+
+
 ALL_PINS = [pin_hand_worked, pin_sdpa_reduction, pin_large_sink_saturates, pin_normalisation,
             pin_single_key_closed_form, pin_identical_keys, pin_split_merge_invariance,
             pin_brute_force_decimal, pin_online_algorithm, pin_paging, pin_gqa_mapping,
-            pin_causal_counts, pin_row_sampling_paths]
+            pin_causal_counts, pin_row_sampling_paths, pin_merge_limits]
 
 
 def failing_pins():

@@ -120,6 +120,28 @@ def _online_d_starts_at_zero(q, k, v, sink, sm_scale, block):
     return acc / d, m + math.log(d)
 
 
+_ORIG_MERGE = oracle.merge
+
+
+def _merge_posinf_as_finite(partial_o, partial_lse):
+    # forgets the +inf case: weights e^(lse - max) with max = +inf
+    po = np.asarray(partial_o, dtype=np.float64)
+    pl = np.asarray(partial_lse, dtype=np.float64)
+    m = pl.max(axis=1, keepdims=True)
+    with np.errstate(invalid="ignore", over="ignore"):
+        w = np.where(np.isneginf(pl), 0.0, np.exp(pl - np.where(np.isneginf(m), 0.0, m)))
+        z = w.sum(axis=1, keepdims=True)
+        lse = np.where(np.isneginf(m), -np.inf, m + np.log(np.where(z > 0, z, 1.0)))[:, 0]
+        out = np.einsum("bsh,bshd->bhd", np.where(z > 0, w / np.where(z > 0, z, 1.0), 0.0), po)
+    return out, lse
+
+
+def _merge_empty_row_lse_zero(partial_o, partial_lse):
+    # an all-empty row reports lse = 0 (log of the guard value) instead of -inf
+    out, lse = _ORIG_MERGE(partial_o, partial_lse)
+    return out, np.where(np.isneginf(lse), 0.0, lse)
+
+
 MUTANTS = {
     "sink_scaled_by_sm_scale": ("attention_with_sink", _mut_attention(_sink_scaled)),
     "sink_dropped": ("attention_with_sink", _mut_attention(_sink_dropped)),
@@ -134,6 +156,8 @@ MUTANTS = {
     "sequence_lookup_left": ("locate_token", _locate_left),
     "row_index_not_local": ("locate_token", _locate_global_index),
     "decode_batches_by_position": ("decode", _decode_batches_by_position),
+    "merge_posinf_as_finite": ("merge", _merge_posinf_as_finite),
+    "merge_empty_row_lse_zero": ("merge", _merge_empty_row_lse_zero),
 }
 
 
