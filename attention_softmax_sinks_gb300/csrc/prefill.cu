@@ -424,7 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
+  // The TMEM base is read from shared memory inside each role that needs it: kept in a
+  // register across the register split, the one-item form spilled it.
+  auto tmem_base = [&]() { return *reinterpret_cast<volatile const uint32_t*>(&sm.tmem_base); };
 
   // Runs `body(item, item_index_of_this_cta, first_global_kv_tile)` for every
   // item of this CTA: the single item of a non-persistent CTA, or the snake
@@ -538,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = warp - 1;
       if (lane == 0 && t < ntiles) {
         bool ok = true;
+        const uint32_t tmem = tmem_base();
         const uint32_t d_s = tmem + kColS + t * 128, d_o = tmem + kColO + t * 64;
         const uint32_t a_p = tmem + kColP + t * 64;
         for_items([&](const WorkItem& w, int it, int g) {
@@ -605,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qw = warp & 3;            // TMEM lane quarter
     const int r = qw * 32 + lane;       // row within the block
     if (t < ntiles) {
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+      const uint32_t lane_base = tmem_base() + (static_cast<uint32_t>(qw * 32) << 16);
       const uint32_t s_col = lane_base + kColS + t * 128;
       const uint32_t o_col = lane_base + kColO + t * 64;
       const uint32_t p_col = lane_base + kColP + t * 64;
@@ -830,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = max(0, issued_q - 2); it < issued_q; ++it)
       mbar_wait(smem_u32(&sm.q_full[it & 1]), (it >> 1) & 1, 2000000000ull);
   }
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem_base(), kTmemCols);
 }
 
 std::atomic<int> g_prefill_sms[64];  // SM count per device, 0 until asked (host threads may race)
