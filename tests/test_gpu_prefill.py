@@ -42,6 +42,20 @@ def test_ragged_prefill(causal, hq, hkv):
     assert sa.sink_attn_device_status(True) == 0
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("lens,hq,hkv", [([1024], 8, 1), ([640, 640, 640], 64, 8)])
+def test_uniform_prefill_both_launch_forms(lens, hq, hkv, causal):
+    """Equal-length contiguous batches: 32 items (one CTA per item, a single wave) and
+    480 items (more than the SMs: the persistent grid)."""
+    sa = require_gpu()
+    data = workloads.make_prefill(8, lens, hq, hkv, 64)
+    o, l = _run(sa, data, lens[0], 0.125, causal)
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"],
+                            0.125, causal)
+    assert_close(host(o), host(l), ro, rl, f"uniform prefill {len(lens)}x{lens[0]} {hq}/{hkv} causal={causal}")
+    assert sa.sink_attn_device_status(True) == 0
+
+
 @pytest.mark.parametrize("sink_fill", [-np.inf, 20.0, 1.0e4])
 def test_prefill_sink_limits(sink_fill):
     sa = require_gpu()
