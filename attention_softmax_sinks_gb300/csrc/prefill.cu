@@ -35,9 +35,12 @@
 //    read from TMEM (M=128, N=64, K=128); completion through tcgen05.commit.
 //    Per KV tile the issuer puts PV(j-1) ahead of S(j+1).
 //  * warps 4-7 and 8-11 -- one softmax warpgroup per query tile; thread r
-//    owns row r (TMEM lane r): reads its 128 scores, masks on diagonal tiles
-//    only, updates the running max lazily (O and d are rescaled only when the
-//    max grows by more than 2^8, which leaves O/d unchanged), writes P as bf16
+//    owns row r (TMEM lane r): reads its 128 scores with the reducing TMEM load
+//    (tcgen05.ld.red, sm_103a), which also returns each 32-column slice's max, so
+//    a full tile's row max costs three max instructions; masks and takes the max
+//    itself on diagonal and tail tiles only; updates the running max lazily
+//    (O and d are rescaled only when the max grows by more than 2^8, which
+//    leaves O/d unchanged), writes P as bf16
 //    into TMEM and finally stores out = O/d and lse = m + ln d.
 //  TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 //                P0 [384,448) P1 [448,512).
@@ -673,35 +676,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int gg = g + j;
           if (!wait_bar(smem_u32(&sm.s_full[t]), gg & 1, a.timeout_ns, abort_flag)) return ok = false;
           tc_fence_after();
+          // S_t row r with the maxima of its four 32-column slices (reducing loads)
           uint32_t sr[128];
-          tmem_ld32_at<0>(s_col + 0, sr);
-          tmem_ld32_at<32>(s_col + 32, sr);
-          tmem_ld32_at<64>(s_col + 64, sr);
-          tmem_ld32_at<96>(s_col + 96, sr);
+          float pm0, pm1, pm2, pm3;
+          tmem_ld32_max_at<0>(s_col + 0, sr, pm0);
+          tmem_ld32_max_at<32>(s_col + 32, sr, pm1);
+          tmem_ld32_max_at<64>(s_col + 64, sr, pm2);
+          tmem_ld32_max_at<96>(s_col + 96, sr, pm3);
           tc_wait_ld();
           tc_fence_before();
           mbar_arrive(smem_u32(&sm.s_free[t]));  // the MMA may now overwrite S_t
           float s[128];
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+          // Row max over the visible keys: on a full tile, the loads' own maxima; on a
+          // diagonal or tail tile the masked scores are dropped first, then four independent
+          // 3-input max chains take the max of what is left.
           const int key0 = j * kBlockK;
-          if (key0 + kBlockK - 1 > limit) {  // diagonal / tail tile: mask
+          float mraw = fmax3(pm0, pm1, fmaxf(pm2, pm3));
+          if (key0 + kBlockK - 1 > limit) {
 #pragma unroll
             for (int c = 0; c < 128; ++c)
               if (key0 + c > limit) s[c] = kNegInf;
-          }
-          // row max: four independent 3-input max chains
-          float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+            float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
 #pragma unroll
-          for (int c = 4; c < 124; c += 8) {
-            m0 = fmax3(m0, s[c], s[c + 1]);
-            m1 = fmax3(m1, s[c + 2], s[c + 3]);
-            m2 = fmax3(m2, s[c + 4], s[c + 5]);
-            m3 = fmax3(m3, s[c + 6], s[c + 7]);
+            for (int c = 4; c < 124; c += 8) {
+              m0 = fmax3(m0, s[c], s[c + 1]);
+              m1 = fmax3(m1, s[c + 2], s[c + 3]);
+              m2 = fmax3(m2, s[c + 4], s[c + 5]);
+              m3 = fmax3(m3, s[c + 6], s[c + 7]);
+            }
+            m0 = fmax3(m0, s[124], s[125]);
+            m1 = fmax3(m1, s[126], s[127]);
+            mraw = fmax3(m0, m1, fmaxf(m2, m3));
           }
-          m0 = fmax3(m0, s[124], s[125]);
-          m1 = fmax3(m1, s[126], s[127]);
-          const float mx = fmax3(m0, m1, fmaxf(m2, m3)) * a.scale_log2;
+          const float mx = mraw * a.scale_log2;
           const bool grow = mx > m + kRescaleThreshold;
           float factor = 1.0f;
           if (grow) {
