@@ -586,8 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(smem_u32(&sm.kv_empty[gg % kStages]));
           };
           // The very first tile of tile 1 starts one softmax phase behind tile 0,
-          // so one warpgroup runs exp2 while the other loads and stores.
-          if (it == 0 && t == 1) ok = wait_bar(smem_u32(&sm.p_full[0]), 0, a.timeout_ns, abort_flag);
+          // so one warpgroup runs exp2 while the other loads and stores.  A parity wait on
+          // p_full[0] is only sound if it begins before tile 0 completes its second step
+          // (parity 0 again).  With q as given both issuers pass the same q_full wait and
+          // tile 1's comes straight here, so it does.  With fused q, tile 1's rows are
+          // released after tile 0's have been rotated and then its own, which already puts
+          // it a phase behind, and the wait could begin too late: it is skipped there.
+          if (it == 0 && t == 1 && !rope.table)
+            ok = wait_bar(smem_u32(&sm.p_full[0]), 0, a.timeout_ns, abort_flag);
           if (ok) s_step(0);
           // Step j: PV_t(j-1) (P_t(j-1) is ready before softmax(j) starts), then
           // S_t(j+1) once softmax t has read S_t(j).
