@@ -78,6 +78,27 @@ def test_prefill_large_scores_rescale():
     assert_close(host(o), host(l), ro, rl, "large logits")
 
 
+def test_prefill_masked_keys_do_not_set_the_row_max():
+    """Rows whose diagonal tile holds masked (future) keys that score over 150 log2 units
+    above every visible key.  A full tile takes its row max from the reducing TMEM load;
+    a diagonal tile must take it over the visible keys only, or every visible
+    probability of these rows would underflow to zero."""
+    sa = require_gpu()
+    lens = [256, 200]
+    data = workloads.make_prefill(9, lens, 8, 1, 64)
+    q = data["q"] & np.uint16(0x7FFF)  # |q|: large positive scores against the keys below
+    k = data["k"].copy()
+    big = np.uint16(0x4180)  # bf16 16.0
+    k[100:128] = big         # sequence 0: future of queries 0..99 inside their diagonal tile
+    k[256 + 150:256 + 200] = big  # sequence 1: future of queries 128..149 in tile 1
+    data = dict(data, q=q, k=k)
+    o, l = _run(sa, data, max(lens), 0.125, True)
+    assert sa.sink_attn_device_status(True) == 0
+    ro, rl = oracle.prefill(data["q"], data["k"], data["v"], data["sinks"], data["cu_seqlens"], 0.125, True)
+    assert np.isfinite(host(l)).all()
+    assert_close(host(o), host(l), ro, rl, "masked large keys")
+
+
 def test_causal_prefill_config_full():
     """4 x 8192 tokens, 64/8 heads, sinks with variance 2: every (token, head) row of
     every sequence against the oracle, element by element."""
