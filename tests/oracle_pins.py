@@ -289,6 +289,29 @@ def pin_causal_counts():
             assert int((p[i] > 0).sum()) == kv_len - q_len + i + 1, (q_len, kv_len, i)
 
 
+def pin_causal_future_independence():
+    """Causal prefill: a query row cannot depend on keys after it, however large their
+    scores.  Rows before the cut c equal the oracle run on the sequence cut at c, after the
+    keys and values from c on are replaced by ones whose scores sit about 3000 nats above
+    every visible score (far past the range of exp in fp64), and the rows from c on, which
+    do see those keys, are dominated by them."""
+    rng = _rng(31)
+    length, c, hq, hkv, d, scale = 24, 13, 4, 2, 16, 0.25
+    q = np.abs(_bf16_floats(rng, (length, hq, d)))
+    k = _bf16_floats(rng, (length, hkv, d))
+    v = _bf16_floats(rng, (length, hkv, d))
+    sinks = rng.standard_normal(hq)
+    k_big, v_big = k.copy(), v.copy()
+    k_big[c:] = 1024.0
+    v_big[c:] = 3.0
+    o_full, l_full = oracle.prefill(q, k_big, v_big, sinks, [0, length], scale, True)
+    o_cut, l_cut = oracle.prefill(q[:c], k[:c], v[:c], sinks, [0, c], scale, True)
+    _close(o_full[:c], o_cut, 1e-12, "rows before the cut")
+    _close(l_full[:c], l_cut, 1e-12, "lse before the cut")
+    assert np.all(l_full[c:] > 1000.0), "rows after the cut must see the large keys"
+    _close(o_full[c:], np.full_like(o_full[c:], 3.0), 1e-9, "rows after the cut")
+
+
 def pin_row_sampling_paths():
     """The sampled paths (``rows=`` of both prefills, ``batches=`` of decode) return
     exactly the matching entries of the full computation, which the other pins tie
@@ -368,7 +391,7 @@ def pin_merge_limits():
 ALL_PINS = [pin_hand_worked, pin_sdpa_reduction, pin_large_sink_saturates, pin_normalisation,
             pin_single_key_closed_form, pin_identical_keys, pin_split_merge_invariance,
             pin_brute_force_decimal, pin_online_algorithm, pin_paging, pin_gqa_mapping,
-            pin_causal_counts, pin_row_sampling_paths, pin_merge_limits]
+            pin_causal_counts, pin_causal_future_independence, pin_row_sampling_paths, pin_merge_limits]
 
 
 def failing_pins():

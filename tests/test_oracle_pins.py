@@ -57,6 +57,27 @@ def _top_left_causal(q_len, kv_len, causal, rows=None):
     return vis
 
 
+def _max_over_masked(orig, q, k, v, sink, sm_scale, visible, with_sink, rp):
+    # the row max taken over the masked scores as well (the mask applied to the
+    # exponentials afterwards): equal in exact arithmetic, but visible terms underflow
+    # when a masked score is far above them
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    n, L = q.shape[0], k.shape[0]
+    scores = sm_scale * (q @ k.T)
+    x = np.concatenate([scores, np.full((n, 1), float(sink) if with_sink else -np.inf)], axis=1)
+    m = x.max(axis=1, keepdims=True)
+    with np.errstate(over="ignore", under="ignore", invalid="ignore"):
+        e = np.exp(x - m)
+    if visible is not None:
+        e[:, :L] = np.where(visible, e[:, :L], 0.0)
+    z = e.sum(axis=1, keepdims=True)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        p_all = np.where(z > 0, e / np.where(z > 0, z, 1.0), 0.0)
+        lse = (m + np.log(np.where(z > 0, z, 1.0)))[:, 0]
+    out = p_all[:, :L] @ v
+    return (out, lse, p_all[:, :L], p_all[:, L]) if rp else (out, lse)
+
+
 _ORIG_VISIBLE = oracle.visible_keys
 
 
@@ -149,6 +170,7 @@ MUTANTS = {
     "sink_has_value_row": ("attention_with_sink", _mut_attention(_sink_has_value_row)),
     "lse_in_log2": ("attention_with_sink", _mut_attention(_lse_log2)),
     "top_left_causal": ("visible_keys", _top_left_causal),
+    "row_max_over_masked_scores": ("attention_with_sink", _mut_attention(_max_over_masked)),
     "gqa_modulo": ("kv_head_of", _gqa_modulo),
     "split_drops_last_token": ("split_token_ranges", _split_drops_last_token),
     "online_d_starts_at_zero": ("online_sink_attention", _online_d_starts_at_zero),
